@@ -1,0 +1,43 @@
+"""Token-to-expert grouping (oracle; test infrastructure only).
+
+``Mxfp4MoEMethod.apply`` (vLLM quantization/mxfp4 API page) hands the fused-MoE
+kernel ``topk_ids`` and ``topk_weights`` of shape [T, topk]; the kernel groups
+the T*topk (token, slot) pairs by expert before the two grouped GEMMs.  The
+pages give no algorithm for this step; the reading used here is a stable
+counting sort of the flat pair index p = t*topk + k by expert id.  Ids outside
+[0, E) (the ``expert_map`` -1 convention for non-local experts) join no group.
+Duplicate ids in one row are separate pairs.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def route(topk_ids: np.ndarray, E: int):
+    """Group pairs by expert.
+
+    Returns ``(counts int32[E], offsets int32[E+1], sorted_pair int32[P],
+    pair_pos int32[P])``: ``sorted_pair[offsets[e]:offsets[e+1]]`` lists expert
+    e's pairs in ascending flat index; entries past ``offsets[E]`` are -1.
+    ``pair_pos[p]`` is the position of pair p in ``sorted_pair`` (-1 if invalid).
+    """
+    ids = np.asarray(topk_ids).reshape(-1).astype(np.int64)
+    P = ids.size
+    valid = (ids >= 0) & (ids < E)
+    counts = np.bincount(ids[valid], minlength=E).astype(np.int32)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    n_valid = int(offsets[-1])
+    key = np.where(valid, ids, E)
+    order = np.argsort(key, kind="stable")
+    sorted_pair = np.full(P, -1, dtype=np.int32)
+    sorted_pair[:n_valid] = order[:n_valid]
+    pair_pos = np.full(P, -1, dtype=np.int32)
+    pair_pos[order[:n_valid]] = np.arange(n_valid, dtype=np.int32)
+    return counts, offsets, sorted_pair, pair_pos
+
+
+def active_experts(counts: np.ndarray) -> np.ndarray:
+    """Ids of experts that received at least one pair, ascending."""
+    return np.nonzero(np.asarray(counts) > 0)[0].astype(np.int32)
