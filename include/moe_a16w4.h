@@ -143,6 +143,19 @@ int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int
  * into *status and clear it.  Synchronises ``stream``. */
 int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream);
 
+/*
+ * Optional per-kernel timing, for benchmarks.  ``events`` holds 2*n
+ * cudaEvent_t handles created by the caller (n <= 8).  The next
+ * moe_a16w4_mxfp4 / moe_a16w4_int4g32 call made from this host thread records
+ * events[2i] just before and events[2i+1] just after its i-th kernel launch
+ * (i < n) on the call's stream; the hook is then cleared.  Kernel order:
+ * weight-streaming path 0 grouping, 1 gate_up GEMM, 2 down GEMM, 3 combine;
+ * tensor-core path 0 grouping, 1 row gather, 2 gate_up GEMM, 3 down GEMM,
+ * 4 combine.  n = 0 clears the hook.  Returns MOE_ERR_BAD_DIMS for n outside
+ * [0, 8] and MOE_ERR_NULL for a NULL ``events`` with n > 0.
+ */
+int moe_set_timing_events(void* const* events, int32_t n);
+
 /* Static text for a MOE_ERR_* code. */
 const char* moe_error_string(int code);
 

@@ -1,0 +1,143 @@
+"""Python binding of the GB300 A16W4 MoE library (argument marshalling only).
+
+Each function checks tensor placement, dtypes and shapes, allocates outputs
+and the workspace with PyTorch when the caller does not pass them, and calls
+the C ABI of ``libmoe_a16w4.so`` (include/moe_a16w4.h) with raw device
+pointers on the current CUDA stream.  Every computation runs in the
+library's CUDA kernels; there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native
+from ._native import (MOE_ACT_SWIGLU, MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL,  # noqa: F401
+                      MOE_STATUS_WAIT_TIMEOUT, MoeDims, MoeError)
+
+__all__ = [
+    "moe_workspace_bytes", "moe_a16w4_mxfp4", "moe_a16w4_int4g32", "requant_mxfp4_to_int4g32",
+    "moe_route", "moe_read_status", "dims", "MoeError",
+]
+
+
+def _lib():
+    return _native.load()
+
+
+def dims(E: int, H: int, I: int, topk: int, T: int, path: int = MOE_PATH_AUTO) -> MoeDims:
+    return MoeDims(E, H, I, topk, T, MOE_ACT_SWIGLU, path)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def moe_workspace_bytes(d: MoeDims) -> int:
+    return int(_lib().moe_workspace_bytes(ctypes.byref(d)))
+
+
+def _workspace(d: MoeDims, workspace, device):
+    need = moe_workspace_bytes(d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, stream, scale_dtype):
+    T, H = x.shape
+    E, two_i, _ = w13.shape
+    I = two_i // 2
+    topk = topk_ids.shape[1]
+    _need(x, "x", torch.bfloat16, (T, H))
+    _need(topk_ids, "topk_ids", torch.int32, (T, topk))
+    _need(topk_w, "topk_w", torch.float32, (T, topk))
+    _need(w13, "w13", torch.uint8, (E, 2 * I, H // 2))
+    _need(s13, "w13_scale", scale_dtype, (E, 2 * I, H // 32))
+    _need(w2, "w2", torch.uint8, (E, H, I // 2))
+    _need(s2, "w2_scale", scale_dtype, (E, H, I // 32))
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, (T, H))
+    d = dims(E, H, I, topk, T, path)
+    workspace = _workspace(d, workspace, x.device)
+    rc = getattr(_lib(), fn_name)(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13),
+                                  _ptr(w2), _ptr(s2), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _native.check(fn_name, rc)
+    return out
+
+
+def moe_a16w4_mxfp4(x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out=None, workspace=None,
+                    path: int = MOE_PATH_AUTO, stream=None):
+    """Fused MoE on MXFP4 weights (uint8 packed E2M1 + uint8 E8M0 scales)."""
+    return _moe("moe_a16w4_mxfp4", x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, workspace, path,
+                stream, torch.uint8)
+
+
+def moe_a16w4_int4g32(x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out=None, workspace=None,
+                      path: int = MOE_PATH_AUTO, stream=None):
+    """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 scales)."""
+    return _moe("moe_a16w4_int4g32", x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out, workspace, path,
+                stream, torch.float32)
+
+
+def requant_mxfp4_to_int4g32(w, scale, out_q=None, out_s=None, experts_per_chunk: int = 8, stream=None):
+    """Lossy MXFP4 -> int4_per_group_32 conversion; returns ``(q uint8, s float32)``."""
+    E, N, Kh = w.shape
+    K = 2 * Kh
+    _need(w, "w", torch.uint8, (E, N, Kh))
+    _need(scale, "scale", torch.uint8, (E, N, K // 32))
+    if out_q is None:
+        out_q = torch.empty_like(w)
+    if out_s is None:
+        out_s = torch.empty((E, N, K // 32), dtype=torch.float32, device=w.device)
+    _need(out_q, "out_q", torch.uint8, (E, N, Kh))
+    _need(out_s, "out_s", torch.float32, (E, N, K // 32))
+    rc = _lib().requant_mxfp4_to_int4g32(E, N, K, _ptr(w), _ptr(scale), _ptr(out_q), _ptr(out_s),
+                                         experts_per_chunk, _stream(stream))
+    _native.check("requant_mxfp4_to_int4g32", rc)
+    return out_q, out_s
+
+
+def moe_route(topk_ids, E: int, stream=None):
+    """Stable grouping of the pairs by expert: ``(counts, offsets, sorted_pair, pair_pos)``."""
+    T, topk = topk_ids.shape
+    _need(topk_ids, "topk_ids", torch.int32, (T, topk))
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    pos = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    d = dims(E, 64, 64, topk, T)
+    rc = _lib().moe_route(ctypes.byref(d), _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(sp), _ptr(pos),
+                          _stream(stream))
+    _native.check("moe_route", rc)
+    return counts, offsets, sp, pos
+
+
+def moe_read_status(d: MoeDims, workspace, stream=None) -> int:
+    """Read and clear the device status word of a workspace (synchronises the stream)."""
+    v = ctypes.c_uint32(0)
+    rc = _lib().moe_read_status(ctypes.byref(d), _ptr(workspace), ctypes.byref(v), _stream(stream))
+    _native.check("moe_read_status", rc)
+    return int(v.value)

@@ -1,0 +1,263 @@
+// C ABI entry points: argument checks, workspace layout, kernel sequencing.
+#include <stdio.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+struct TimingHook {
+  cudaEvent_t ev[16];
+  int n = 0;
+};
+thread_local TimingHook g_timing;
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// The library is built for sm_103a only.
+int check_device(int* num_sms) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
+  if (num_sms && cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+RouteOut route_view(uint8_t* ws, const Workspace& L) {
+  RouteOut r;
+  r.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  r.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  r.active = reinterpret_cast<int32_t*>(ws + L.active);
+  r.n_active = reinterpret_cast<int32_t*>(ws + L.n_active);
+  r.sorted_pair = reinterpret_cast<int32_t*>(ws + L.sorted_pair);
+  r.pair_pos = reinterpret_cast<int32_t*>(ws + L.pair_pos);
+  r.mtiles = reinterpret_cast<int32_t*>(ws + L.mtiles);
+  r.n_mtiles = reinterpret_cast<int32_t*>(ws + L.n_mtiles);
+  return r;
+}
+
+int common_checks(const moe_dims_t* d, const void* x, const int32_t* ids, const float* tw, const void* w13,
+                  const void* s13, const void* w2, const void* s2, void* out, void* ws, size_t ws_bytes,
+                  WeightKind kind) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED_ACT;
+  if (!dims_valid(d)) return MOE_ERR_BAD_DIMS;
+  if (kind == WeightKind::kInt4 && d->path == MOE_PATH_PREFILL) return MOE_ERR_BAD_DIMS;
+  if (d->path == MOE_PATH_PREFILL && !use_prefill(d, kind)) return MOE_ERR_BAD_DIMS;
+  if (d->T == 0) return MOE_OK;
+  if (!x || !ids || !tw || !w13 || !s13 || !w2 || !s2 || !out || !ws) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(s13, 16) || !aligned(w2, 16) || !aligned(s2, 16) ||
+      !aligned(out, 16) || !aligned(ws, 256) || !aligned(ids, 4) || !aligned(tw, 4))
+    return MOE_ERR_ALIGN;
+  if (ws_bytes < workspace_layout(d, kind).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float* tw, const uint8_t* w13,
+            const void* s13, const uint8_t* w2, const void* s2, void* out, void* workspace, size_t ws_bytes,
+            void* stream, WeightKind kind) {
+  int rc = common_checks(d, x, ids, tw, w13, s13, w2, s2, out, workspace, ws_bytes, kind);
+  if (rc != MOE_OK || d->T == 0) return rc;
+  int sms = 0;
+  rc = check_device(&sms);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Workspace L = workspace_layout(d, kind);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  const RouteOut r = route_view(ws, L);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+
+  timing_mark(0, false, s);
+  if (launch_route(ids, d->E, d->T, d->topk, r, L.prefill ? 1 : 0, s) != cudaSuccess) return MOE_ERR_CUDA;
+  timing_mark(0, true, s);
+  cudaError_t e;
+  if (L.prefill) {
+    PrefillArgs a{};
+    a.E = d->E; a.H = d->H; a.I = d->I; a.topk = d->topk; a.T = d->T;
+    a.x = x; a.topk_w = tw; a.topk_ids = ids;
+    a.w13 = w13; a.w13_s = reinterpret_cast<const uint8_t*>(s13);
+    a.w2 = w2; a.w2_s = reinterpret_cast<const uint8_t*>(s2);
+    a.out = out; a.route = r;
+    a.xs = ws + L.xs; a.as = ws + L.as;
+    a.outacc = reinterpret_cast<float*>(ws + L.outacc);
+    a.status = status; a.num_sms = sms;
+    e = launch_prefill(a, s);
+  } else {
+    DecodeArgs a{};
+    a.kind = kind;
+    a.E = d->E; a.H = d->H; a.I = d->I; a.topk = d->topk; a.T = d->T;
+    a.x = x; a.topk_w = tw; a.topk_ids = ids;
+    a.w13 = w13; a.w13_s = s13; a.w2 = w2; a.w2_s = s2;
+    a.out = out; a.route = r;
+    a.abuf = reinterpret_cast<float*>(ws + L.abuf);
+    a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
+    a.status = status; a.num_sms = sms;
+    e = launch_decode(a, s);
+  }
+  g_timing.n = 0;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+void timing_mark(int index, bool end, cudaStream_t s) {
+  if (index < g_timing.n) cudaEventRecord(g_timing.ev[2 * index + (end ? 1 : 0)], s);
+}
+
+bool dims_valid(const moe_dims_t* d) {
+  if (!d) return false;
+  if (d->E < 1 || d->E > kMaxExperts) return false;
+  if (d->H < 64 || d->H > 8192 || d->H % 64) return false;
+  if (d->I < 64 || d->I > 8192 || d->I % 64) return false;
+  if (d->topk < 1 || d->topk > 64) return false;
+  if (d->T < 0 || (long long)d->T * d->topk > (1ll << 24)) return false;
+  if (d->path < MOE_PATH_AUTO || d->path > MOE_PATH_PREFILL) return false;
+  return true;
+}
+
+bool use_prefill(const moe_dims_t* d, WeightKind kind) {
+  if (kind != WeightKind::kMxfp4) return false;
+  const bool ok = (d->H % 512 == 0) && (d->I % 512 == 0) && kPrefillAvailable;
+  if (d->path == MOE_PATH_PREFILL) return ok;
+  if (d->path == MOE_PATH_DECODE) return false;
+  return ok && d->T >= kPrefillMinTokens;
+}
+
+Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
+  Workspace L{};
+  const size_t E = d->E, P = (size_t)d->T * d->topk, H = d->H, I = d->I, T = d->T;
+  L.prefill = use_prefill(d, kind);
+  size_t o = 0;
+  L.status = o; o = align256(o + 256);
+  L.counts = o; o = align256(o + 4 * E);
+  L.offsets = o; o = align256(o + 4 * (E + 1));
+  L.active = o; o = align256(o + 4 * E);
+  L.n_active = o; o = align256(o + 4);
+  L.sorted_pair = o; o = align256(o + 4 * P);
+  L.pair_pos = o; o = align256(o + 4 * P);
+  L.mtiles = o; o = align256(o + 4 * (P / kTcM + E + 1));
+  L.n_mtiles = o; o = align256(o + 4);
+  if (L.prefill) {
+    L.xs = o; o = align256(o + 2 * P * H);
+    L.as = o; o = align256(o + 2 * P * I);
+    L.outacc = o; o = align256(o + 4 * T * H);
+  } else {
+    L.abuf = o; o = align256(o + 4 * P * I);
+    L.ybuf = o; o = align256(o + 4 * P * H);
+  }
+  L.total = o;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_dims_t* d) {
+  if (!dims_valid(d)) return 0;
+  return workspace_layout(d, WeightKind::kMxfp4).total > workspace_layout(d, WeightKind::kInt4).total
+             ? workspace_layout(d, WeightKind::kMxfp4).total
+             : workspace_layout(d, WeightKind::kInt4).total;
+}
+
+int moe_a16w4_mxfp4(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                    const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                    void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_moe(d, x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, workspace, workspace_bytes, stream,
+                 WeightKind::kMxfp4);
+}
+
+int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                      const uint8_t* w13_q, const float* w13_s, const uint8_t* w2_q, const float* w2_s, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return run_moe(d, x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out, workspace, workspace_bytes, stream,
+                 WeightKind::kInt4);
+}
+
+int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale,
+                             uint8_t* out_q, float* out_s, int32_t experts_per_chunk, void* stream) {
+  if (E < 1 || N < 1 || K < 32 || K % 32 || experts_per_chunk < 1) return MOE_ERR_BAD_DIMS;
+  if (!w || !scale || !out_q || !out_s) return MOE_ERR_NULL;
+  if (!aligned(w, 16) || !aligned(out_q, 16) || !aligned(out_s, 16)) return MOE_ERR_ALIGN;
+  const int rc = check_device(nullptr);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long groups_per_expert = (long long)N * (K / 32);
+  for (int lo = 0; lo < E; lo += experts_per_chunk) {
+    const int hi = lo + experts_per_chunk < E ? lo + experts_per_chunk : E;
+    const long long g0 = (long long)lo * groups_per_expert;
+    if (launch_requant(w + g0 * 16, scale + g0, out_q + g0 * 16, out_s + g0, (long long)(hi - lo) * groups_per_expert,
+                       s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+              int32_t* sorted_pair, int32_t* pair_pos, void* stream) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->E < 1 || d->E > kMaxExperts || d->topk < 1 || d->topk > 64 || d->T < 0 ||
+      (long long)d->T * d->topk > (1ll << 24))
+    return MOE_ERR_BAD_DIMS;
+  if (!counts || !offsets) return MOE_ERR_NULL;
+  if (d->T > 0 && (!topk_ids || !sorted_pair || !pair_pos)) return MOE_ERR_NULL;
+  const int rc = check_device(nullptr);
+  if (rc != MOE_OK) return rc;
+  // Only the four grouping outputs are requested; the kernel skips the
+  // auxiliary lists when their pointers are null.
+  RouteOut r{};
+  r.counts = counts;
+  r.offsets = offsets;
+  r.sorted_pair = sorted_pair;
+  r.pair_pos = pair_pos;
+  if (launch_route(topk_ids, d->E, d->T, d->topk, r, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream) {
+  if (!d || !workspace || !status) return MOE_ERR_NULL;
+  if (!dims_valid(d)) return MOE_ERR_BAD_DIMS;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(v), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+int moe_set_timing_events(void* const* events, int32_t n) {
+  if (n < 0 || n > 8) return MOE_ERR_BAD_DIMS;
+  if (n > 0 && !events) return MOE_ERR_NULL;
+  for (int i = 0; i < 2 * n; ++i) g_timing.ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+  g_timing.n = n;
+  return MOE_OK;
+}
+
+const char* moe_error_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_BAD_DIMS: return "unsupported problem size";
+    case MOE_ERR_ALIGN: return "pointer not aligned as documented";
+    case MOE_ERR_UNSUPPORTED_ACT: return "unsupported activation (only SwiGLU is implemented)";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE: return "device is not a compute capability 10.3 GPU";
+    default: return "unknown error";
+  }
+}
+
+int moe_abi_version(void) { return 100; }
+
+}  // extern "C"

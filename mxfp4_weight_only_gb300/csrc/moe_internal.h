@@ -1,0 +1,105 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_a16w4.h"
+
+namespace moe {
+
+constexpr uint32_t kStatusWaitTimeout = MOE_STATUS_WAIT_TIMEOUT;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+constexpr int kMaxExperts = 1024;
+constexpr int kRouteThreads = 1024;
+
+// Tokens at or above which MOE_PATH_AUTO picks the tensor-core kernels.
+constexpr int kPrefillMinTokens = 64;
+// Whether the tensor-core (prefill) kernels are built into this library.
+constexpr bool kPrefillAvailable = false;
+
+// Prefill tile sizes (tcgen05, cta_group::1).
+constexpr int kTcM = 128;  // rows of x per M tile
+constexpr int kTcN = 128;  // weight rows per N tile
+constexpr int kTcK = 64;   // K per pipeline step (one 128-byte swizzle row of bf16)
+
+enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
+
+// Byte offsets of the workspace regions for one problem.
+struct Workspace {
+  size_t status, counts, offsets, active, n_active, sorted_pair, pair_pos, mtiles, n_mtiles;
+  size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
+  size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 [P][I], f32 [T][H]
+  size_t total;
+  bool prefill;
+};
+
+bool dims_valid(const moe_dims_t* d);
+bool use_prefill(const moe_dims_t* d, WeightKind kind);
+Workspace workspace_layout(const moe_dims_t* d, WeightKind kind);
+
+// Device view of the routing result inside a workspace.
+struct RouteOut {
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  int32_t* active;       // [E] ids of experts with >= 1 pair, ascending
+  int32_t* n_active;     // [1]
+  int32_t* sorted_pair;  // [P]
+  int32_t* pair_pos;     // [P]
+  int32_t* mtiles;       // [max_mtiles] (expert << 20 | first row / kTcM) for the tensor-core path
+  int32_t* n_mtiles;     // [1]
+};
+
+// Benchmark timing hook (moe_set_timing_events): record the caller's event
+// before (end = false) or after (end = true) kernel ``index`` of this call.
+void timing_mark(int index, bool end, cudaStream_t s);
+
+cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const RouteOut& r, int make_mtiles,
+                         cudaStream_t s);
+
+cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, float* out_s,
+                           long long n_groups, cudaStream_t s);
+
+struct DecodeArgs {
+  WeightKind kind;
+  int E, H, I, topk, T;
+  const void* x;          // bf16 [T][H]
+  const float* topk_w;    // [T][topk]
+  const int32_t* topk_ids;
+  const uint8_t* w13;     // packed [E][2I][H/2]
+  const void* w13_s;      // u8 or f32 [E][2I][H/32]
+  const uint8_t* w2;      // packed [E][H][I/2]
+  const void* w2_s;       // u8 or f32 [E][H][I/32]
+  void* out;              // bf16 [T][H]
+  RouteOut route;
+  float* abuf;            // [P][I], rows by sorted position
+  float* ybuf;            // [P][H], rows by flat pair index
+  uint32_t* status;
+  int num_sms;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+struct PrefillArgs {
+  int E, H, I, topk, T;
+  const void* x;
+  const float* topk_w;
+  const int32_t* topk_ids;
+  const uint8_t* w13;
+  const uint8_t* w13_s;
+  const uint8_t* w2;
+  const uint8_t* w2_s;
+  void* out;
+  RouteOut route;
+  void* xs;       // bf16 [P][H]
+  void* as;       // bf16 [P][I]
+  float* outacc;  // f32 [T][H]
+  uint32_t* status;
+  int num_sms;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,147 @@
+// MXFP4 -> int4_per_group_32 requantisation (load time, lossy, opt-in).
+//
+// Follows Mxfp4MoEMethod._setup_kernel_k3_situ_gfx942 (vLLM quantization/mxfp4
+// API page): decode E2M1 elements and the E8M0 block scale, multiply, cast to
+// bf16 (exact for these values), then symmetric int4 per 32-group with
+//   scale = fl32(amax / 7),  q = round_half_even(fl32(w / scale)), q in [-8, 7],
+// an all-zero group giving scale 0 and q 0.
+//
+// One thread per 32-group: 16 bytes in, one scale byte in, 16 bytes and one
+// float out, all coalesced.  HBM-bound.  Division-free fast path: inside the
+// normal float32 range every element is c * 2^(s-127) and the group maximum is
+// cmax * 2^(s-127), so fl32(w / fl32(amax / 7)) equals
+// fl32(c / fl32(cmax / 7)) -- the power of two cancels exactly.  The quotient
+// therefore depends only on the two codes, and a 8x8 table of q, built with
+// the same IEEE round-to-nearest divisions at kernel start, replaces the 32
+// divisions.  Groups whose scale byte puts values near the subnormal range or
+// near overflow take the per-element division path, so results are bit-exact
+// for every scale byte in [0, 252].
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRequantThreads = 256;
+// Scale bytes inside which the table path is exact (values, amax/7 and the
+// quotients are normal float32 numbers and nothing overflows).
+constexpr uint32_t kFastLo = 8, kFastHi = 250;
+
+// Magnitude of an E2M1 code (low 3 bits): exponent field e = c>>1 (bias 1),
+// mantissa bit c&1; e = 0 is the subnormal 0.5 * mantissa.
+__device__ __forceinline__ float e2m1_mag(uint32_t c) {
+  c &= 7u;
+  const uint32_t normal = (((c >> 1) + 126u) << 23) | ((c & 1u) << 22);
+  return __uint_as_float(c >= 2u ? normal : (c ? 0x3F000000u : 0u));
+}
+
+// 4 output bytes (int4 codes of elements 0..3 of ``sel`` nibbles) via byte permutes.
+// pos/neg: 8-entry tables (two words each) of q and (-q)&15 by magnitude code.
+__device__ __forceinline__ uint32_t lookup4(uint32_t nib4, uint32_t pos0, uint32_t pos1, uint32_t neg0,
+                                            uint32_t neg1) {
+  const uint32_t mags = nib4 & 0x7777u;
+  const uint32_t a = prmt(pos0, pos1, mags);
+  const uint32_t b = prmt(neg0, neg1, mags);
+  // selector (sign bit, index 4): sign 0 copies byte 4 (0x80), sign 1 replicates its
+  // top bit (0xFF): a per-byte select mask for the negated values.
+  const uint32_t ssel = (nib4 & 0x8888u) | 0x4444u;
+  const uint32_t m = prmt(0u, 0x80808080u, ssel);
+  return (a & ~m) | (b & m);
+}
+
+// bytes [q0 q1 q2 q3] (each < 16) -> 16-bit value q0 | q1<<4 | q2<<8 | q3<<12 (in bytes 0 and 2)
+__device__ __forceinline__ uint32_t squeeze(uint32_t q4) { return q4 | (q4 >> 4); }
+
+__global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t* __restrict__ w,
+                                                                  const uint8_t* __restrict__ scale,
+                                                                  uint8_t* __restrict__ out_q,
+                                                                  float* __restrict__ out_s,
+                                                                  long long n_groups) {
+  __shared__ uint4 lut[8];  // per cmax: q by code (2 words), (-q)&15 by code (2 words)
+  if (threadIdx.x < 8) {
+    const uint32_t cm = threadIdx.x;
+    uint32_t pos[2] = {0, 0}, neg[2] = {0, 0};
+    if (cm > 0) {
+      const float sc = __fdiv_rn(e2m1_mag(cm), 7.0f);
+      for (uint32_t c = 0; c < 8; ++c) {
+        int q = __float2int_rn(__fdiv_rn(e2m1_mag(c), sc));
+        q = min(max(q, -8), 7);
+        pos[c >> 2] |= uint32_t(q & 0xF) << (8 * (c & 3));
+        neg[c >> 2] |= uint32_t((-q) & 0xF) << (8 * (c & 3));
+      }
+    }
+    lut[cm] = make_uint4(pos[0], pos[1], neg[0], neg[1]);
+  }
+  __syncthreads();
+
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups; g += stride) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(w) + g);
+    const uint32_t s = scale[g];
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    // largest magnitude code in the group
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t mg = wd[i] & 0x77777777u;
+      m = __vmaxu4(m, __vmaxu4(mg & 0x0F0F0F0Fu, (mg >> 4) & 0x0F0F0F0Fu));
+    }
+    m = __vmaxu4(m, m >> 16);
+    m = __vmaxu4(m, m >> 8);
+    const uint32_t cmax = m & 0xFu;
+    const float sc_unit = e8m0_to_float(s);
+    uint32_t oq[4];
+    float oscale;
+    if (cmax == 0) {
+      oq[0] = oq[1] = oq[2] = oq[3] = 0u;
+      oscale = 0.f;
+    } else if (s >= kFastLo && s <= kFastHi) {
+      oscale = __fdiv_rn(e2m1_mag(cmax) * sc_unit, 7.0f);
+      const uint4 t = lut[cmax];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = squeeze(lookup4(wd[i], t.x, t.y, t.z, t.w));
+        const uint32_t hi = squeeze(lookup4(wd[i] >> 16, t.x, t.y, t.z, t.w));
+        oq[i] = prmt(lo, hi, 0x6420u);
+      }
+    } else {
+      // exact per-element path (values near the subnormal range or near overflow)
+      const float amax = e2m1_mag(cmax) * sc_unit;
+      oscale = __fdiv_rn(amax, 7.0f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t r = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t c = (wd[i] >> (4 * j)) & 0xFu;
+          float val = e2m1_mag(c) * sc_unit;
+          val = (c & 8u) ? -val : val;
+          int q = oscale > 0.f ? __float2int_rn(__fdiv_rn(val, oscale)) : 0;
+          q = min(max(q, -8), 7);
+          r |= uint32_t(q & 0xF) << (4 * j);
+        }
+        oq[i] = r;
+      }
+    }
+    __stcs(reinterpret_cast<uint4*>(out_q) + g, make_uint4(oq[0], oq[1], oq[2], oq[3]));
+    __stcs(out_s + g, oscale);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, float* out_s,
+                           long long n_groups, cudaStream_t s) {
+  if (n_groups <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long want = (n_groups + kRequantThreads - 1) / kRequantThreads;
+  const int grid = (int)(want < (long long)sms * 8 ? want : (long long)sms * 8);
+  requant_kernel<<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,135 @@
+// Token -> expert grouping: a stable counting sort of the T*topk (token, slot)
+// pairs by expert id, in one CTA.
+//
+// The fused MoE call of Mxfp4MoEMethod.apply (vLLM quantization/mxfp4 API page)
+// receives topk_ids[T, topk]; the grouped GEMMs need each expert's pairs
+// contiguous.  Pairs keep ascending flat index p = t*topk + k inside each
+// expert, ids outside [0, E) are dropped.  Besides counts/offsets/order this
+// kernel emits the list of active experts (weight-streaming kernels iterate
+// over it) and, on request, the list of 128-row M tiles per expert for the
+// tensor-core kernels.
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+// Exclusive scan of one value per thread over a 1024-thread CTA.
+// ``scratch`` holds 32 ints.  Returns the exclusive prefix; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = scratch[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += y;
+    }
+    scratch[lane] = si - s;  // exclusive prefix of warp sums
+    if (lane == 31) scratch[32] = si;
+  }
+  __syncthreads();
+  const int r = incl - v + scratch[warp];
+  *total = scratch[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const int32_t* __restrict__ ids, int E, int P, RouteOut r, int make_mtiles) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;           // [E]
+  int32_t* base = sm + E;      // [E]
+  int32_t* wcnt = sm + 2 * E;  // [32][E]
+  __shared__ int scratch[33];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int p = tid; p < P; p += kRouteThreads) {
+    const int e = ids[p];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+
+  int total = 0;
+  const int v = tid < E ? cnt[tid] : 0;
+  const int excl = block_excl_scan(v, scratch, &total);
+  if (tid < E) {
+    r.counts[tid] = v;
+    r.offsets[tid] = excl;
+    base[tid] = excl;
+  }
+  if (tid == 0) r.offsets[E] = total;
+  const int n_valid = total;
+
+  int n_act = 0;
+  const int apos = block_excl_scan(v > 0 ? 1 : 0, scratch, &n_act);
+  if (r.active) {
+    if (tid < E && v > 0) r.active[apos] = tid;
+    if (tid == 0) *r.n_active = n_act;
+  }
+
+  if (make_mtiles) {
+    const int nt = (v + kTcM - 1) / kTcM;
+    int n_tiles = 0;
+    const int tpos = block_excl_scan(nt, scratch, &n_tiles);
+    for (int i = 0; i < nt; ++i) r.mtiles[tpos + i] = (tid << 20) | i;
+    if (tid == 0) *r.n_mtiles = n_tiles;
+  }
+  __syncthreads();
+
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < P; c0 += kRouteThreads) {
+    for (int i = tid; i < 32 * E; i += kRouteThreads) wcnt[i] = 0;
+    const int p = c0 + tid;
+    const int e = p < P ? ids[p] : -1;
+    const bool valid = p < P && (unsigned)e < (unsigned)E;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int rank = __popc(peers & lt_mask);
+    if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    int run = 0;
+    if (tid < E) {
+      for (int w = 0; w < 32; ++w) {
+        const int t = wcnt[w * E + tid];
+        wcnt[w * E + tid] = run;
+        run += t;
+      }
+    }
+    __syncthreads();
+    if (valid) {
+      const int pos = base[e] + wcnt[warp * E + e] + rank;
+      r.sorted_pair[pos] = p;
+      r.pair_pos[p] = pos;
+    } else if (p < P) {
+      r.pair_pos[p] = -1;
+    }
+    __syncthreads();
+    if (tid < E) base[tid] += run;
+  }
+  for (int i = n_valid + tid; i < P; i += kRouteThreads) r.sorted_pair[i] = -1;
+}
+
+}  // namespace
+
+cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const RouteOut& r, int make_mtiles,
+                         cudaStream_t s) {
+  const size_t smem = (size_t)34 * E * sizeof(int32_t);
+  cudaError_t err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  route_kernel<<<1, kRouteThreads, smem, s>>>(topk_ids, E, T * topk, r, make_mtiles);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
