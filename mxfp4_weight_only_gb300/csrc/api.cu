@@ -35,6 +35,7 @@ RouteOut route_view(uint8_t* ws, const Workspace& L) {
   r.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   r.active = reinterpret_cast<int32_t*>(ws + L.active);
   r.n_active = reinterpret_cast<int32_t*>(ws + L.n_active);
+  r.gprefix = reinterpret_cast<int32_t*>(ws + L.gprefix);
   r.sorted_pair = reinterpret_cast<int32_t*>(ws + L.sorted_pair);
   r.pair_pos = reinterpret_cast<int32_t*>(ws + L.pair_pos);
   r.mtiles = reinterpret_cast<int32_t*>(ws + L.mtiles);
@@ -107,7 +108,8 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
 }  // namespace
 
 void timing_mark(int index, bool end, cudaStream_t s) {
-  if (index < g_timing.n) cudaEventRecord(g_timing.ev[2 * index + (end ? 1 : 0)], s);
+  // External records also become event nodes when the stream is being captured.
+  if (index < g_timing.n) cudaEventRecordWithFlags(g_timing.ev[2 * index + (end ? 1 : 0)], s, cudaEventRecordExternal);
 }
 
 bool dims_valid(const moe_dims_t* d) {
@@ -139,6 +141,7 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.offsets = o; o = align256(o + 4 * (E + 1));
   L.active = o; o = align256(o + 4 * E);
   L.n_active = o; o = align256(o + 4);
+  L.gprefix = o; o = align256(o + 4 * (E + 1));
   L.sorted_pair = o; o = align256(o + 4 * P);
   L.pair_pos = o; o = align256(o + 4 * P);
   L.mtiles = o; o = align256(o + 4 * (P / kTcM + E + 1));

@@ -9,43 +9,51 @@
 //   gemm2:  y = W2[e] a  -> ybuf (fp32, rows by flat pair index)
 //   combine: out[t] = bf16( sum_k topk_w[t,k] * y[t*topk + k] ), k ascending.
 //
-// Work item = (active expert, 16 weight rows x all of K).  For gemm1 the 16
-// rows are 8 gate rows j..j+7 and the matching 8 up rows I+j.., so the
-// activation is local to the item.  Items are split into one contiguous run
-// per CTA (one CTA per SM, persistent); consecutive items of one CTA share an
-// expert, so its activations stay in registers across items.
+// Work unit = (active expert, group of up to 8 of its pairs, 32 weight rows x
+// all of K).  For gemm1 the 32 rows are 16 gate rows j..j+15 and the matching
+// 16 up rows I+j.., so the activation is local to the unit.  Units are split
+// into one contiguous run per CTA (one CTA per SM, persistent); consecutive
+// units of one CTA share an expert and group, so its activations stay in
+// registers across units.
 //
-// Per CTA: one producer warp streams each item's 16 weight rows (row-wise
-// cp.async.bulk into a padded shared-memory stage, conflict-free for the
-// consumers) and their scales through an mbarrier ring.  Fifteen consumer
-// warps split K (16 warps per CTA: four per SM sub-partition); each turns its part of the packed rows into m16n8k16 f16 MMA
-// operands (E2M1 pairs via cvt.rn.f16x2.e2m1x2, exact; int4 pairs via the
-// 1024-offset f16 trick, exact), multiplies by up to 8 activation columns, and
-// applies the per-32-block weight scale to each block's fp32 partial sum.
-// Activations enter the MMA as f16 scaled by a power of two per (pair, warp
-// K-range) so they cannot overflow; the scale is removed in fp32 afterwards.
-// Partial sums of the consumer warps are reduced through shared memory.
+// Per CTA (8 warps): one producer warp streams each item's 32 weight rows
+// (one cp.async.bulk per row into a padded shared-memory stage, so consumer
+// reads are bank-conflict-free) and their scales through an mbarrier ring.
+// Seven consumer warps split K.  Each turns its part of the packed rows into
+// m16n8k16 f16 MMA operands (E2M1 pairs via cvt.rn.f16x2.e2m1x2, exact; int4
+// pairs via the 1024-offset f16 trick, exact) and multiplies them by up to 8
+// activation columns held in registers; the per-32-block weight scale is
+// applied to each block's fp32 partial sum (E8M0 pairs decoded with
+// cvt.rn.bf16x2.ue8m0x2, exact).  Activations enter the MMA as f16 scaled by a
+// power of two per (pair, warp K-range) so they cannot overflow; the scale is
+// removed in fp32 afterwards.  Partial sums of the consumer warps are reduced
+// through shared memory.
 #include "common.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kConsumerWarps = 15;
+constexpr int kConsumerWarps = 7;
 constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRows = 16;          // weight rows per item
-constexpr int kCols = 8;           // pairs per MMA column group
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kTiles = 2;             // 16-row MMA tiles per item
+constexpr int kRows = 16 * kTiles;    // weight rows per item
+constexpr int kGroup = 8;             // pair columns per group (one 8-column MMA block)
+constexpr int kRedFloats = kConsumerWarps * kRows * kGroup;  // one reduction buffer
+static_assert(kGroup == kMoeGroup, "routing and the decode kernels must agree on the group size");
 constexpr int kSmemBudget = 220 * 1024;
 
 struct GemmParams {
   const uint8_t* w;        // packed weights [E][N][K/2]
   const void* ws;          // scales [E][N][K/32], u8 (E8M0) or f32
   int N, K, I;             // rows per expert, reduction size, I (gate/up split for gemm1)
-  int tiles;               // items per expert
+  int tiles;               // weight tiles per expert
   const void* src;         // gemm1: x bf16 [T][K]; gemm2: abuf f32 [P][K]
   const int32_t* offsets;
   const int32_t* active;
   const int32_t* n_active;
+  const int32_t* gprefix;  // [n_active+1] exclusive prefix of 8-pair groups over active experts
   const int32_t* sorted_pair;
   int topk;
   float* dst;              // gemm1: abuf [P][I]; gemm2: ybuf [P][N]
@@ -74,9 +82,18 @@ __device__ __forceinline__ void int4x8_to_f16x8(uint32_t w, uint32_t& o0, uint32
   o3 = f16x2_sub(((u >> 12) & 0x000F000Fu) | magic, bias);
 }
 
+// Two E8M0 bytes (low byte = first) -> their values 2^(s-127) as floats, exact
+// (bf16 keeps the full exponent range, including 2^-127).
+__device__ __forceinline__ void e8m0x2_to_float2(uint32_t two_bytes, float& lo, float& hi) {
+  uint32_t r;
+  asm("{\n .reg .b16 b;\n cvt.u16.u32 b, %1;\n cvt.rn.bf16x2.ue8m0x2 %0, b;\n}" : "=r"(r) : "r"(two_bytes));
+  lo = __uint_as_float(r << 16);
+  hi = __uint_as_float(r & 0xFFFF0000u);
+}
+
 template <bool GATE_UP>
 __device__ __forceinline__ int item_row(int r, int j, int I) {
-  if (GATE_UP) return r < 8 ? 8 * j + r : I + 8 * j + (r - 8);
+  if (GATE_UP) return r < kRows / 2 ? (kRows / 2) * j + r : I + (kRows / 2) * j + (r - kRows / 2);
   return kRows * j + r;
 }
 
@@ -94,6 +111,91 @@ __device__ __forceinline__ void load8(const void* row, int k0, float (&v)[8]) {
   }
 }
 
+// Activation fragments of one 8-pair column block (pairs slot0 + g, g = lane/4)
+// over the calling warp's blocks [wb0, wb0 + cnt), as f16 scaled by a power of
+// two per pair; inv receives the undo factors for accumulator columns 2t, 2t+1.
+template <WeightKind KIND, bool GATE_UP, int NBW>
+__device__ __forceinline__ void load_frags(const GemmParams& p, int slot0, int base, int npairs, int wb0, int cnt,
+                                           int g, int t, uint32_t (&xf)[NBW][4], float (&inv)[2]) {
+  const int slot = slot0 + g;
+  const bool valid = slot < npairs;
+  const void* row = nullptr;
+  if (valid) {
+    if (GATE_UP) {
+      const int tok = p.sorted_pair[base + slot] / p.topk;
+      row = reinterpret_cast<const uint16_t*>(p.src) + (size_t)tok * p.K;
+    } else {
+      row = reinterpret_cast<const float*>(p.src) + (size_t)(base + slot) * p.K;
+    }
+  }
+  float mx = 0.f;
+#pragma unroll
+  for (int bb = 0; bb < NBW; ++bb) {
+    if (valid && bb < cnt) {
+      float v[8];
+      load8<GATE_UP>(row, (wb0 + bb) * 32 + 8 * t, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(v[q]));
+    }
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  int ex = 0;
+  if (mx > 0.f) {
+    const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
+    ex = min(max(14 - lg, -126), 126);
+  }
+  const float sc = exp2_int(ex);
+#pragma unroll
+  for (int bb = 0; bb < NBW; ++bb) {
+    float v[8];
+    if (valid && bb < cnt) {
+      load8<GATE_UP>(row, (wb0 + bb) * 32 + 8 * t, v);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] *= sc;
+    if (KIND == WeightKind::kMxfp4) {
+      xf[bb][0] = f32x2_to_f16x2(v[0], v[1]);
+      xf[bb][1] = f32x2_to_f16x2(v[2], v[3]);
+      xf[bb][2] = f32x2_to_f16x2(v[4], v[5]);
+      xf[bb][3] = f32x2_to_f16x2(v[6], v[7]);
+    } else {
+      xf[bb][0] = f32x2_to_f16x2(v[0], v[4]);
+      xf[bb][1] = f32x2_to_f16x2(v[1], v[5]);
+      xf[bb][2] = f32x2_to_f16x2(v[2], v[6]);
+      xf[bb][3] = f32x2_to_f16x2(v[3], v[7]);
+    }
+  }
+  const int ex0 = __shfl_sync(0xffffffffu, ex, (2 * t) * 4);
+  const int ex1 = __shfl_sync(0xffffffffu, ex, (2 * t + 1) * 4);
+  inv[0] = exp2_int(-ex0);
+  inv[1] = exp2_int(-ex1);
+}
+
+// Scales of rows r and r+8 of one 16-row tile for blocks b, b+1 (b even).
+template <WeightKind KIND>
+__device__ __forceinline__ void load_scales2(const uint8_t* ss, int srow, int r, int b, float (&s)[2][2]) {
+  if (KIND == WeightKind::kMxfp4) {
+    const uint32_t u0 = *reinterpret_cast<const uint16_t*>(ss + r * srow + b);
+    const uint32_t u1 = *reinterpret_cast<const uint16_t*>(ss + (r + 8) * srow + b);
+    e8m0x2_to_float2(u0, s[0][0], s[0][1]);
+    e8m0x2_to_float2(u1, s[1][0], s[1][1]);
+  } else {
+    const float2 f0 = *reinterpret_cast<const float2*>(ss + r * srow + 4 * b);
+    const float2 f1 = *reinterpret_cast<const float2*>(ss + (r + 8) * srow + 4 * b);
+    s[0][0] = f0.x; s[0][1] = f0.y; s[1][0] = f1.x; s[1][1] = f1.y;
+  }
+}
+
+template <WeightKind KIND>
+__device__ __forceinline__ void weights_to_f16(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  if (KIND == WeightKind::kMxfp4) e2m1x8_to_f16x8(w, o0, o1, o2, o3);
+  else int4x8_to_f16x8(w, o0, o1, o2, o3);
+}
+
 template <WeightKind KIND, bool GATE_UP, int NBW>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -103,8 +205,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   uint64_t* empty = full + S;
   uint64_t* redbar = empty + S;  // [2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(redbar + 2);
-  float* red = reinterpret_cast<float*>(smem + 1024);  // [2][warps][16][8]
-  uint8_t* stages = smem + 1024 + 2 * kConsumerWarps * kRows * kCols * sizeof(float);
+  float* red = reinterpret_cast<float*>(smem + 1024);  // [2][warps][32 rows][16 pair columns]
+  uint8_t* stages = smem + 1024 + 2 * kRedFloats * sizeof(float);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -118,220 +220,179 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   }
   __syncthreads();
 
-  const long long n_items = (long long)(*p.n_active) * p.tiles;
-  const long long i0 = n_items * blockIdx.x / gridDim.x;
-  const long long i1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  // Work units: (active expert d, 8-pair group, weight tile j), group-major
+  // within an expert, so a CTA's contiguous run reloads activations only at
+  // group boundaries.  Experts with more than 8 pairs stream their weights
+  // once per group.
+  const int n_act = *p.n_active;
+  const long long n_units = (long long)p.gprefix[n_act] * p.tiles;
+  const long long u0 = n_units * blockIdx.x / gridDim.x;
+  const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
   const int Kh = p.K >> 1;
   const int nb = p.K >> 5;
+  // first active expert whose units reach u0
+  int d0 = 0;
+  {
+    int lo = 0, hi = n_act;  // largest d with gprefix[d] * tiles <= u0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((long long)p.gprefix[mid] * p.tiles <= u0) lo = mid; else hi = mid;
+    }
+    d0 = lo;
+  }
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
     long long issued = 0;
-    for (long long i = i0; i < i1; ++i, ++issued) {
+    int d = d0;
+    for (long long u = u0; u < u1; ++u, ++issued) {
       if (*abort_flag) break;
+      while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
+      const int j = (int)((u - (long long)p.gprefix[d] * p.tiles) % p.tiles);
       const int stage = (int)(issued % S);
       const long long use = issued / S;
       if (use > 0 && !mbar_wait(&empty[stage], (uint32_t)((use - 1) & 1), p.status)) {
         *abort_flag = 1;
         break;
       }
-      const int d = (int)(i / p.tiles), j = (int)(i % p.tiles);
       const int e = p.active[d];
       uint8_t* sw = stages + (size_t)stage * p.stage_bytes;
       uint8_t* ss = sw + kRows * p.row_stride;
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], kRows * (Kh + p.srow_bytes));
       __syncwarp();
-      if (lane < kRows) {
+      {
         const int row = item_row<GATE_UP>(lane, j, p.I);
         bulk_g2s(sw + lane * p.row_stride, p.w + ((size_t)e * p.N + row) * Kh, Kh, &full[stage], policy);
-      } else if (lane == kRows || (GATE_UP && lane == kRows + 1)) {
-        const int half = lane - kRows;  // gemm1: 0 gate rows, 1 up rows; gemm2: all 16 rows
-        const int rows = GATE_UP ? 8 : kRows;
-        const int row0 = item_row<GATE_UP>(half * 8, j, p.I);
+      }
+      if (lane < (GATE_UP ? 2 : 1)) {
+        // scales: gemm1 gate rows then up rows (each contiguous); gemm2 all rows
+        const int rows = GATE_UP ? kRows / 2 : kRows;
+        const int row0 = item_row<GATE_UP>(lane * (kRows / 2), j, p.I);
         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws) + ((size_t)e * p.N + row0) * p.srow_bytes;
-        bulk_g2s(ss + half * 8 * p.srow_bytes, src, rows * p.srow_bytes, &full[stage], policy);
+        bulk_g2s(ss + lane * (kRows / 2) * p.srow_bytes, src, rows * p.srow_bytes, &full[stage], policy);
       }
     }
     // make sure nothing issued is still in flight before the CTA can exit
     const long long first = issued > S ? issued - S : 0;
-    for (long long u = first; u < issued; ++u)
-      mbar_wait(&full[u % S], (uint32_t)((u / S) & 1), p.status);
+    for (long long v = first; v < issued; ++v)
+      mbar_wait(&full[v % S], (uint32_t)((v / S) & 1), p.status);
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
-  const int nbw = (nb + kConsumerWarps - 1) / kConsumerWarps;
-  const int wb0 = min(nb, warp * nbw), wb1 = min(nb, wb0 + nbw);
-  constexpr bool kSrcBf16 = GATE_UP;
+  // even number of blocks per warp, so blocks are processed in pairs
+  const int nbw = 2 * ((nb + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps));
+  const int wb0 = min(nb, warp * nbw);
+  const int cnt = min(nbw, nb - wb0);
 
   uint32_t xf[NBW][4];
-  float inv0 = 1.f, inv1 = 1.f;  // power-of-two undo for accumulator columns 2t, 2t+1
+  float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1
   int cur_e = -1, cur_grp = -1;
-  long long use_cnt = 0;  // reduction-buffer uses
 
   long long it = 0;
-  for (long long i = i0; i < i1; ++i, ++it) {
+  int d = d0;
+  for (long long u = u0; u < u1; ++u, ++it) {
     if (*abort_flag) break;
+    while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
+    const long long rem = u - (long long)p.gprefix[d] * p.tiles;
+    const int grp = (int)(rem / p.tiles), j = (int)(rem % p.tiles);
     const int stage = (int)(it % S);
-    const int d = (int)(i / p.tiles), j = (int)(i % p.tiles);
     const int e = p.active[d];
     const int base = p.offsets[e];
     const int npairs = p.offsets[e + 1] - base;
-    const int ngroups = (npairs + kCols - 1) / kCols;
+    if (e != cur_e || grp != cur_grp) {
+      load_frags<KIND, GATE_UP, NBW>(p, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
+      cur_e = e;
+      cur_grp = grp;
+    }
     if (!mbar_wait(&full[stage], (uint32_t)((it / S) & 1), p.status)) {
       *abort_flag = 1;
       break;
     }
     const uint8_t* sw = stages + (size_t)stage * p.stage_bytes;
     const uint8_t* ss = sw + kRows * p.row_stride;
-    bool stop = false;
-    for (int grp = 0; grp < ngroups; ++grp) {
-      if (e != cur_e || grp != cur_grp) {
-        // ---- activation fragments for pairs grp*8 .. grp*8+7 over this warp's K range
-        const int slot = grp * kCols + g;
-        const bool valid = slot < npairs;
-        const void* row = nullptr;
-        if (valid) {
-          if (GATE_UP) {
-            const int tok = p.sorted_pair[base + slot] / p.topk;
-            row = reinterpret_cast<const uint16_t*>(p.src) + (size_t)tok * p.K;
-          } else {
-            row = reinterpret_cast<const float*>(p.src) + (size_t)(base + slot) * p.K;
-          }
-        }
-        float mx = 0.f;
-#pragma unroll
-        for (int bb = 0; bb < NBW; ++bb) {
-          const int b = wb0 + bb;
-          if (valid && b < wb1) {
-            float v[8];
-            load8<kSrcBf16>(row, b * 32 + 8 * t, v);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(v[q]));
-          }
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        int ex = 0;
-        if (mx > 0.f) {
-          const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
-          ex = min(max(14 - lg, -126), 126);
-        }
-        const float sc = exp2_int(ex);
-#pragma unroll
-        for (int bb = 0; bb < NBW; ++bb) {
-          const int b = wb0 + bb;
-          float v[8];
-          if (valid && b < wb1) {
-            load8<kSrcBf16>(row, b * 32 + 8 * t, v);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = 0.f;
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] *= sc;
-          if (KIND == WeightKind::kMxfp4) {
-            xf[bb][0] = f32x2_to_f16x2(v[0], v[1]);
-            xf[bb][1] = f32x2_to_f16x2(v[2], v[3]);
-            xf[bb][2] = f32x2_to_f16x2(v[4], v[5]);
-            xf[bb][3] = f32x2_to_f16x2(v[6], v[7]);
-          } else {
-            xf[bb][0] = f32x2_to_f16x2(v[0], v[4]);
-            xf[bb][1] = f32x2_to_f16x2(v[1], v[5]);
-            xf[bb][2] = f32x2_to_f16x2(v[2], v[6]);
-            xf[bb][3] = f32x2_to_f16x2(v[3], v[7]);
-          }
-        }
-        const int ex0 = __shfl_sync(0xffffffffu, ex, (2 * t) * 4);
-        const int ex1 = __shfl_sync(0xffffffffu, ex, (2 * t + 1) * 4);
-        inv0 = exp2_int(-ex0);
-        inv1 = exp2_int(-ex1);
-        cur_e = e;
-        cur_grp = grp;
-      }
 
-      // ---- main loop over this warp's 32-element blocks
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- main loop over this warp's 32-element blocks, two at a time
+    float acc[kTiles][4];
 #pragma unroll
-      for (int bb = 0; bb < NBW; ++bb) {
+    for (int tl = 0; tl < kTiles; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int bb = 0; bb < NBW; bb += 2) {
+      if (bb < cnt) {
         const int b = wb0 + bb;
-        if (b < wb1) {
-          const uint8_t* rg = sw + g * p.row_stride + b * 16 + 4 * t;
-          const uint32_t wg = *reinterpret_cast<const uint32_t*>(rg);
-          const uint32_t wg8 = *reinterpret_cast<const uint32_t*>(rg + 8 * p.row_stride);
-          float sg, sg8;
-          uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-          if (KIND == WeightKind::kMxfp4) {
-            sg = e8m0_to_float(ss[g * p.srow_bytes + b]);
-            sg8 = e8m0_to_float(ss[(g + 8) * p.srow_bytes + b]);
-            e2m1x8_to_f16x8(wg, a0, a1, a2, a3);
-            e2m1x8_to_f16x8(wg8, c0, c1, c2, c3);
-          } else {
-            const float* sf = reinterpret_cast<const float*>(ss);
-            const int spr = p.srow_bytes >> 2;
-            sg = sf[g * spr + b];
-            sg8 = sf[(g + 8) * spr + b];
-            int4x8_to_f16x8(wg, a0, a1, a2, a3);
-            int4x8_to_f16x8(wg8, c0, c1, c2, c3);
-          }
-          float dd[4];
-          mma_f16_16816(dd, a0, c0, a1, c1, xf[bb][0], xf[bb][1], zero);
-          mma_f16_16816(dd, a2, c2, a3, c3, xf[bb][2], xf[bb][3], dd);
-          acc[0] = fmaf(sg, dd[0], acc[0]);
-          acc[1] = fmaf(sg, dd[1], acc[1]);
-          acc[2] = fmaf(sg8, dd[2], acc[2]);
-          acc[3] = fmaf(sg8, dd[3], acc[3]);
-        }
-      }
-      if (grp == ngroups - 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-      }
-
-      // ---- cross-warp reduction and epilogue
-      const int buf = (int)(use_cnt & 1);
-      float* rb = red + buf * (kConsumerWarps * kRows * kCols);
-      float* rw = rb + warp * (kRows * kCols);
-      *reinterpret_cast<float2*>(rw + g * kCols + 2 * t) = make_float2(acc[0] * inv0, acc[1] * inv1);
-      *reinterpret_cast<float2*>(rw + (g + 8) * kCols + 2 * t) = make_float2(acc[2] * inv0, acc[3] * inv1);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&redbar[buf]);
-      // every consumer waits: a warp may only write this buffer again two uses
-      // later, after all warps have arrived at the use in between
-      const bool epi = GATE_UP ? (tid < 64) : (tid < 128);
-      if (!mbar_wait(&redbar[buf], (uint32_t)((use_cnt >> 1) & 1), p.status)) {
-        *abort_flag = 1;
-        stop = true;
-      } else if (epi) {
-        if (GATE_UP) {
-          const int c = tid >> 3, r = tid & 7;
-          float hg = 0.f, hu = 0.f;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            hg += rb[w * kRows * kCols + r * kCols + c];
-            hu += rb[w * kRows * kCols + (r + 8) * kCols + c];
-          }
-          const int slot = grp * kCols + c;
-          if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + 8 * j + r] = silu(hg) * hu;
-        } else {
-          const int c = tid >> 4, r = tid & 15;
-          float y = 0.f;
+        for (int tl = 0; tl < kTiles; ++tl) {
+          const int r = 16 * tl + g;
+          float sc[2][2];  // [row r / r+8][block b / b+1]
+          load_scales2<KIND>(ss, p.srow_bytes, r, b, sc);
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kCols + r * kCols + c];
-          const int slot = grp * kCols + c;
-          if (slot < npairs) {
-            const int pair = p.sorted_pair[base + slot];
-            p.dst[(size_t)pair * p.N + kRows * j + r] = y;
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t* rg = sw + r * p.row_stride + (b + h) * 16 + 4 * t;
+            uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+            weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg), a0, a1, a2, a3);
+            weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg + 8 * p.row_stride), c0, c1, c2, c3);
+            float dd[4];
+            mma_f16_16816(dd, a0, c0, a1, c1, xf[bb + h][0], xf[bb + h][1], zero);
+            mma_f16_16816(dd, a2, c2, a3, c3, xf[bb + h][2], xf[bb + h][3], dd);
+            acc[tl][0] = fmaf(sc[0][h], dd[0], acc[tl][0]);
+            acc[tl][1] = fmaf(sc[0][h], dd[1], acc[tl][1]);
+            acc[tl][2] = fmaf(sc[1][h], dd[2], acc[tl][2]);
+            acc[tl][3] = fmaf(sc[1][h], dd[3], acc[tl][3]);
           }
         }
       }
-      ++use_cnt;
-      if (stop) break;
     }
-    if (stop) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+
+    // ---- cross-warp reduction and epilogue
+    const int buf = (int)(it & 1);
+    float* rb = red + buf * kRedFloats;
+    float* rw = rb + warp * (kRows * kGroup);
+#pragma unroll
+    for (int tl = 0; tl < kTiles; ++tl) {
+      const int r = 16 * tl + g;
+      *reinterpret_cast<float2*>(rw + r * kGroup + 2 * t) = make_float2(acc[tl][0] * inv[0], acc[tl][1] * inv[1]);
+      *reinterpret_cast<float2*>(rw + (r + 8) * kGroup + 2 * t) =
+          make_float2(acc[tl][2] * inv[0], acc[tl][3] * inv[1]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&redbar[buf]);
+    // every consumer waits: a warp may only write this buffer again two units
+    // later, after all warps have arrived at the unit in between
+    if (!mbar_wait(&redbar[buf], (uint32_t)((it >> 1) & 1), p.status)) {
+      *abort_flag = 1;
+      break;
+    }
+    if (GATE_UP) {
+      constexpr int kOut = kRows / 2;  // activated outputs per unit
+      for (int idx = tid; idx < kOut * kGroup; idx += kConsumerThreads) {
+        const int c = idx / kOut, r = idx % kOut;
+        float hg = 0.f, hu = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          hg += rb[w * kRows * kGroup + r * kGroup + c];
+          hu += rb[w * kRows * kGroup + (r + kOut) * kGroup + c];
+        }
+        const int slot = grp * kGroup + c;
+        if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + kOut * j + r] = silu(hg) * hu;
+      }
+    } else {
+      for (int idx = tid; idx < kRows * kGroup; idx += kConsumerThreads) {
+        const int c = idx / kRows, r = idx % kRows;
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + r * kGroup + c];
+        const int slot = grp * kGroup + c;
+        if (slot < npairs) {
+          const int pair = p.sorted_pair[base + slot];
+          p.dst[(size_t)pair * p.N + kRows * j + r] = y;
+        }
+      }
+    }
   }
 }
 
@@ -339,20 +400,36 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ ids,
                                                       const float* __restrict__ topk_w, int E, int topk,
                                                       int H, uint16_t* __restrict__ out) {
+  __shared__ int s_ids[64];
+  __shared__ float s_w[64];
   const int t = blockIdx.y;
+  if (threadIdx.x < topk) {
+    s_ids[threadIdx.x] = ids[t * topk + threadIdx.x];
+    s_w[threadIdx.x] = topk_w[t * topk + threadIdx.x];
+  }
+  __syncthreads();
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c4 * 4 >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < topk; ++k) {
-    const int pr = t * topk + k;
-    const int e = ids[pr];
-    if ((unsigned)e >= (unsigned)E) continue;
-    const float wk = topk_w[pr];
-    const float4 y = __ldcg(reinterpret_cast<const float4*>(ybuf + (size_t)pr * H) + c4);
-    acc.x = fmaf(wk, y.x, acc.x);
-    acc.y = fmaf(wk, y.y, acc.y);
-    acc.z = fmaf(wk, y.z, acc.z);
-    acc.w = fmaf(wk, y.w, acc.w);
+  const float4* yb = reinterpret_cast<const float4*>(ybuf + (size_t)t * topk * H) + c4;
+  const int h4 = H / 4;
+  for (int k0 = 0; k0 < topk; k0 += 8) {
+    float4 y[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool valid = k0 + k < topk && (unsigned)s_ids[k0 + k] < (unsigned)E;
+      y[k] = valid ? __ldcg(yb + (size_t)(k0 + k) * h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k0 + k < topk && (unsigned)s_ids[k0 + k] < (unsigned)E) {
+        const float wk = s_w[k0 + k];
+        acc.x = fmaf(wk, y[k].x, acc.x);
+        acc.y = fmaf(wk, y[k].y, acc.y);
+        acc.z = fmaf(wk, y[k].z, acc.z);
+        acc.w = fmaf(wk, y[k].w, acc.w);
+      }
+    }
   }
   uint2 o;
   o.x = f32x2_to_bf16x2(acc.x, acc.y);
@@ -362,7 +439,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 
 template <WeightKind KIND, bool GATE_UP, int NBW>
 cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
-  const size_t smem = 1024 + 2 * kConsumerWarps * kRows * kCols * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
+  const size_t smem = 1024 + 2 * kRedFloats * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -372,10 +449,11 @@ cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
 
 template <WeightKind KIND, bool GATE_UP>
 cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
-  const int nbw = ((gp.K >> 5) + kConsumerWarps - 1) / kConsumerWarps;
+  const int nbw = 2 * (((gp.K >> 5) + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps));
   if (nbw <= 8) return launch_gemm<KIND, GATE_UP, 8>(gp, grid, s);
   if (nbw <= 16) return launch_gemm<KIND, GATE_UP, 16>(gp, grid, s);
-  return launch_gemm<KIND, GATE_UP, 32>(gp, grid, s);
+  if (nbw <= 24) return launch_gemm<KIND, GATE_UP, 24>(gp, grid, s);
+  return launch_gemm<KIND, GATE_UP, 38>(gp, grid, s);
 }
 
 void fill_stage_geometry(GemmParams& gp, WeightKind kind) {
@@ -383,7 +461,7 @@ void fill_stage_geometry(GemmParams& gp, WeightKind kind) {
   gp.srow_bytes = (gp.K >> 5) * (kind == WeightKind::kMxfp4 ? 1 : 4);
   const int raw = kRows * gp.row_stride + kRows * gp.srow_bytes;
   gp.stage_bytes = (raw + 127) & ~127;
-  const int avail = kSmemBudget - 1024 - 2 * kConsumerWarps * kRows * kCols * (int)sizeof(float);
+  const int avail = kSmemBudget - 1024 - 2 * kRedFloats * (int)sizeof(float);
   int st = avail / gp.stage_bytes;
   gp.n_stages = st > 8 ? 8 : st;
 }
@@ -397,11 +475,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g1.N = 2 * a.I;
   g1.K = a.H;
   g1.I = a.I;
-  g1.tiles = a.I / 8;
+  g1.tiles = a.I / (kRows / 2);
   g1.src = a.x;
   g1.offsets = a.route.offsets;
   g1.active = a.route.active;
   g1.n_active = a.route.n_active;
+  g1.gprefix = a.route.gprefix;
   g1.sorted_pair = a.route.sorted_pair;
   g1.topk = a.topk;
   g1.dst = a.abuf;

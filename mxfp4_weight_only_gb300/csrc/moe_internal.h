@@ -15,21 +15,25 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kMaxExperts = 1024;
 constexpr int kRouteThreads = 1024;
 
+// Pairs per activation group of the weight-streaming kernels.
+constexpr int kMoeGroup = 8;
+
 // Tokens at or above which MOE_PATH_AUTO picks the tensor-core kernels.
 constexpr int kPrefillMinTokens = 64;
 // Whether the tensor-core (prefill) kernels are built into this library.
-constexpr bool kPrefillAvailable = false;
+constexpr bool kPrefillAvailable = true;
 
 // Prefill tile sizes (tcgen05, cta_group::1).
 constexpr int kTcM = 128;  // rows of x per M tile
 constexpr int kTcN = 128;  // weight rows per N tile
 constexpr int kTcK = 64;   // K per pipeline step (one 128-byte swizzle row of bf16)
+constexpr int kTcRows = 2 * kTcM;  // sorted rows per work item (two M tiles share each weight tile)
 
 enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
 
 // Byte offsets of the workspace regions for one problem.
 struct Workspace {
-  size_t status, counts, offsets, active, n_active, sorted_pair, pair_pos, mtiles, n_mtiles;
+  size_t status, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles;
   size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
   size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 [P][I], f32 [T][H]
   size_t total;
@@ -46,9 +50,10 @@ struct RouteOut {
   int32_t* offsets;      // [E+1]
   int32_t* active;       // [E] ids of experts with >= 1 pair, ascending
   int32_t* n_active;     // [1]
+  int32_t* gprefix;      // [E+1] exclusive prefix over active experts of ceil(count / kMoeGroup)
   int32_t* sorted_pair;  // [P]
   int32_t* pair_pos;     // [P]
-  int32_t* mtiles;       // [max_mtiles] (expert << 20 | first row / kTcM) for the tensor-core path
+  int32_t* mtiles;       // [max_mtiles] (expert << 20 | tile index), tiles of kTcRows rows, tensor-core path
   int32_t* n_mtiles;     // [1]
 };
 

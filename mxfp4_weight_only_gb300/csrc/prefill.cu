@@ -1,8 +1,566 @@
-// Tensor-core (tcgen05) grouped GEMMs for large batches (prefill).
+// Tensor-core grouped GEMMs for large batches (prefill): tcgen05 MMAs with TMEM
+// accumulators, activations by TMA, MXFP4 weights dequantised to bf16 in
+// shared memory.
+//
+// Same two stages as the weight-streaming path (Mxfp4MoEMethod.apply on the
+// vLLM quantization/mxfp4 API page, gate_up ``w13`` then down ``w2``), laid
+// out for a dense contraction:
+//   gather:  xs[i] = x[token of sorted pair i]                 (bf16 rows)
+//   gemm1:   h = xs W13[e]^T, a = SiLU(h_gate) * h_up -> as    (bf16 rows)
+//   gemm2:   y = as W2[e]^T, outacc[t] += topk_w * y          (fp32, red.add)
+//   cast:    out = bf16(outacc)
+//
+// Work item = (expert, up to 256 sorted rows, one N tile of 128 weight rows;
+// gemm1 tiles hold 64 gate rows and the matching 64 up rows).  One CTA per
+// SM walks items round-robin.  Warp roles per CTA:
+//   warp 0      TMA producer: two 128x64 bf16 activation tiles per K step
+//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads)
+//   warp 1      TMEM owner and MMA issuer (one thread): 128x128x16 bf16 MMAs,
+//               f32 accumulators in TMEM, two accumulator sets (one per
+//               128-row half) double-buffered across items (512 columns)
+//   warps 2-5   weight producers: each thread owns one weight row, streams
+//               its packed E2M1 bytes and E8M0 scales from global memory
+//               (8 K steps ahead in registers), converts them exactly to bf16
+//               (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by the
+//               block scale) and writes the 128x64 swizzled B tile
+//   warps 6-9   epilogue: tcgen05.ld of the accumulators, SiLU gating (gemm1)
+//               or router-weighted scatter-add (gemm2), global stores
+// Each 128x64 B tile feeds the MMAs of both 128-row halves, so the weight
+// conversion cost is spread over up to 256 rows.
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
 
-cudaError_t launch_prefill(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kPThreads = 320;
+constexpr int kPStages = 4;
+constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kPStageBytes = 3 * kTileBytes;  // A half 0, A half 1, B
+constexpr uint32_t kTmemCols = 512;
+constexpr int kPrefetch = 8;  // K steps of packed weights in flight per converter thread
+
+struct TcParams {
+  const uint8_t* w;   // packed [E][N][K/2]
+  const uint8_t* ws;  // E8M0 [E][N][K/32]
+  int N, K, I, H;
+  int n_tiles;        // N tiles per expert
+  const int32_t* mtiles;
+  const int32_t* n_mtiles;
+  const int32_t* offsets;
+  const int32_t* counts;
+  const int32_t* sorted_pair;
+  int topk;
+  const float* topk_w;
+  uint16_t* act_out;  // gemm1: [P][I] bf16
+  float* outacc;      // gemm2: [T][H]
+  uint32_t* status;
+};
+
+// ------------------------------------------------------------------ tcgen05 / TMA helpers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Two exact E2M1 values as f16 (one packed byte) -> the same values times
+// 2^-112 as bf16: the f16 exponent field and mantissa bit move down 3 bits
+// into the bf16 layout, sign kept, zero stays zero.
+__device__ __forceinline__ uint32_t f16pair_to_bf16_rebias(uint32_t h) {
+  return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+}
+
+// 32 E2M1 values (16 packed bytes) of one block with E8M0 scale s -> 4 chunks of
+// 8 bf16 (16 B each), exact.
+__device__ __forceinline__ void dequant_block(const uint4& q, uint32_t s, uint4 (&out)[4]) {
+  // value * 2^-112 * 2^(s-15) = value * 2^(s-127); 2^(s-15) is a normal bf16 for s <= 142
+  const bool big = s > 142u;
+  const uint32_t e1 = big ? 127u + 127u : s - 15u + 127u;
+  const uint32_t f1 = (e1 << 7) | (e1 << 23);
+  const uint32_t e2 = big ? s - 142u + 127u : 127u;
+  const uint32_t f2 = (e2 << 7) | (e2 << 23);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h0, h1, h2, h3;
+    e2m1x8_to_f16x8(w[i], h0, h1, h2, h3);
+    uint32_t b0 = bf16x2_mul(f16pair_to_bf16_rebias(h0), f1);
+    uint32_t b1 = bf16x2_mul(f16pair_to_bf16_rebias(h1), f1);
+    uint32_t b2 = bf16x2_mul(f16pair_to_bf16_rebias(h2), f1);
+    uint32_t b3 = bf16x2_mul(f16pair_to_bf16_rebias(h3), f1);
+    if (big) {
+      b0 = bf16x2_mul(b0, f2);
+      b1 = bf16x2_mul(b1, f2);
+      b2 = bf16x2_mul(b2, f2);
+      b3 = bf16x2_mul(b3, f2);
+    }
+    out[i] = make_uint4(b0, b1, b2, b3);
+  }
+}
+
+struct ItemInfo {
+  int e, nt, row0, rows;
+};
+
+__device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long item) {
+  ItemInfo it;
+  const int mp = (int)(item / p.n_tiles);
+  it.nt = (int)(item % p.n_tiles);
+  const int code = p.mtiles[mp];
+  it.e = code >> 20;
+  const int mi = code & 0xFFFFF;
+  it.row0 = p.offsets[it.e] + kTcRows * mi;
+  it.rows = min(kTcRows, p.counts[it.e] - kTcRows * mi);
+  return it;
+}
+
+template <bool GATE_UP>
+__global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                               const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPStages * kPStageBytes);
+  uint64_t* a_full = bars;
+  uint64_t* b_full = bars + kPStages;
+  uint64_t* empty = bars + 2 * kPStages;
+  uint64_t* acc_full = bars + 3 * kPStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&b_full[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const long long n_items = (long long)(*p.n_mtiles) * p.n_tiles;
+  const int KS = p.K / kTcK;
+  const uint32_t idesc = idesc_bf16(kTcM, kTcN);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      long long g = 0;
+      for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+        const ItemInfo it = decode_item(p, item);
+        const int halves = it.rows > kTcM ? 2 : 1;
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int stage = (int)(g % kPStages);
+          const long long u = g / kPStages;
+          if (u > 0 && !mbar_wait(&empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st = smem + stage * kPStageBytes;
+          mbar_arrive_expect_tx(&a_full[stage], halves * kTileBytes);
+          tma_load_2d(st, &tmap_a, ks * kTcK, it.row0, &a_full[stage]);
+          if (halves == 2) tma_load_2d(st + kTileBytes, &tmap_a, ks * kTcK, it.row0 + kTcM, &a_full[stage]);
+        }
+      }
+      // nothing issued may still be in flight when the CTA exits
+      const long long first = g > kPStages ? g - kPStages : 0;
+      for (long long v = first; v < g; ++v) mbar_wait(&a_full[v % kPStages], (uint32_t)((v / kPStages) & 1), p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      long long g = 0, j = 0;
+      for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
+        const ItemInfo it = decode_item(p, item);
+        const int halves = it.rows > kTcM ? 2 : 1;
+        const int buf = (int)(j & 1);
+        const long long u = j >> 1;
+        if (u > 0 && !mbar_wait(&acc_empty[buf], (uint32_t)((u - 1) & 1), p.status)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + buf * 256, d1 = d0 + 128;
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int stage = (int)(g % kPStages);
+          const uint32_t par = (uint32_t)((g / kPStages) & 1);
+          if (!mbar_wait(&a_full[stage], par, p.status) || !mbar_wait(&b_full[stage], par, p.status)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * kPStageBytes);
+          const uint64_t a0 = sw128_desc(st), a1 = sw128_desc(st + kTileBytes), b = sw128_desc(st + 2 * kTileBytes);
+#pragma unroll
+          for (int k = 0; k < kTcK / 16; ++k) {
+            const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
+            mma_bf16(d0, a0 + 2 * k, b + 2 * k, idesc, acc);
+            if (halves == 2) mma_bf16(d1, a1 + 2 * k, b + 2 * k, idesc, acc);
+          }
+          mma_commit(&empty[stage]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[buf]);
+      }
+      // all issued MMAs complete before TMEM is released
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.status);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ weight converters
+    const int r = tid - 64;  // B-tile row 0..127
+    const int Kh = p.K >> 1, Kb = p.K >> 5;
+    long long g = 0;
+    uint8_t* const brow_base = smem + 2 * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+    const int sw = r & 7;
+    for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+      const ItemInfo it = decode_item(p, item);
+      int wrow;
+      if (GATE_UP) wrow = r < 64 ? 64 * it.nt + r : p.I + 64 * it.nt + (r - 64);
+      else wrow = kTcN * it.nt + r;
+      const uint8_t* wr = p.w + ((size_t)it.e * p.N + wrow) * Kh;
+      const uint8_t* sr = p.ws + ((size_t)it.e * p.N + wrow) * Kb;
+      uint4 pq[kPrefetch][2];
+      uint32_t ps[kPrefetch];
+#pragma unroll
+      for (int d = 0; d < kPrefetch; ++d) {
+        if (d < KS) {
+          const uint4* src = reinterpret_cast<const uint4*>(wr + d * 32);
+          pq[d][0] = __ldcs(src);
+          pq[d][1] = __ldcs(src + 1);
+          ps[d] = *reinterpret_cast<const uint16_t*>(sr + 2 * d);
+        }
+      }
+      bool stop = false;
+      for (int ks0 = 0; ks0 < KS && !stop; ks0 += kPrefetch) {
+#pragma unroll
+        for (int d = 0; d < kPrefetch; ++d) {
+          const int ks = ks0 + d;
+          if (ks < KS && !stop) {
+            const uint4 q0 = pq[d][0], q1 = pq[d][1];
+            const uint32_t sc = ps[d];
+            if (ks + kPrefetch < KS) {
+              const uint4* src = reinterpret_cast<const uint4*>(wr + (ks + kPrefetch) * 32);
+              pq[d][0] = __ldcs(src);
+              pq[d][1] = __ldcs(src + 1);
+              ps[d] = *reinterpret_cast<const uint16_t*>(sr + 2 * (ks + kPrefetch));
+            }
+            const int stage = (int)(g % kPStages);
+            const long long u = g / kPStages;
+            if (u > 0 && !mbar_wait(&empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+              *abort_flag = 1;
+              stop = true;
+            } else {
+              uint8_t* brow = brow_base + stage * kPStageBytes;
+              uint4 c[4];
+              dequant_block(q0, sc & 0xFFu, c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + ((i ^ sw) << 4)) = c[i];
+              dequant_block(q1, sc >> 8, c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + (((4 + i) ^ sw) << 4)) = c[i];
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&b_full[stage]);
+              ++g;
+            }
+          }
+        }
+      }
+      if (stop) break;
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    long long j = 0;
+    for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
+      const ItemInfo it = decode_item(p, item);
+      const int halves = it.rows > kTcM ? 2 : 1;
+      const int buf = (int)(j & 1);
+      if (!mbar_wait(&acc_full[buf], (uint32_t)((j >> 1) & 1), p.status)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      for (int h = 0; h < halves; ++h) {
+        const int lrow = h * kTcM + q * 32 + lane;
+        const bool valid = lrow < it.rows;
+        const int row = it.row0 + lrow;
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256 + h * 128;
+        if (GATE_UP) {
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tbase + c0, gv);
+            tmem_ld32(tbase + 64 + c0, uv);
+            tmem_ld_wait();
+            if (valid) {
+              uint16_t* dst = p.act_out + (size_t)row * p.I + 64 * it.nt + c0;
+#pragma unroll
+              for (int v = 0; v < 32; v += 8) {
+                uint32_t o[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                  const float a0 = silu(__uint_as_float(gv[v + 2 * z])) * __uint_as_float(uv[v + 2 * z]);
+                  const float a1 = silu(__uint_as_float(gv[v + 2 * z + 1])) * __uint_as_float(uv[v + 2 * z + 1]);
+                  o[z] = f32x2_to_bf16x2(a0, a1);
+                }
+                *reinterpret_cast<uint4*>(dst + v) = make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            }
+          }
+        } else {
+          int tok = 0;
+          float wk = 0.f;
+          if (valid) {
+            const int pair = p.sorted_pair[row];
+            tok = pair / p.topk;
+            wk = p.topk_w[pair];
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t yv[32];
+            tmem_ld32(tbase + c0, yv);
+            tmem_ld_wait();
+            if (valid) {
+              float* dst = p.outacc + (size_t)tok * p.H + kTcN * it.nt + c0;
+#pragma unroll
+              for (int v = 0; v < 32; v += 4)
+                red_add_v4(dst + v, wk * __uint_as_float(yv[v]), wk * __uint_as_float(yv[v + 1]),
+                           wk * __uint_as_float(yv[v + 2]), wk * __uint_as_float(yv[v + 3]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ sorted_pair,
+                                                          const int32_t* __restrict__ n_valid, int topk, int H,
+                                                          uint16_t* __restrict__ xs) {
+  const int i = blockIdx.x;
+  if (i >= *n_valid) return;
+  const int tok = sorted_pair[i] / topk;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
+  uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)i * H);
+  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) dst[c] = __ldg(src + c);
+}
+
+__global__ void __launch_bounds__(256) cast_out_kernel(const float* __restrict__ acc, long long n4,
+                                                       uint16_t* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(acc) + i);
+    uint2 o;
+    o.x = f32x2_to_bf16x2(v.x, v.y);
+    o.y = f32x2_to_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2*>(out)[i] = o;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t get_encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  if (!cached) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    cached = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  *fn = cached;
+  return cudaSuccess;
+}
+
+// bf16 [rows][K] row-major, 128 x 64 boxes with 128-byte swizzle.
+cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K) {
+  EncodeTiledFn enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool GATE_UP>
+cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
+  const size_t smem = 1024 + (size_t)kPStages * kPStageBytes + 256;
+  auto kern = tc_gemm_kernel<GATE_UP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kPThreads, smem, s>>>(map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
+  const long long P = (long long)a.T * a.topk;
+  CUtensorMap map_x, map_a;
+  cudaError_t e = make_act_map(&map_x, a.xs, P, a.H);
+  if (e != cudaSuccess) return e;
+  e = make_act_map(&map_a, a.as, P, a.I);
+  if (e != cudaSuccess) return e;
+
+  timing_mark(1, false, s);
+  gather_rows_kernel<<<(unsigned)P, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(a.x), a.route.sorted_pair,
+                                                  a.route.offsets + a.E, a.topk, a.H,
+                                                  reinterpret_cast<uint16_t*>(a.xs));
+  timing_mark(1, true, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  TcParams p{};
+  p.w = a.w13;
+  p.ws = a.w13_s;
+  p.N = 2 * a.I;
+  p.K = a.H;
+  p.I = a.I;
+  p.H = a.H;
+  p.n_tiles = a.I / 64;
+  p.mtiles = a.route.mtiles;
+  p.n_mtiles = a.route.n_mtiles;
+  p.offsets = a.route.offsets;
+  p.counts = a.route.counts;
+  p.sorted_pair = a.route.sorted_pair;
+  p.topk = a.topk;
+  p.topk_w = a.topk_w;
+  p.act_out = reinterpret_cast<uint16_t*>(a.as);
+  p.outacc = a.outacc;
+  p.status = a.status;
+  timing_mark(2, false, s);
+  e = launch_tc<true>(map_x, p, a.num_sms, s);
+  timing_mark(2, true, s);
+  if (e != cudaSuccess) return e;
+
+  if ((e = cudaMemsetAsync(a.outacc, 0, (size_t)a.T * a.H * sizeof(float), s)) != cudaSuccess) return e;
+  TcParams p2 = p;
+  p2.w = a.w2;
+  p2.ws = a.w2_s;
+  p2.N = a.H;
+  p2.K = a.I;
+  p2.n_tiles = a.H / kTcN;
+  timing_mark(3, false, s);
+  e = launch_tc<false>(map_a, p2, a.num_sms, s);
+  timing_mark(3, true, s);
+  if (e != cudaSuccess) return e;
+
+  const long long n4 = (long long)a.T * a.H / 4;
+  const int grid = (int)((n4 + 255) / 256 < (long long)a.num_sms * 8 ? (n4 + 255) / 256 : (long long)a.num_sms * 8);
+  timing_mark(4, false, s);
+  cast_out_kernel<<<grid, 256, 0, s>>>(a.outacc, n4, reinterpret_cast<uint16_t*>(a.out));
+  timing_mark(4, true, s);
+  return cudaGetLastError();
+}
 
 }  // namespace moe

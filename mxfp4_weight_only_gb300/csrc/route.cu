@@ -6,7 +6,7 @@
 // contiguous.  Pairs keep ascending flat index p = t*topk + k inside each
 // expert, ids outside [0, E) are dropped.  Besides counts/offsets/order this
 // kernel emits the list of active experts (weight-streaming kernels iterate
-// over it) and, on request, the list of 128-row M tiles per expert for the
+// over it) and, on request, the list of 256-row M tiles per expert for the
 // tensor-core kernels.
 #include "common.cuh"
 
@@ -77,10 +77,16 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   if (r.active) {
     if (tid < E && v > 0) r.active[apos] = tid;
     if (tid == 0) *r.n_active = n_act;
+    // activation groups per active expert, prefix-summed in active-list order
+    int n_groups = 0;
+    const int ng = (v + kMoeGroup - 1) / kMoeGroup;
+    const int gpos = block_excl_scan(ng, scratch, &n_groups);
+    if (tid < E && v > 0) r.gprefix[apos] = gpos;
+    if (tid == 0) r.gprefix[n_act] = n_groups;
   }
 
   if (make_mtiles) {
-    const int nt = (v + kTcM - 1) / kTcM;
+    const int nt = (v + kTcRows - 1) / kTcRows;
     int n_tiles = 0;
     const int tpos = block_excl_scan(nt, scratch, &n_tiles);
     for (int i = 0; i < nt; ++i) r.mtiles[tpos + i] = (tid << 20) | i;

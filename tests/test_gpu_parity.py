@@ -223,3 +223,60 @@ def test_moe_k3_int4_sampled(mw, k3_weights, T):
         oq2[e], of2[e] = a[0], b[0]
     ref = moe.moe_forward_sampled(x, ids, w, oq13, of13, oq2, of2, toks, cols, kind="int4g32")
     assert_moe_close(got[np.ix_(toks, cols)], ref)
+
+
+# ----------------------------------------------------------------------------- tensor-core (prefill) path
+
+
+@pytest.mark.parametrize("E,H,I,T,topk,bias", [(8, 512, 512, 200, 4, None), (4, 512, 1024, 300, 2, 2.0),
+                                               (16, 1024, 512, 130, 6, 2.0)])
+def test_moe_prefill_small(mw, E, H, I, T, topk, bias):
+    prob = gaussian_problem(E * 7 + T, E, H, I, T, topk, bias)
+    ref = moe.moe_forward(*prob)
+    assert_moe_close(run_gpu(mw, prob, path=2), ref)
+
+
+def test_moe_prefill_tile_boundaries(mw):
+    # expert 0 gets 257 rows (a full 256-row item plus a 1-row item), expert 1
+    # exactly 256, expert 2 exactly 128, expert 3 none; invalid ids in between
+    E, H, I, topk = 4, 512, 512, 1
+    counts = [257, 256, 128]
+    ids = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)] + [np.array([-1, 7], np.int32)])
+    g = np.random.default_rng(11)
+    ids = ids[g.permutation(ids.size)][:, None].astype(np.int32)
+    T = ids.shape[0]
+    prob = list(gaussian_problem(12, E, H, I, T, topk))
+    prob[1] = ids
+    prob[2] = g.uniform(0.1, 1.0, size=(T, 1)).astype(np.float32)
+    ref = moe.moe_forward(*prob)
+    got = run_gpu(mw, prob, path=2)
+    assert_moe_close(got, ref)
+    assert np.all(got[(ids[:, 0] < 0) | (ids[:, 0] >= E)] == 0)
+
+
+def test_prefill_and_decode_paths_agree_with_oracle(mw):
+    prob = gaussian_problem(21, 8, 512, 512, 96, 4)
+    ref = moe.moe_forward(*prob)
+    a = run_gpu(mw, prob, path=1)
+    b = run_gpu(mw, prob, path=2)
+    assert_moe_close(a, ref)
+    assert_moe_close(b, ref)
+    c = run_gpu(mw, prob, path=0)  # T >= 64: the automatic choice is the tensor-core path
+    assert np.array_equal(b, c)
+
+
+def test_moe_k3_prefill_sampled(mw, k3_weights):
+    (w13, s13, w2, s2), dw = k3_weights
+    T = 4096
+    S = synth.k3(T)
+    g = synth.rng(400)
+    x = synth.activations_bf16(g, T, S.H)
+    ids, w = synth.router_topk(g, T, S.E, S.topk, expert_bias_std=2.0)
+    out = mw.moe_a16w4_mxfp4(x_dev(x), dev(ids), dev(w), *dw)
+    torch.cuda.synchronize()
+    got = formats.bf16_to_f64(out_host(out))
+    toks = np.array([0, 2047, 4095])
+    cols = np.sort(g.choice(S.H, 96, replace=False))
+    ref = moe.moe_forward_sampled(x, ids, w, w13, s13, w2, s2, toks, cols)
+    assert_moe_close(got[np.ix_(toks, cols)], ref)
+    assert np.isfinite(got).all()
