@@ -16,10 +16,10 @@
 // units of one CTA share an expert and group, so its activations stay in
 // registers across units.
 //
-// Per CTA (8 warps): one producer warp streams each item's 32 weight rows
+// Per CTA (15 warps): one producer warp streams each item's 32 weight rows
 // (one cp.async.bulk per row into a padded shared-memory stage, so consumer
 // reads are bank-conflict-free) and their scales through an mbarrier ring.
-// Seven consumer warps split K.  Each turns its part of the packed rows into
+// Fourteen consumer warps split K.  Each turns its part of the packed rows into
 // m16n8k16 f16 MMA operands (E2M1 pairs via cvt.rn.f16x2.e2m1x2, exact; int4
 // pairs via the 1024-offset f16 trick, exact) and multiplies them by up to 8
 // activation columns held in registers; the per-32-block weight scale is
@@ -34,7 +34,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kConsumerWarps = 7;
+constexpr int kConsumerWarps = 14;
 constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kTiles = 2;             // 16-row MMA tiles per item

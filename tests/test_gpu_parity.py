@@ -262,7 +262,7 @@ def test_prefill_and_decode_paths_agree_with_oracle(mw):
     assert_moe_close(a, ref)
     assert_moe_close(b, ref)
     c = run_gpu(mw, prob, path=0)  # T >= 64: the automatic choice is the tensor-core path
-    assert np.array_equal(b, c)
+    assert_moe_close(c, ref)  # the tensor-core combine adds in arrival order: equal within tolerance
 
 
 def test_moe_k3_prefill_sampled(mw, k3_weights):
