@@ -144,6 +144,34 @@ int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int
 int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream);
 
 /*
+ * Allocation-free variant of moe_a16w4_mxfp4.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory when
+ * they run the layer (a serving thread that must not call cudaMalloc or a
+ * framework allocator, a plugin that is handed only input and output pointers,
+ * a process whose device memory is reserved up front).  It takes the same
+ * inputs and output as moe_a16w4_mxfp4 but no workspace: its scratch is one
+ * fixed 16 MiB device array inside the library, which every GPU that loads the
+ * library holds until the process exits.
+ *   - Runs the weight-streaming kernels (d->path AUTO or DECODE; PREFILL is
+ *     rejected with MOE_ERR_BAD_DIMS).  Problems whose workspace
+ *     (moe_workspace_bytes with path DECODE) exceeds 16 MiB are rejected with
+ *     MOE_ERR_WORKSPACE; the 112-expert, H=3584, I=3072, top-15 layer fits up
+ *     to 32 tokens.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (once per device, with that device current); make
+ *     that first call before any stream capture.
+ *   - All calls share the one array, which keeps the previous call's contents;
+ *     every region is written before it is read within a call, so nothing needs
+ *     clearing.  Calls that may overlap on the GPU (different streams, or
+ *     different host threads on one device) race on the array: order them.
+ *   - Device status bits of this variant are not exposed.
+ */
+int moe_a16w4_mxfp4_noalloc(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
+                            const uint8_t* w2_scale, void* out, void* stream);
+
+/*
  * Optional per-kernel timing, for benchmarks.  ``events`` holds 2*n
  * cudaEvent_t handles created by the caller (n <= 8).  The next
  * moe_a16w4_mxfp4 / moe_a16w4_int4g32 call made from this host thread records

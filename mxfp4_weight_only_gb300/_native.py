@@ -39,6 +39,7 @@ SIGNATURES = {
     "requant_mxfp4_to_int4g32": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
     "moe_route": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_read_status": (ctypes.c_int, [_DimsP, _vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "moe_a16w4_mxfp4_noalloc": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_set_timing_events": (ctypes.c_int, [ctypes.POINTER(_vp), _i32]),
     "moe_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_abi_version": (ctypes.c_int, []),

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libmoe_a16w4.so"
-SOURCES = ["api.cu", "route.cu", "requant.cu", "decode.cu", "prefill.cu"]
+SOURCES = ["api.cu", "route.cu", "requant.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "moe_internal.h")] + [
     os.path.join(ROOT, "include", "moe_a16w4.h")
 ]
