@@ -475,6 +475,33 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
     rows["int4g32_decode"] = i4
     del q_copies
     torch.cuda.empty_cache()
+    # tensor-core (prefill) path: 4096 tokens, skewed routing
+    T = 4096
+    pb = [dev_batch(T, 2000 + i, bias=2.0) for i in range(2)]
+    d = m.dims(SHAPE.E, SHAPE.H, SHAPE.I, SHAPE.topk, T, m.MOE_PATH_PREFILL)
+    ws = torch.empty(m.moe_workspace_bytes(d), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, SHAPE.H), dtype=torch.bfloat16, device=dev)
+    flops = 2.0 * T * SHAPE.topk * 3 * SHAPE.H * SHAPE.I
+    ms_list = []
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(6):
+        x, ids, w, _ = pb[i % 2]
+        s_ev.record()
+        m.moe_a16w4_mxfp4(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws,
+                          path=m.MOE_PATH_PREFILL)
+        e_ev.record()
+        e_ev.synchronize()
+        if i >= 2:
+            ms_list.append(s_ev.elapsed_time(e_ev))
+    ms = statistics.median(ms_list)
+    tf = flops / (ms * 1e-3) / 1e12
+    rows["mxfp4_prefill_T4096_skewed"] = {
+        "ms_per_call": round(ms, 3), "TFLOPs_useful": round(tf, 1),
+        "bf16_frac_burst": round(tf / peaks["bf16_tflops"], 3),
+        "bf16_frac_sustained": round(tf / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]), 3),
+        "useful_flops": flops}
+    del ws, out
+    torch.cuda.empty_cache()
     return rows
 
 

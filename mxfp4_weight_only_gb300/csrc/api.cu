@@ -148,7 +148,7 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.n_mtiles = o; o = align256(o + 4);
   if (L.prefill) {
     L.xs = o; o = align256(o + 2 * P * H);
-    L.as = o; o = align256(o + 2 * P * I);
+    L.as = o; o = align256(o + 4 * P * I);
     L.outacc = o; o = align256(o + 4 * T * H);
   } else {
     L.abuf = o; o = align256(o + 4 * P * I);

@@ -97,6 +97,18 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Block until the grids this one depends on (launched before it on the
+// stream) have completed and their writes are visible.  No-op for a normal launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid on the stream, if launched as a programmatic dependent,
+// to start being scheduled.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barriers
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
@@ -144,7 +156,7 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z));
 // D = A * B + C for one m16n8k16 tile, f16 inputs, f32 accumulate.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])

@@ -16,7 +16,7 @@
 // units of one CTA share an expert and group, so its activations stay in
 // registers across units.
 //
-// Per CTA (15 warps): one producer warp streams each item's 32 weight rows
+// Per CTA (15 warps): one producer warp streams each unit's 32 weight rows
 // (one cp.async.bulk per row into a padded shared-memory stage, so consumer
 // reads are bank-conflict-free) and their scales through an mbarrier ring.
 // Fourteen consumer warps split K.  Each turns its part of the packed rows into
@@ -219,6 +219,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     fence_barrier_init();
   }
   __syncthreads();
+  // gate_up reads the grouping of the kernel before it; down reads only
+  // weights and grouping here and waits for gate_up's activations further down
+  if (GATE_UP) grid_dep_wait();
+  grid_dep_launch_dependents();
 
   // Work units: (active expert d, 8-pair group, weight tile j), group-major
   // within an expert, so a CTA's contiguous run reloads activations only at
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   uint32_t xf[NBW][4];
   float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1
   int cur_e = -1, cur_grp = -1;
+  if (!GATE_UP) grid_dep_wait();  // the activations come from the gate_up kernel
 
   long long it = 0;
   int d = d0;
@@ -402,6 +407,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       int H, uint16_t* __restrict__ out) {
   __shared__ int s_ids[64];
   __shared__ float s_w[64];
+  grid_dep_wait();  // ybuf comes from the down kernel
   const int t = blockIdx.y;
   if (threadIdx.x < topk) {
     s_ids[threadIdx.x] = ids[t * topk + threadIdx.x];
@@ -443,8 +449,7 @@ cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDecThreads, smem, s>>>(gp);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, gp);
 }
 
 template <WeightKind KIND, bool GATE_UP>
@@ -512,10 +517,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   dim3 cgrid((a.H / 4 + 127) / 128, a.T);
   timing_mark(3, false, s);
-  combine_kernel<<<cgrid, 128, 0, s>>>(a.ybuf, a.topk_ids, a.topk_w, a.E, a.topk, a.H,
-                                       reinterpret_cast<uint16_t*>(a.out));
+  e = launch_kernel(combine_kernel, cgrid, dim3(128), 0, s, true, (const float*)a.ybuf, a.topk_ids, a.topk_w, a.E,
+                    a.topk, a.H, reinterpret_cast<uint16_t*>(a.out));
   timing_mark(3, true, s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

@@ -35,7 +35,7 @@ enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
 struct Workspace {
   size_t status, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles;
   size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
-  size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 [P][I], f32 [T][H]
+  size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 hi/lo [P][2I], f32 [T][H]
   size_t total;
   bool prefill;
 };
@@ -56,6 +56,25 @@ struct RouteOut {
   int32_t* mtiles;       // [max_mtiles] (expert << 20 | tile index), tiles of kTcRows rows, tensor-core path
   int32_t* n_mtiles;     // [1]
 };
+
+// Launch ``kern`` on ``s``; with ``pdl`` the launch may begin before the previous
+// kernel on the stream finishes (the kernel must call grid_dep_wait() before
+// reading that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // Benchmark timing hook (moe_set_timing_events): record the caller's event
 // before (end = false) or after (end = true) kernel ``index`` of this call.
@@ -99,7 +118,7 @@ struct PrefillArgs {
   void* out;
   RouteOut route;
   void* xs;       // bf16 [P][H]
-  void* as;       // bf16 [P][I]
+  void* as;       // bf16 [P][2I]: hi and lo parts of the activated intermediate
   float* outacc;  // f32 [T][H]
   uint32_t* status;
   int num_sms;

@@ -6,15 +6,18 @@
 // vLLM quantization/mxfp4 API page, gate_up ``w13`` then down ``w2``), laid
 // out for a dense contraction:
 //   gather:  xs[i] = x[token of sorted pair i]                 (bf16 rows)
-//   gemm1:   h = xs W13[e]^T, a = SiLU(h_gate) * h_up -> as    (bf16 rows)
-//   gemm2:   y = as W2[e]^T, outacc[t] += topk_w * y          (fp32, red.add)
+//   gemm1:   h = xs W13[e]^T, a = SiLU(h_gate) * h_up -> as    (a as bf16
+//            hi + lo parts, interleaved per 64 columns: 16 significant bits)
+//   gemm2:   y = [a_hi a_lo] [W2[e] W2[e]]^T, outacc[t] += topk_w * y
+//                                                              (fp32, red.add)
 //   cast:    out = bf16(outacc)
 //
 // Work item = (expert, up to 256 sorted rows, one N tile of 128 weight rows;
 // gemm1 tiles hold 64 gate rows and the matching 64 up rows).  One CTA per
 // SM walks items round-robin.  Warp roles per CTA:
 //   warp 0      TMA producer: two 128x64 bf16 activation tiles per K step
-//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads)
+//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads);
+//               the down GEMM loads the hi and the lo tiles of each K step
 //   warp 1      TMEM owner and MMA issuer (one thread): 128x128x16 bf16 MMAs,
 //               f32 accumulators in TMEM, two accumulator sets (one per
 //               128-row half) double-buffered across items (512 columns)
@@ -25,8 +28,10 @@
 //               block scale) and writes the 128x64 swizzled B tile
 //   warps 6-9   epilogue: tcgen05.ld of the accumulators, SiLU gating (gemm1)
 //               or router-weighted scatter-add (gemm2), global stores
-// Each 128x64 B tile feeds the MMAs of both 128-row halves, so the weight
-// conversion cost is spread over up to 256 rows.
+// Each 128x64 B tile feeds the MMAs of both 128-row halves (and, in the down
+// GEMM, of the hi and the lo activation parts), so the weight conversion cost
+// is spread over up to 256 rows.  Activation and weight tiles travel in
+// separate mbarrier rings.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -36,9 +41,11 @@ namespace moe {
 namespace {
 
 constexpr int kPThreads = 320;
-constexpr int kPStages = 4;
-constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr int kPStageBytes = 3 * kTileBytes;  // A half 0, A half 1, B
+constexpr int kTileBytes = 128 * 128;         // 128 rows x 64 bf16
+constexpr int kAStages = 4;                   // activation ring: two 128-row halves per stage
+constexpr int kAStageBytes = 2 * kTileBytes;
+constexpr int kBStages = 4;                   // weight ring: one 128 x 64 tile per stage
+constexpr int kRingBytes = kAStages * kAStageBytes + kBStages * kTileBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPrefetch = 8;  // K steps of packed weights in flight per converter thread
 
@@ -54,7 +61,7 @@ struct TcParams {
   const int32_t* sorted_pair;
   int topk;
   const float* topk_w;
-  uint16_t* act_out;  // gemm1: [P][I] bf16
+  uint16_t* act_out;  // gemm1: [P][2I] bf16, hi and lo parts per 64 columns
   float* outacc;      // gemm2: [T][H]
   uint32_t* status;
 };
@@ -195,11 +202,14 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
                                                                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPStages * kPStageBytes);
+  uint8_t* a_ring = smem;
+  uint8_t* b_ring = smem + kAStages * kAStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
   uint64_t* a_full = bars;
-  uint64_t* b_full = bars + kPStages;
-  uint64_t* empty = bars + 2 * kPStages;
-  uint64_t* acc_full = bars + 3 * kPStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* b_full = a_empty + kAStages;
+  uint64_t* b_empty = b_full + kBStages;
+  uint64_t* acc_full = b_empty + kBStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -207,10 +217,13 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < kAStages; ++s) {
       mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
       mbar_init(&b_full[s], 4);
-      mbar_init(&empty[s], 1);
+      mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -228,36 +241,41 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
 
   const long long n_items = (long long)(*p.n_mtiles) * p.n_tiles;
   const int KS = p.K / kTcK;
+  // gate_up reads one bf16 activation tile per K step; down reads the hi and
+  // lo bf16 parts of the activated intermediate (interleaved per 64 columns)
+  constexpr int kParts = GATE_UP ? 1 : 2;
   const uint32_t idesc = idesc_bf16(kTcM, kTcN);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       long long g = 0;
-      for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+      bool stop = false;
+      for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
         const ItemInfo it = decode_item(p, item);
         const int halves = it.rows > kTcM ? 2 : 1;
-        for (int ks = 0; ks < KS; ++ks, ++g) {
-          const int stage = (int)(g % kPStages);
-          const long long u = g / kPStages;
-          if (u > 0 && !mbar_wait(&empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+        for (int step = 0; step < KS * kParts; ++step, ++g) {
+          const int stage = (int)(g % kAStages);
+          const long long u = g / kAStages;
+          if (u > 0 && !mbar_wait(&a_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
             *abort_flag = 1;
+            stop = true;
             break;
           }
-          uint8_t* st = smem + stage * kPStageBytes;
+          uint8_t* st = a_ring + stage * kAStageBytes;
           mbar_arrive_expect_tx(&a_full[stage], halves * kTileBytes);
-          tma_load_2d(st, &tmap_a, ks * kTcK, it.row0, &a_full[stage]);
-          if (halves == 2) tma_load_2d(st + kTileBytes, &tmap_a, ks * kTcK, it.row0 + kTcM, &a_full[stage]);
+          tma_load_2d(st, &tmap_a, step * kTcK, it.row0, &a_full[stage]);
+          if (halves == 2) tma_load_2d(st + kTileBytes, &tmap_a, step * kTcK, it.row0 + kTcM, &a_full[stage]);
         }
       }
       // nothing issued may still be in flight when the CTA exits
-      const long long first = g > kPStages ? g - kPStages : 0;
-      for (long long v = first; v < g; ++v) mbar_wait(&a_full[v % kPStages], (uint32_t)((v / kPStages) & 1), p.status);
+      const long long first = g > kAStages ? g - kAStages : 0;
+      for (long long v = first; v < g; ++v) mbar_wait(&a_full[v % kAStages], (uint32_t)((v / kAStages) & 1), p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      long long g = 0, j = 0;
+      long long ga = 0, gb = 0, j = 0;
       for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
         const ItemInfo it = decode_item(p, item);
         const int halves = it.rows > kTcM ? 2 : 1;
@@ -270,26 +288,37 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
         tc_fence_after();
         const uint32_t d0 = tmem_base + buf * 256, d1 = d0 + 128;
         bool ok = true;
-        for (int ks = 0; ks < KS; ++ks, ++g) {
-          const int stage = (int)(g % kPStages);
-          const uint32_t par = (uint32_t)((g / kPStages) & 1);
-          if (!mbar_wait(&a_full[stage], par, p.status) || !mbar_wait(&b_full[stage], par, p.status)) {
-            *abort_flag = 1;
+        for (int ks = 0; ks < KS && ok; ++ks, ++gb) {
+          const int bs = (int)(gb % kBStages);
+          if (!mbar_wait(&b_full[bs], (uint32_t)((gb / kBStages) & 1), p.status)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + stage * kPStageBytes);
-          const uint64_t a0 = sw128_desc(st), a1 = sw128_desc(st + kTileBytes), b = sw128_desc(st + 2 * kTileBytes);
+          const uint64_t b = sw128_desc(smem_u32(b_ring + bs * kTileBytes));
+          for (int part = 0; part < kParts; ++part, ++ga) {
+            const int as = (int)(ga % kAStages);
+            if (!mbar_wait(&a_full[as], (uint32_t)((ga / kAStages) & 1), p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = smem_u32(a_ring + as * kAStageBytes);
+            const uint64_t a0 = sw128_desc(st), a1 = sw128_desc(st + kTileBytes);
 #pragma unroll
-          for (int k = 0; k < kTcK / 16; ++k) {
-            const uint32_t acc = (ks > 0 || k > 0) ? 1u : 0u;
-            mma_bf16(d0, a0 + 2 * k, b + 2 * k, idesc, acc);
-            if (halves == 2) mma_bf16(d1, a1 + 2 * k, b + 2 * k, idesc, acc);
+            for (int k = 0; k < kTcK / 16; ++k) {
+              const uint32_t acc = (ks > 0 || part > 0 || k > 0) ? 1u : 0u;
+              mma_bf16(d0, a0 + 2 * k, b + 2 * k, idesc, acc);
+              if (halves == 2) mma_bf16(d1, a1 + 2 * k, b + 2 * k, idesc, acc);
+            }
+            mma_commit(&a_empty[as]);
           }
-          mma_commit(&empty[stage]);
+          if (!ok) break;
+          mma_commit(&b_empty[bs]);
         }
-        if (!ok) break;
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
         mma_commit(&acc_full[buf]);
       }
       // all issued MMAs complete before TMEM is released
@@ -301,7 +330,7 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
     const int r = tid - 64;  // B-tile row 0..127
     const int Kh = p.K >> 1, Kb = p.K >> 5;
     long long g = 0;
-    uint8_t* const brow_base = smem + 2 * kTileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+    uint8_t* const brow_base = b_ring + (r >> 3) * 1024 + (r & 7) * 128;
     const int sw = r & 7;
     for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
       const ItemInfo it = decode_item(p, item);
@@ -335,13 +364,13 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
               pq[d][1] = __ldcs(src + 1);
               ps[d] = *reinterpret_cast<const uint16_t*>(sr + 2 * (ks + kPrefetch));
             }
-            const int stage = (int)(g % kPStages);
-            const long long u = g / kPStages;
-            if (u > 0 && !mbar_wait(&empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+            const int stage = (int)(g % kBStages);
+            const long long u = g / kBStages;
+            if (u > 0 && !mbar_wait(&b_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
               *abort_flag = 1;
               stop = true;
             } else {
-              uint8_t* brow = brow_base + stage * kPStageBytes;
+              uint8_t* brow = brow_base + stage * kTileBytes;
               uint4 c[4];
               dequant_block(q0, sc & 0xFFu, c);
 #pragma unroll
@@ -385,17 +414,20 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
             tmem_ld32(tbase + 64 + c0, uv);
             tmem_ld_wait();
             if (valid) {
-              uint16_t* dst = p.act_out + (size_t)row * p.I + 64 * it.nt + c0;
+              // a = hi + lo with hi = bf16(a), lo = bf16(a - hi): 16 significant bits
+              uint16_t* dst = p.act_out + (size_t)row * (2 * p.I) + 128 * it.nt + c0;
 #pragma unroll
               for (int v = 0; v < 32; v += 8) {
-                uint32_t o[4];
+                uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int z = 0; z < 4; ++z) {
                   const float a0 = silu(__uint_as_float(gv[v + 2 * z])) * __uint_as_float(uv[v + 2 * z]);
                   const float a1 = silu(__uint_as_float(gv[v + 2 * z + 1])) * __uint_as_float(uv[v + 2 * z + 1]);
-                  o[z] = f32x2_to_bf16x2(a0, a1);
+                  hi[z] = f32x2_to_bf16x2(a0, a1);
+                  lo[z] = f32x2_to_bf16x2(a0 - bf16_lo(hi[z]), a1 - bf16_hi(hi[z]));
                 }
-                *reinterpret_cast<uint4*>(dst + v) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(dst + v) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(dst + 64 + v) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
               }
             }
           }
@@ -495,7 +527,7 @@ cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K
 
 template <bool GATE_UP>
 cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
-  const size_t smem = 1024 + (size_t)kPStages * kPStageBytes + 256;
+  const size_t smem = 1024 + (size_t)kRingBytes + 256;
   auto kern = tc_gemm_kernel<GATE_UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -510,7 +542,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   CUtensorMap map_x, map_a;
   cudaError_t e = make_act_map(&map_x, a.xs, P, a.H);
   if (e != cudaSuccess) return e;
-  e = make_act_map(&map_a, a.as, P, a.I);
+  e = make_act_map(&map_a, a.as, P, 2 * a.I);
   if (e != cudaSuccess) return e;
 
   timing_mark(1, false, s);
