@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--copies", type=int, default=4, help="rotating weight copies (L2 defeat)")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the timed region")
+    ap.add_argument("--rows", default="sweep,requant,int4,prefill",
+                    help="comma list of secondary measurements to run (sweep, requant, int4, prefill)")
+    ap.add_argument("--prefill-tokens", type=int, default=4096, help="tokens of the prefill row")
     return ap.parse_args()
 
 
@@ -396,7 +399,8 @@ def run_ours(args, rank: int, world: int):
 
     rows = {}
     if not args.no_rows and rank == 0:
-        rows = secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, distinct, dev_batch)
+        rows = secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, distinct, dev_batch,
+                              set(args.rows.split(",")), args.prefill_tokens)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -430,19 +434,66 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
-def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, distinct, dev_batch):
+def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens):
+    """Tensor-core (prefill) path: skewed routing, median of 4 timed calls."""
+    rows = {}
+    T = prefill_tokens
+    pb = [dev_batch(T, 2000 + i, bias=2.0) for i in range(2)]
+    d = m.dims(SHAPE.E, SHAPE.H, SHAPE.I, SHAPE.topk, T, m.MOE_PATH_PREFILL)
+    ws = torch.empty(m.moe_workspace_bytes(d), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, SHAPE.H), dtype=torch.bfloat16, device=dev)
+    flops = 2.0 * T * SHAPE.topk * 3 * SHAPE.H * SHAPE.I
+    ms_list = []
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    for ev in kev:
+        ev.record()
+    lib = m._native.load()
+    for i in range(6):
+        x, ids, w, _ = pb[i % 2]
+        if i == 5:  # per-kernel times of the last call
+            arr = (ctypes.c_void_p * 10)(*[ev.cuda_event for ev in kev])
+            m._native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 5))
+        s_ev.record()
+        m.moe_a16w4_mxfp4(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws,
+                          path=m.MOE_PATH_PREFILL)
+        e_ev.record()
+        e_ev.synchronize()
+        if i >= 2:
+            ms_list.append(s_ev.elapsed_time(e_ev))
+    ms = statistics.median(ms_list)
+    tf = flops / (ms * 1e-3) / 1e12
+    names = ["route", "gather", "gemm1_gate_up_tc", "gemm2_down_tc", "cast"]
+    kms = {n: round(kev[2 * q].elapsed_time(kev[2 * q + 1]), 3) for q, n in enumerate(names)}
+    rows[f"mxfp4_prefill_T{T}_skewed"] = {
+        "ms_per_call": round(ms, 3), "TFLOPs_useful": round(tf, 1), "kernels_ms": kms,
+        "bf16_frac_burst": round(tf / peaks["bf16_tflops"], 3),
+        "bf16_frac_sustained": round(tf / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]), 3),
+        "useful_flops": flops}
+    del ws, out
+    torch.cuda.empty_cache()
+    return rows
+
+
+def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, distinct, dev_batch, which,
+                   prefill_tokens):
     rows = {}
     reps = 10
+    if "prefill" in which:
+        rows.update(prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens))
     # decode sweep
     sweep = {}
-    for T in (4, 7, 16, 32):
+    for T in ((4, 7, 16, 32) if "sweep" in which else ()):
         g, _, nbytes, _ = capture(T, 8)
         time_graph(g, 2)
         ms = time_graph(g, reps) / reps
         us = ms * 1000 / 8
         gbs = nbytes / (ms * 1e-3) / 1e9
         sweep[f"T{T}"] = {"us_per_call": round(us, 2), "GBps": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
-    rows["mxfp4_decode_sweep"] = sweep
+    if sweep:
+        rows["mxfp4_decode_sweep"] = sweep
+    if not ({"requant", "int4"} & which):
+        return rows
     # requantiser over all experts (w13 and w2), then the int4 MoE
     q_copies = []
     s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -474,33 +525,6 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
                        "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
     rows["int4g32_decode"] = i4
     del q_copies
-    torch.cuda.empty_cache()
-    # tensor-core (prefill) path: 4096 tokens, skewed routing
-    T = 4096
-    pb = [dev_batch(T, 2000 + i, bias=2.0) for i in range(2)]
-    d = m.dims(SHAPE.E, SHAPE.H, SHAPE.I, SHAPE.topk, T, m.MOE_PATH_PREFILL)
-    ws = torch.empty(m.moe_workspace_bytes(d), dtype=torch.uint8, device=dev)
-    out = torch.empty((T, SHAPE.H), dtype=torch.bfloat16, device=dev)
-    flops = 2.0 * T * SHAPE.topk * 3 * SHAPE.H * SHAPE.I
-    ms_list = []
-    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(6):
-        x, ids, w, _ = pb[i % 2]
-        s_ev.record()
-        m.moe_a16w4_mxfp4(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws,
-                          path=m.MOE_PATH_PREFILL)
-        e_ev.record()
-        e_ev.synchronize()
-        if i >= 2:
-            ms_list.append(s_ev.elapsed_time(e_ev))
-    ms = statistics.median(ms_list)
-    tf = flops / (ms * 1e-3) / 1e12
-    rows["mxfp4_prefill_T4096_skewed"] = {
-        "ms_per_call": round(ms, 3), "TFLOPs_useful": round(tf, 1),
-        "bf16_frac_burst": round(tf / peaks["bf16_tflops"], 3),
-        "bf16_frac_sustained": round(tf / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]), 3),
-        "useful_flops": flops}
-    del ws, out
     torch.cuda.empty_cache()
     return rows
 

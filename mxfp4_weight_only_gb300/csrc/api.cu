@@ -108,8 +108,15 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
 }  // namespace
 
 void timing_mark(int index, bool end, cudaStream_t s) {
-  // External records also become event nodes when the stream is being captured.
-  if (index < g_timing.n) cudaEventRecordWithFlags(g_timing.ev[2 * index + (end ? 1 : 0)], s, cudaEventRecordExternal);
+  if (index >= g_timing.n) return;
+  cudaEvent_t ev = g_timing.ev[2 * index + (end ? 1 : 0)];
+  // Under stream capture only an external record becomes an event node of the
+  // graph; outside capture a plain record is used.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
 }
 
 bool dims_valid(const moe_dims_t* d) {

@@ -16,7 +16,7 @@
 // units of one CTA share an expert and group, so its activations stay in
 // registers across units.
 //
-// Per CTA (15 warps): one producer warp streams each unit's 32 weight rows
+// Per CTA (16 warps): one producer warp streams each unit's 32 weight rows
 // (one cp.async.bulk per row into a padded shared-memory stage, so consumer
 // reads are bank-conflict-free) and their scales through an mbarrier ring.
 // Fourteen consumer warps split K.  Each turns its part of the packed rows into
@@ -26,8 +26,9 @@
 // applied to each block's fp32 partial sum (E8M0 pairs decoded with
 // cvt.rn.bf16x2.ue8m0x2, exact).  Activations enter the MMA as f16 scaled by a
 // power of two per (pair, warp K-range) so they cannot overflow; the scale is
-// removed in fp32 afterwards.  Partial sums of the consumer warps are reduced
-// through shared memory.
+// removed in fp32 afterwards.  The consumer warps hand their partial sums to an
+// epilogue warp through a ring of shared-memory buffers; it reduces them and
+// writes the results while the consumers go on with the next units.
 #include "common.cuh"
 
 namespace moe {
@@ -35,14 +36,16 @@ namespace moe {
 namespace {
 
 constexpr int kConsumerWarps = 14;
-constexpr int kDecThreads = (kConsumerWarps + 1) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kProducerWarp = kConsumerWarps;      // streams weights
+constexpr int kEpilogueWarp = kConsumerWarps + 1;  // reduces partial sums, writes results
+constexpr int kDecThreads = (kConsumerWarps + 2) * 32;
 constexpr int kTiles = 2;             // 16-row MMA tiles per item
 constexpr int kRows = 16 * kTiles;    // weight rows per item
 constexpr int kGroup = 8;             // pair columns per group (one 8-column MMA block)
 constexpr int kRedFloats = kConsumerWarps * kRows * kGroup;  // one reduction buffer
+constexpr int kRedBufs = 3;                                  // reduction ring depth
 static_assert(kGroup == kMoeGroup, "routing and the decode kernels must agree on the group size");
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kSmemBudget = 226 * 1024;
 
 struct GemmParams {
   const uint8_t* w;        // packed weights [E][N][K/2]
@@ -203,18 +206,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   const int S = p.n_stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + S;
-  uint64_t* redbar = empty + S;  // [2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(redbar + 2);
-  float* red = reinterpret_cast<float*>(smem + 1024);  // [2][warps][32 rows][16 pair columns]
-  uint8_t* stages = smem + 1024 + 2 * kRedFloats * sizeof(float);
+  uint64_t* red_full = empty + S;            // [kRedBufs]
+  uint64_t* red_empty = red_full + kRedBufs;  // [kRedBufs]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + kRedBufs);
+  float* red = reinterpret_cast<float*>(smem + 1024);  // [kRedBufs][warps][32 rows][8 pair columns]
+  uint8_t* stages = smem + 1024 + kRedBufs * kRedFloats * sizeof(float);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    mbar_init(&redbar[0], kConsumerWarps);
-    mbar_init(&redbar[1], kConsumerWarps);
+    for (int b = 0; b < kRedBufs; ++b) {
+      mbar_init(&red_full[b], kConsumerWarps);
+      mbar_init(&red_empty[b], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     d0 = lo;
   }
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
     long long issued = 0;
@@ -284,6 +290,61 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     return;
   }
 
+  if (warp == kEpilogueWarp) {
+    // ------------------------------------------------------------ epilogue
+    // Sums the consumer warps' partials of each unit and writes the results,
+    // while the consumers already work on the next units.
+    long long it = 0;
+    int d = d0;
+    for (long long u = u0; u < u1; ++u, ++it) {
+      while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
+      const long long rem = u - (long long)p.gprefix[d] * p.tiles;
+      const int grp = (int)(rem / p.tiles), j = (int)(rem % p.tiles);
+      const int e = p.active[d];
+      const int base = p.offsets[e];
+      const int npairs = p.offsets[e + 1] - base;
+      const int rbuf = (int)(it % kRedBufs);
+      if (!mbar_wait(&red_full[rbuf], (uint32_t)((it / kRedBufs) & 1), p.status)) {
+        *abort_flag = 1;
+        break;
+      }
+      const float* rb = red + rbuf * kRedFloats;
+      if (GATE_UP) {
+        constexpr int kOut = kRows / 2;  // activated outputs per unit
+#pragma unroll
+        for (int q = 0; q < kOut * kGroup / 32; ++q) {
+          const int idx = lane + 32 * q;
+          const int r = idx / kGroup, c = idx % kGroup;
+          float hg = 0.f, hu = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            hg += rb[w * kRows * kGroup + r * kGroup + c];
+            hu += rb[w * kRows * kGroup + (r + kOut) * kGroup + c];
+          }
+          const int slot = grp * kGroup + c;
+          if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + kOut * j + r] = silu(hg) * hu;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < kRows * kGroup / 32; ++q) {
+          const int idx = lane + 32 * q;
+          const int r = idx / kGroup, c = idx % kGroup;
+          float y = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + r * kGroup + c];
+          const int slot = grp * kGroup + c;
+          if (slot < npairs) {
+            const int pair = p.sorted_pair[base + slot];
+            p.dst[(size_t)pair * p.N + kRows * j + r] = y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_empty[rbuf]);
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
   // even number of blocks per warp, so blocks are processed in pairs
@@ -302,7 +363,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     if (*abort_flag) break;
     while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
     const long long rem = u - (long long)p.gprefix[d] * p.tiles;
-    const int grp = (int)(rem / p.tiles), j = (int)(rem % p.tiles);
+    const int grp = (int)(rem / p.tiles);
     const int stage = (int)(it % S);
     const int e = p.active[d];
     const int base = p.offsets[e];
@@ -353,10 +414,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
 
-    // ---- cross-warp reduction and epilogue
-    const int buf = (int)(it & 1);
-    float* rb = red + buf * kRedFloats;
-    float* rw = rb + warp * (kRows * kGroup);
+    // ---- hand the partial sums to the epilogue warp
+    const int rbuf = (int)(it % kRedBufs);
+    if (it >= kRedBufs && !mbar_wait(&red_empty[rbuf], (uint32_t)((it / kRedBufs - 1) & 1), p.status)) {
+      *abort_flag = 1;
+      break;
+    }
+    float* rw = red + rbuf * kRedFloats + warp * (kRows * kGroup);
 #pragma unroll
     for (int tl = 0; tl < kTiles; ++tl) {
       const int r = 16 * tl + g;
@@ -365,39 +429,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
           make_float2(acc[tl][2] * inv[0], acc[tl][3] * inv[1]);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&redbar[buf]);
-    // every consumer waits: a warp may only write this buffer again two units
-    // later, after all warps have arrived at the unit in between
-    if (!mbar_wait(&redbar[buf], (uint32_t)((it >> 1) & 1), p.status)) {
-      *abort_flag = 1;
-      break;
-    }
-    if (GATE_UP) {
-      constexpr int kOut = kRows / 2;  // activated outputs per unit
-      for (int idx = tid; idx < kOut * kGroup; idx += kConsumerThreads) {
-        const int c = idx / kOut, r = idx % kOut;
-        float hg = 0.f, hu = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          hg += rb[w * kRows * kGroup + r * kGroup + c];
-          hu += rb[w * kRows * kGroup + (r + kOut) * kGroup + c];
-        }
-        const int slot = grp * kGroup + c;
-        if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + kOut * j + r] = silu(hg) * hu;
-      }
-    } else {
-      for (int idx = tid; idx < kRows * kGroup; idx += kConsumerThreads) {
-        const int c = idx / kRows, r = idx % kRows;
-        float y = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + r * kGroup + c];
-        const int slot = grp * kGroup + c;
-        if (slot < npairs) {
-          const int pair = p.sorted_pair[base + slot];
-          p.dst[(size_t)pair * p.N + kRows * j + r] = y;
-        }
-      }
-    }
+    if (lane == 0) mbar_arrive(&red_full[rbuf]);
   }
 }
 
@@ -445,7 +477,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 
 template <WeightKind KIND, bool GATE_UP, int NBW>
 cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
-  const size_t smem = 1024 + 2 * kRedFloats * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
+  const size_t smem = 1024 + kRedBufs * kRedFloats * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -466,7 +498,7 @@ void fill_stage_geometry(GemmParams& gp, WeightKind kind) {
   gp.srow_bytes = (gp.K >> 5) * (kind == WeightKind::kMxfp4 ? 1 : 4);
   const int raw = kRows * gp.row_stride + kRows * gp.srow_bytes;
   gp.stage_bytes = (raw + 127) & ~127;
-  const int avail = kSmemBudget - 1024 - 2 * kRedFloats * (int)sizeof(float);
+  const int avail = kSmemBudget - 1024 - kRedBufs * kRedFloats * (int)sizeof(float);
   int st = avail / gp.stage_bytes;
   gp.n_stages = st > 8 ? 8 : st;
 }
