@@ -62,7 +62,9 @@ extern "C" {
  *   topk  experts per token                                1 <= topk <= 64
  *   T     tokens                                           0 <= T, T*topk <= 2^24
  *   act   MOE_ACT_SWIGLU
- *   path  MOE_PATH_*; the tensor-core path additionally needs H and I multiples of 512
+ *   path  MOE_PATH_*; the tensor-core path additionally needs H and I to be
+ *         multiples of 512 and at most 4096 (MOE_PATH_AUTO falls back to the
+ *         weight-streaming kernels otherwise)
  */
 typedef struct moe_dims {
   int32_t E, H, I, topk, T;

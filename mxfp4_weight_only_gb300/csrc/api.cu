@@ -132,7 +132,9 @@ bool dims_valid(const moe_dims_t* d) {
 
 bool use_prefill(const moe_dims_t* d, WeightKind kind) {
   if (kind != WeightKind::kMxfp4) return false;
-  const bool ok = (d->H % 512 == 0) && (d->I % 512 == 0) && kPrefillAvailable;
+  // the tensor-core kernels stage a 128-byte-wide K slice of packed weights
+  // and one item's scales (K/32 <= 128 bytes per row) in shared memory
+  const bool ok = (d->H % 512 == 0) && (d->I % 512 == 0) && d->H <= 4096 && d->I <= 4096 && kPrefillAvailable;
   if (d->path == MOE_PATH_PREFILL) return ok;
   if (d->path == MOE_PATH_DECODE) return false;
   return ok && d->T >= kPrefillMinTokens;

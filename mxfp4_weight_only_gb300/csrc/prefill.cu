@@ -21,11 +21,14 @@
 //   warp 1      TMEM owner and MMA issuer (one thread): 128x128x16 bf16 MMAs,
 //               f32 accumulators in TMEM, two accumulator sets (one per
 //               128-row half) double-buffered across items (512 columns)
-//   warps 2-5   weight producers: each thread owns one weight row, streams
-//               its packed E2M1 bytes and E8M0 scales from global memory
-//               (8 K steps ahead in registers), converts them exactly to bf16
-//               (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by the
-//               block scale) and writes the 128x64 swizzled B tile
+//               lane 1: TMA for the packed E2M1 weights (128 rows x 128
+//               bytes = 4 K steps per stage, 128-byte swizzle) and, once per
+//               item, the E8M0 scales of its 128 weight rows
+//   warps 2-5   weight converters: each thread owns one weight row, reads its
+//               packed bytes and scales from shared memory, converts them
+//               exactly to bf16 (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias,
+//               multiply by the block scale) and writes the 128x64 swizzled
+//               B tile
 //   warps 6-9   epilogue: tcgen05.ld of the accumulators, SiLU gating (gemm1)
 //               or router-weighted scatter-add (gemm2), global stores
 // Each 128x64 B tile feeds the MMAs of both 128-row halves (and, in the down
@@ -42,12 +45,16 @@ namespace {
 
 constexpr int kPThreads = 320;
 constexpr int kTileBytes = 128 * 128;         // 128 rows x 64 bf16
-constexpr int kAStages = 4;                   // activation ring: two 128-row halves per stage
+constexpr int kAStages = 3;                   // activation ring: two 128-row halves per stage
 constexpr int kAStageBytes = 2 * kTileBytes;
-constexpr int kBStages = 4;                   // weight ring: one 128 x 64 tile per stage
-constexpr int kRingBytes = kAStages * kAStageBytes + kBStages * kTileBytes;
+constexpr int kBStages = 3;                   // bf16 weight ring: one 128 x 64 tile per stage
+constexpr int kRawStages = 2;                 // packed weight ring: 128 rows x 128 bytes (4 K steps)
+constexpr int kRawBytes = 128 * 128;
+constexpr int kRawSteps = 4;                  // K steps per packed stage
+constexpr int kScaleBytes = 128 * 128;        // E8M0 scales of one item: 128 rows x K/32 (<= 128) bytes
+constexpr int kRingBytes =
+    kAStages * kAStageBytes + kBStages * kTileBytes + kRawStages * kRawBytes + 2 * kScaleBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPrefetch = 8;  // K steps of packed weights in flight per converter thread
 
 struct TcParams {
   const uint8_t* w;   // packed [E][N][K/2]
@@ -199,17 +206,25 @@ __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long ite
 
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                               const __grid_constant__ CUtensorMap tmap_w,
+                                                               const __grid_constant__ CUtensorMap tmap_s,
                                                                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_ring = smem;
-  uint8_t* b_ring = smem + kAStages * kAStageBytes;
+  uint8_t* b_ring = a_ring + kAStages * kAStageBytes;
+  uint8_t* raw_ring = b_ring + kBStages * kTileBytes;
+  uint8_t* sc_buf = raw_ring + kRawStages * kRawBytes;  // [2][128 rows][K/32]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
   uint64_t* a_full = bars;
   uint64_t* a_empty = a_full + kAStages;
   uint64_t* b_full = a_empty + kAStages;
   uint64_t* b_empty = b_full + kBStages;
-  uint64_t* acc_full = b_empty + kBStages;
+  uint64_t* raw_full = b_empty + kBStages;
+  uint64_t* raw_empty = raw_full + kRawStages;
+  uint64_t* sc_full = raw_empty + kRawStages;
+  uint64_t* sc_empty = sc_full + 2;
+  uint64_t* acc_full = sc_empty + 2;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -224,6 +239,14 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(&b_full[s], 4);
       mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sc_full[s], 1);
+      mbar_init(&sc_empty[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -271,6 +294,43 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
       // nothing issued may still be in flight when the CTA exits
       const long long first = g > kAStages ? g - kAStages : 0;
       for (long long v = first; v < g; ++v) mbar_wait(&a_full[v % kAStages], (uint32_t)((v / kAStages) & 1), p.status);
+    } else if (lane == 1) {
+      // packed weights (128 rows x 128 bytes per stage) and each item's scales
+      const int Kb = p.K >> 5;
+      const int n_raw = (p.K >> 1) / 128;
+      long long g = 0, j = 0;
+      bool stop = false;
+      for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
+        const ItemInfo it = decode_item(p, item);
+        // weight rows of this N tile: two blocks of 64 (gate and up rows for gate_up)
+        const int row_a = it.e * p.N + (GATE_UP ? 64 * it.nt : kTcN * it.nt);
+        const int row_b = GATE_UP ? it.e * p.N + p.I + 64 * it.nt : row_a + 64;
+        const int sb = (int)(j & 1);
+        if (j >= 2 && !mbar_wait(&sc_empty[sb], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&sc_full[sb], 128 * Kb);
+        tma_load_2d(sc_buf + sb * kScaleBytes, &tmap_s, 0, row_a, &sc_full[sb]);
+        tma_load_2d(sc_buf + sb * kScaleBytes + 64 * Kb, &tmap_s, 0, row_b, &sc_full[sb]);
+        for (int rs = 0; rs < n_raw; ++rs, ++g) {
+          const int stage = (int)(g % kRawStages);
+          const long long u = g / kRawStages;
+          if (u > 0 && !mbar_wait(&raw_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          uint8_t* st = raw_ring + stage * kRawBytes;
+          mbar_arrive_expect_tx(&raw_full[stage], kRawBytes);
+          tma_load_2d(st, &tmap_w, rs * 128, row_a, &raw_full[stage]);
+          tma_load_2d(st + 64 * 128, &tmap_w, rs * 128, row_b, &raw_full[stage]);
+        }
+      }
+      const long long first = g > kRawStages ? g - kRawStages : 0;
+      for (long long v = first; v < g; ++v)
+        mbar_wait(&raw_full[v % kRawStages], (uint32_t)((v / kRawStages) & 1), p.status);
+      for (long long v = j > 2 ? j - 2 : 0; v < j; ++v) mbar_wait(&sc_full[v & 1], (uint32_t)((v >> 1) & 1), p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -328,65 +388,58 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
   } else if (warp < 6) {
     // ------------------------------------------------------------------ weight converters
     const int r = tid - 64;  // B-tile row 0..127
-    const int Kh = p.K >> 1, Kb = p.K >> 5;
-    long long g = 0;
+    const int Kb = p.K >> 5;
+    long long g = 0, graw = 0, j = 0;
     uint8_t* const brow_base = b_ring + (r >> 3) * 1024 + (r & 7) * 128;
     const int sw = r & 7;
-    for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
-      const ItemInfo it = decode_item(p, item);
-      int wrow;
-      if (GATE_UP) wrow = r < 64 ? 64 * it.nt + r : p.I + 64 * it.nt + (r - 64);
-      else wrow = kTcN * it.nt + r;
-      const uint8_t* wr = p.w + ((size_t)it.e * p.N + wrow) * Kh;
-      const uint8_t* sr = p.ws + ((size_t)it.e * p.N + wrow) * Kb;
-      uint4 pq[kPrefetch][2];
-      uint32_t ps[kPrefetch];
-#pragma unroll
-      for (int d = 0; d < kPrefetch; ++d) {
-        if (d < KS) {
-          const uint4* src = reinterpret_cast<const uint4*>(wr + d * 32);
-          pq[d][0] = __ldcs(src);
-          pq[d][1] = __ldcs(src + 1);
-          ps[d] = *reinterpret_cast<const uint16_t*>(sr + 2 * d);
-        }
+    const int n_raw = (p.K >> 1) / 128;
+    bool stop = false;
+    for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
+      const int sb = (int)(j & 1);
+      if (!mbar_wait(&sc_full[sb], (uint32_t)((j >> 1) & 1), p.status)) {
+        *abort_flag = 1;
+        break;
       }
-      bool stop = false;
-      for (int ks0 = 0; ks0 < KS && !stop; ks0 += kPrefetch) {
+      const uint8_t* srow = sc_buf + sb * kScaleBytes + r * Kb;
+      for (int rs = 0; rs < n_raw && !stop; ++rs, ++graw) {
+        const int rstage = (int)(graw % kRawStages);
+        if (!mbar_wait(&raw_full[rstage], (uint32_t)((graw / kRawStages) & 1), p.status)) {
+          *abort_flag = 1;
+          stop = true;
+          break;
+        }
+        // row r of the packed stage: 128 bytes, 16-byte chunks swizzled by (r & 7)
+        const uint8_t* rrow = raw_ring + rstage * kRawBytes + r * 128;
 #pragma unroll
-        for (int d = 0; d < kPrefetch; ++d) {
-          const int ks = ks0 + d;
-          if (ks < KS && !stop) {
-            const uint4 q0 = pq[d][0], q1 = pq[d][1];
-            const uint32_t sc = ps[d];
-            if (ks + kPrefetch < KS) {
-              const uint4* src = reinterpret_cast<const uint4*>(wr + (ks + kPrefetch) * 32);
-              pq[d][0] = __ldcs(src);
-              pq[d][1] = __ldcs(src + 1);
-              ps[d] = *reinterpret_cast<const uint16_t*>(sr + 2 * (ks + kPrefetch));
-            }
-            const int stage = (int)(g % kBStages);
-            const long long u = g / kBStages;
-            if (u > 0 && !mbar_wait(&b_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
-              *abort_flag = 1;
-              stop = true;
-            } else {
-              uint8_t* brow = brow_base + stage * kTileBytes;
-              uint4 c[4];
-              dequant_block(q0, sc & 0xFFu, c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + ((i ^ sw) << 4)) = c[i];
-              dequant_block(q1, sc >> 8, c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + (((4 + i) ^ sw) << 4)) = c[i];
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&b_full[stage]);
-              ++g;
-            }
+        for (int q = 0; q < kRawSteps; ++q, ++g) {
+          const int ks = rs * kRawSteps + q;
+          const uint4 q0 = *reinterpret_cast<const uint4*>(rrow + (((2 * q) ^ sw) << 4));
+          const uint4 q1 = *reinterpret_cast<const uint4*>(rrow + (((2 * q + 1) ^ sw) << 4));
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(srow + 2 * ks);
+          const int stage = (int)(g % kBStages);
+          const long long u = g / kBStages;
+          if (u > 0 && !mbar_wait(&b_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+            *abort_flag = 1;
+            stop = true;
+            break;
           }
+          uint8_t* brow = brow_base + stage * kTileBytes;
+          uint4 c[4];
+          dequant_block(q0, sc & 0xFFu, c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + ((i ^ sw) << 4)) = c[i];
+          dequant_block(q1, sc >> 8, c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + (((4 + i) ^ sw) << 4)) = c[i];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b_full[stage]);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rstage]);
       }
-      if (stop) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc_empty[sb]);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -525,13 +578,34 @@ cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Packed weights or scales, uint8 [rows][cols], boxes of box_cols x 64 rows
+// (128-byte swizzle for the 128-byte packed-weight boxes).
+cudaError_t make_u8_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_cols, bool swizzle) {
+  EncodeTiledFn enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, 64u};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <bool GATE_UP>
-cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s, int E) {
+  CUtensorMap map_w, map_s;
+  cudaError_t e0 = make_u8_map(&map_w, p.w, (long long)E * p.N, p.K / 2, 128, true);
+  if (e0 != cudaSuccess) return e0;
+  e0 = make_u8_map(&map_s, p.ws, (long long)E * p.N, p.K / 32, p.K / 32, false);
+  if (e0 != cudaSuccess) return e0;
   const size_t smem = 1024 + (size_t)kRingBytes + 256;
   auto kern = tc_gemm_kernel<GATE_UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kPThreads, smem, s>>>(map, p);
+  kern<<<grid, kPThreads, smem, s>>>(map, map_w, map_s, p);
   return cudaGetLastError();
 }
 
@@ -571,7 +645,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.outacc = a.outacc;
   p.status = a.status;
   timing_mark(2, false, s);
-  e = launch_tc<true>(map_x, p, a.num_sms, s);
+  e = launch_tc<true>(map_x, p, a.num_sms, s, a.E);
   timing_mark(2, true, s);
   if (e != cudaSuccess) return e;
 
@@ -583,7 +657,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.K = a.I;
   p2.n_tiles = a.H / kTcN;
   timing_mark(3, false, s);
-  e = launch_tc<false>(map_a, p2, a.num_sms, s);
+  e = launch_tc<false>(map_a, p2, a.num_sms, s, a.E);
   timing_mark(3, true, s);
   if (e != cudaSuccess) return e;
 

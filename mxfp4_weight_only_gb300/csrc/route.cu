@@ -5,9 +5,9 @@
 // receives topk_ids[T, topk]; the grouped GEMMs need each expert's pairs
 // contiguous.  Pairs keep ascending flat index p = t*topk + k inside each
 // expert, ids outside [0, E) are dropped.  Besides counts/offsets/order this
-// kernel emits the list of active experts (weight-streaming kernels iterate
-// over it) and, on request, the list of 256-row M tiles per expert for the
-// tensor-core kernels.
+// kernel emits the list of active experts with their 8-pair group counts
+// (the weight-streaming kernels iterate over it) and, on request, the list of
+// 256-row M tiles per expert for the tensor-core kernels.
 #include "common.cuh"
 
 namespace moe {
@@ -45,25 +45,47 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const int32_t* __restrict__ ids, int E, int P, RouteOut r, int make_mtiles) {
+    route_kernel(const int32_t* __restrict__ ids, int E, int T, int topk, RouteOut r, int make_mtiles) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;           // [E]
   int32_t* base = sm + E;      // [E]
   int32_t* wcnt = sm + 2 * E;  // [32][E]
   __shared__ int scratch[33];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = T * topk;
 
   for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
+  // one pair per thread stays in a register when P fits one pass
+  const int my_e = tid < P ? ids[tid] : -1;
   __syncthreads();
-  for (int p = tid; p < P; p += kRouteThreads) {
-    const int e = ids[p];
-    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+  if (P <= kRouteThreads) {
+    if ((unsigned)my_e < (unsigned)E) atomicAdd(&cnt[my_e], 1);
+  } else {
+    for (int p = tid; p < P; p += kRouteThreads) {
+      const int e = ids[p];
+      if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    }
   }
   __syncthreads();
 
-  int total = 0;
   const int v = tid < E ? cnt[tid] : 0;
-  const int excl = block_excl_scan(v, scratch, &total);
+  const int ng = (v + kMoeGroup - 1) / kMoeGroup;
+  int excl, apos, gpos, total, n_act, n_groups;
+  if (P < 1024) {
+    // counts < 2^11, active flags < 2^11, groups < 2^10: one packed scan
+    int tot = 0;
+    const int packed = block_excl_scan(v | ((v > 0 ? 1 : 0) << 11) | (ng << 22), scratch, &tot);
+    excl = packed & 0x7FF;
+    apos = (packed >> 11) & 0x7FF;
+    gpos = (packed >> 22) & 0x3FF;
+    total = tot & 0x7FF;
+    n_act = (tot >> 11) & 0x7FF;
+    n_groups = (tot >> 22) & 0x3FF;
+  } else {
+    excl = block_excl_scan(v, scratch, &total);
+    apos = block_excl_scan(v > 0 ? 1 : 0, scratch, &n_act);
+    gpos = block_excl_scan(ng, scratch, &n_groups);
+  }
   if (tid < E) {
     r.counts[tid] = v;
     r.offsets[tid] = excl;
@@ -71,18 +93,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   if (tid == 0) r.offsets[E] = total;
   const int n_valid = total;
-
-  int n_act = 0;
-  const int apos = block_excl_scan(v > 0 ? 1 : 0, scratch, &n_act);
   if (r.active) {
-    if (tid < E && v > 0) r.active[apos] = tid;
-    if (tid == 0) *r.n_active = n_act;
-    // activation groups per active expert, prefix-summed in active-list order
-    int n_groups = 0;
-    const int ng = (v + kMoeGroup - 1) / kMoeGroup;
-    const int gpos = block_excl_scan(ng, scratch, &n_groups);
-    if (tid < E && v > 0) r.gprefix[apos] = gpos;
-    if (tid == 0) r.gprefix[n_act] = n_groups;
+    if (tid < E && v > 0) {
+      r.active[apos] = tid;
+      r.gprefix[apos] = gpos;  // activation groups per active expert, in active-list order
+    }
+    if (tid == 0) {
+      *r.n_active = n_act;
+      r.gprefix[n_act] = n_groups;
+    }
   }
 
   if (make_mtiles) {
@@ -95,34 +114,50 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   __syncthreads();
 
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < P; c0 += kRouteThreads) {
-    for (int i = tid; i < 32 * E; i += kRouteThreads) wcnt[i] = 0;
-    const int p = c0 + tid;
-    const int e = p < P ? ids[p] : -1;
-    const bool valid = p < P && (unsigned)e < (unsigned)E;
-    __syncthreads();
-    const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-    const int rank = __popc(peers & lt_mask);
-    if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
-    __syncthreads();
-    int run = 0;
-    if (tid < E) {
-      for (int w = 0; w < 32; ++w) {
-        const int t = wcnt[w * E + tid];
-        wcnt[w * E + tid] = run;
-        run += t;
+  if (P <= 32) {
+    // one warp holds every pair: its rank among equal ids is the position in the group
+    if (warp == 0) {
+      const bool valid = tid < P && (unsigned)my_e < (unsigned)E;
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? my_e : -1);
+      const int rank = __popc(peers & lt_mask);
+      if (valid) {
+        const int pos = base[my_e] + rank;
+        r.sorted_pair[pos] = tid;
+        r.pair_pos[tid] = pos;
+      } else if (tid < P) {
+        r.pair_pos[tid] = -1;
       }
     }
-    __syncthreads();
-    if (valid) {
-      const int pos = base[e] + wcnt[warp * E + e] + rank;
-      r.sorted_pair[pos] = p;
-      r.pair_pos[p] = pos;
-    } else if (p < P) {
-      r.pair_pos[p] = -1;
+  } else {
+    for (int c0 = 0; c0 < P; c0 += kRouteThreads) {
+      for (int i = tid; i < 32 * E; i += kRouteThreads) wcnt[i] = 0;
+      const int p = c0 + tid;
+      const int e = p < P ? (c0 == 0 ? my_e : ids[p]) : -1;
+      const bool valid = p < P && (unsigned)e < (unsigned)E;
+      __syncthreads();
+      const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+      const int rank = __popc(peers & lt_mask);
+      if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
+      __syncthreads();
+      int run = 0;
+      if (tid < E) {
+        for (int w = 0; w < 32; ++w) {
+          const int t = wcnt[w * E + tid];
+          wcnt[w * E + tid] = run;
+          run += t;
+        }
+      }
+      __syncthreads();
+      if (valid) {
+        const int pos = base[e] + wcnt[warp * E + e] + rank;
+        r.sorted_pair[pos] = p;
+        r.pair_pos[p] = pos;
+      } else if (p < P) {
+        r.pair_pos[p] = -1;
+      }
+      __syncthreads();
+      if (tid < E) base[tid] += run;
     }
-    __syncthreads();
-    if (tid < E) base[tid] += run;
   }
   for (int i = n_valid + tid; i < P; i += kRouteThreads) r.sorted_pair[i] = -1;
 }
@@ -134,7 +169,7 @@ cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const 
   const size_t smem = (size_t)34 * E * sizeof(int32_t);
   cudaError_t err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  route_kernel<<<1, kRouteThreads, smem, s>>>(topk_ids, E, T * topk, r, make_mtiles);
+  route_kernel<<<1, kRouteThreads, smem, s>>>(topk_ids, E, T, topk, r, make_mtiles);
   return cudaGetLastError();
 }
 
