@@ -153,7 +153,7 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.gprefix = o; o = align256(o + 4 * (E + 1));
   L.sorted_pair = o; o = align256(o + 4 * P);
   L.pair_pos = o; o = align256(o + 4 * P);
-  L.mtiles = o; o = align256(o + 4 * (P / kTcM + E + 1));
+  L.mtiles = o; o = align256(o + 4 * (P / kTcRows + E + 1));
   L.n_mtiles = o; o = align256(o + 4);
   if (L.prefill) {
     L.xs = o; o = align256(o + 2 * P * H);

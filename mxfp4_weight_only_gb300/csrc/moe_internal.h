@@ -23,11 +23,12 @@ constexpr int kPrefillMinTokens = 64;
 // Whether the tensor-core (prefill) kernels are built into this library.
 constexpr bool kPrefillAvailable = true;
 
-// Prefill tile sizes (tcgen05, cta_group::1).
-constexpr int kTcM = 128;  // rows of x per M tile
-constexpr int kTcN = 128;  // weight rows per N tile
-constexpr int kTcK = 64;   // K per pipeline step (one 128-byte swizzle row of bf16)
-constexpr int kTcRows = 2 * kTcM;  // sorted rows per work item (two M tiles share each weight tile)
+// Prefill tile sizes (tcgen05, cta_group::1).  The MMA's M side is a tile of
+// 128 dequantised weight rows held in tensor memory; its N side is a tile of
+// up to kTcRows sorted activation rows of one expert in shared memory.
+constexpr int kTcW = 128;     // weight rows per work item (MMA M)
+constexpr int kTcK = 64;      // K per pipeline step (one 128-byte swizzle row of bf16)
+constexpr int kTcRows = 192;  // sorted activation rows per work item (MMA N, at most)
 
 enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
 

@@ -1,40 +1,40 @@
-// Tensor-core grouped GEMMs for large batches (prefill): tcgen05 MMAs with TMEM
-// accumulators, activations by TMA, MXFP4 weights dequantised to bf16 in
-// shared memory.
+// Tensor-core grouped GEMMs for large batches (prefill): tcgen05 MMAs with the
+// dequantised weights and the accumulators in tensor memory, activations by
+// TMA in shared memory.
 //
 // Same two stages as the weight-streaming path (Mxfp4MoEMethod.apply on the
 // vLLM quantization/mxfp4 API page, gate_up ``w13`` then down ``w2``), laid
 // out for a dense contraction:
 //   gather:  xs[i] = x[token of sorted pair i]                 (bf16 rows)
-//   gemm1:   h = xs W13[e]^T, a = SiLU(h_gate) * h_up -> as    (a as bf16
+//   gemm1:   h = W13[e] xs^T, a = SiLU(h_gate) * h_up -> as    (a as bf16
 //            hi + lo parts, interleaved per 64 columns: 16 significant bits)
-//   gemm2:   y = [a_hi a_lo] [W2[e] W2[e]]^T, outacc[t] += topk_w * y
+//   gemm2:   y = W2[e] [a_hi + a_lo]^T, outacc[t] += topk_w * y
 //                                                              (fp32, red.add)
 //   cast:    out = bf16(outacc)
 //
-// Work item = (expert, up to 256 sorted rows, one N tile of 128 weight rows;
-// gemm1 tiles hold 64 gate rows and the matching 64 up rows).  One CTA per
-// SM walks items round-robin.  Warp roles per CTA:
-//   warp 0      TMA producer: two 128x64 bf16 activation tiles per K step
-//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads);
-//               the down GEMM loads the hi and the lo tiles of each K step
-//   warp 1      TMEM owner and MMA issuer (one thread): 128x128x16 bf16 MMAs,
-//               f32 accumulators in TMEM, two accumulator sets (one per
-//               128-row half) double-buffered across items (512 columns)
-//               lane 1: TMA for the packed E2M1 weights (128 rows x 128
-//               bytes = 4 K steps per stage, 128-byte swizzle) and, once per
-//               item, the E8M0 scales of its 128 weight rows
-//   warps 2-5   weight converters: each thread owns one weight row, reads its
-//               packed bytes and scales from shared memory, converts them
-//               exactly to bf16 (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias,
-//               multiply by the block scale) and writes the 128x64 swizzled
-//               B tile
-//   warps 6-9   epilogue: tcgen05.ld of the accumulators, SiLU gating (gemm1)
+// Work item = (expert, up to 192 of its sorted rows, one tile of 128 weight
+// rows; gemm1 tiles hold 64 gate rows and the matching 64 up rows).  The MMA
+// is D[128 weight rows][rows] += W[128][16] X[rows][16]^T: M = 128 from the
+// weight tile in tensor memory, N = the item's row count rounded up to 16
+// from the activation tile in shared memory, so a short item costs only the
+// MMA work of its own rows.  One CTA per SM walks items round-robin.
+// Warp roles per CTA:
+//   warp 0      lane 0: TMA of the 192 x 64 bf16 activation tile of each K
+//               step (SWIZZLE_128B, the canonical K-major layout tcgen05
+//               reads); the down GEMM loads the hi and the lo tile
+//               lane 1: TMA of the packed E2M1 weights (128 rows x 128 bytes
+//               = 4 K steps per stage) and, once per item, the E8M0 scales
+//   warp 1      TMEM owner and MMA issuer (one thread)
+//   warps 2-9   weight converters: thread = one weight row (its TMEM lane)
+//               and one 32-element half of the K step; reads its packed
+//               bytes and scale from shared memory, converts them exactly to
+//               bf16 (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by
+//               the block scale) and stores them into the tensor-memory
+//               weight stage with tcgen05.st
+//   warps 10-13 epilogue: tcgen05.ld of the accumulators, SiLU gating (gemm1)
 //               or router-weighted scatter-add (gemm2), global stores
-// Each 128x64 B tile feeds the MMAs of both 128-row halves (and, in the down
-// GEMM, of the hi and the lo activation parts), so the weight conversion cost
-// is spread over up to 256 rows.  Activation and weight tiles travel in
-// separate mbarrier rings.
+// Tensor memory (512 columns): four 32-column weight stages, then two
+// 192-column accumulators (double-buffered across items).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -43,24 +43,29 @@ namespace moe {
 
 namespace {
 
-constexpr int kPThreads = 320;
-constexpr int kTileBytes = 128 * 128;         // 128 rows x 64 bf16
-constexpr int kAStages = 3;                   // activation ring: two 128-row halves per stage
-constexpr int kAStageBytes = 2 * kTileBytes;
-constexpr int kBStages = 3;                   // bf16 weight ring: one 128 x 64 tile per stage
-constexpr int kRawStages = 2;                 // packed weight ring: 128 rows x 128 bytes (4 K steps)
-constexpr int kRawBytes = 128 * 128;
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarp0 = 2 + kConvWarps;
+constexpr int kPThreads = (kEpiWarp0 + 4) * 32;
+constexpr int kActTileBytes = kTcRows * 128;  // kTcRows rows x 64 bf16
+constexpr int kActStages = 4;                 // one activation tile (part) per stage
+constexpr int kRawStages = 3;                 // packed weight ring: 128 rows x 128 bytes (4 K steps)
+constexpr int kRawBytes = kTcW * 128;
 constexpr int kRawSteps = 4;                  // K steps per packed stage
-constexpr int kScaleBytes = 128 * 128;        // E8M0 scales of one item: 128 rows x K/32 (<= 128) bytes
+constexpr int kScaleBytes = kTcW * 128;       // E8M0 scales of one item: 128 rows x K/32 (<= 128) bytes
+constexpr int kWStages = 4;                   // bf16 weight stages in tensor memory, 32 columns each
+constexpr int kEpiTable = 4 * kTcRows * 8;    // per epilogue warp: (token, router weight) of each row
 constexpr int kRingBytes =
-    kAStages * kAStageBytes + kBStages * kTileBytes + kRawStages * kRawBytes + 2 * kScaleBytes;
+    kActStages * kActTileBytes + kRawStages * kRawBytes + 2 * kScaleBytes + kEpiTable;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol0 = kWStages * 32;  // first accumulator column
+static_assert(kAccCol0 + 2 * kTcRows <= kTmemCols, "tensor memory budget");
+static_assert(kTcRows % 32 == 0 && kTcRows <= 256, "MMA N limit");
 
 struct TcParams {
   const uint8_t* w;   // packed [E][N][K/2]
   const uint8_t* ws;  // E8M0 [E][N][K/32]
   int N, K, I, H;
-  int n_tiles;        // N tiles per expert
+  int n_tiles;        // weight tiles per expert
   const int32_t* mtiles;
   const int32_t* n_mtiles;
   const int32_t* offsets;
@@ -105,12 +110,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D (tensor memory) (+)= A (tensor memory) * B (shared memory descriptor)^T.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -134,6 +140,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16 consecutive 32-bit columns of the calling thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&c)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(c[0].x), "r"(c[0].y), "r"(c[0].z), "r"(c[0].w), "r"(c[1].x), "r"(c[1].y), "r"(c[1].z), "r"(c[1].w),
+      "r"(c[2].x), "r"(c[2].y), "r"(c[2].z), "r"(c[2].w), "r"(c[3].x), "r"(c[3].y), "r"(c[3].z), "r"(c[3].w)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -148,9 +166,14 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return r;
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ void red_add(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
 }
 
 // Two exact E2M1 values as f16 (one packed byte) -> the same values times
@@ -160,8 +183,8 @@ __device__ __forceinline__ uint32_t f16pair_to_bf16_rebias(uint32_t h) {
   return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
 }
 
-// 32 E2M1 values (16 packed bytes) of one block with E8M0 scale s -> 4 chunks of
-// 8 bf16 (16 B each), exact.
+// 32 E2M1 values (16 packed bytes) of one block with E8M0 scale s -> 16 words
+// of two bf16 (K order, lower element in the low half), exact.
 __device__ __forceinline__ void dequant_block(const uint4& q, uint32_t s, uint4 (&out)[4]) {
   // value * 2^-112 * 2^(s-15) = value * 2^(s-127); 2^(s-15) is a normal bf16 for s <= 142
   const bool big = s > 142u;
@@ -204,6 +227,18 @@ __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long ite
   return it;
 }
 
+// Row of the packed-weight (and scale) stage that feeds TMEM lane L.  The
+// stage holds the item's 128 weight rows as two TMA boxes of 64: for gate_up
+// the 64 gate rows then the matching 64 up rows.  Gate_up puts, in every
+// 32-lane quadrant q, 16 gate rows (lanes 0-15) and their up rows (lanes
+// 16-31), so one epilogue warp sees both halves of its 16 activations.
+template <bool GATE_UP>
+__device__ __forceinline__ int stage_row(int L) {
+  if (!GATE_UP) return L;
+  const int q = L >> 5, l = L & 31;
+  return l < 16 ? 16 * q + l : 64 + 16 * q + (l - 16);
+}
+
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                const __grid_constant__ CUtensorMap tmap_w,
@@ -211,20 +246,20 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
                                                                const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* a_ring = smem;
-  uint8_t* b_ring = a_ring + kAStages * kAStageBytes;
-  uint8_t* raw_ring = b_ring + kBStages * kTileBytes;
+  uint8_t* act_ring = smem;
+  uint8_t* raw_ring = act_ring + kActStages * kActTileBytes;
   uint8_t* sc_buf = raw_ring + kRawStages * kRawBytes;  // [2][128 rows][K/32]
+  uint8_t* epi_tab = sc_buf + 2 * kScaleBytes;          // [4 warps][kTcRows] (token, weight)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
-  uint64_t* a_full = bars;
-  uint64_t* a_empty = a_full + kAStages;
-  uint64_t* b_full = a_empty + kAStages;
-  uint64_t* b_empty = b_full + kBStages;
-  uint64_t* raw_full = b_empty + kBStages;
+  uint64_t* act_full = bars;
+  uint64_t* act_empty = act_full + kActStages;
+  uint64_t* raw_full = act_empty + kActStages;
   uint64_t* raw_empty = raw_full + kRawStages;
   uint64_t* sc_full = raw_empty + kRawStages;
   uint64_t* sc_empty = sc_full + 2;
-  uint64_t* acc_full = sc_empty + 2;
+  uint64_t* w_full = sc_empty + 2;
+  uint64_t* w_empty = w_full + kWStages;
+  uint64_t* acc_full = w_empty + kWStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -232,21 +267,21 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&a_full[s], 1);
-      mbar_init(&a_empty[s], 1);
-    }
-    for (int s = 0; s < kBStages; ++s) {
-      mbar_init(&b_full[s], 4);
-      mbar_init(&b_empty[s], 1);
+    for (int s = 0; s < kActStages; ++s) {
+      mbar_init(&act_full[s], 1);
+      mbar_init(&act_empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 4);
+      mbar_init(&raw_empty[s], kConvWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sc_full[s], 1);
-      mbar_init(&sc_empty[s], 4);
+      mbar_init(&sc_empty[s], kConvWarps);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&w_full[s], kConvWarps);
+      mbar_init(&w_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -267,50 +302,47 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
   // gate_up reads one bf16 activation tile per K step; down reads the hi and
   // lo bf16 parts of the activated intermediate (interleaved per 64 columns)
   constexpr int kParts = GATE_UP ? 1 : 2;
-  const uint32_t idesc = idesc_bf16(kTcM, kTcN);
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // ------------------------------------------------------------------ activation TMA
       long long g = 0;
       bool stop = false;
       for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
         const ItemInfo it = decode_item(p, item);
-        const int halves = it.rows > kTcM ? 2 : 1;
         for (int step = 0; step < KS * kParts; ++step, ++g) {
-          const int stage = (int)(g % kAStages);
-          const long long u = g / kAStages;
-          if (u > 0 && !mbar_wait(&a_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+          const int stage = (int)(g % kActStages);
+          const long long u = g / kActStages;
+          if (u > 0 && !mbar_wait(&act_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
-          uint8_t* st = a_ring + stage * kAStageBytes;
-          mbar_arrive_expect_tx(&a_full[stage], halves * kTileBytes);
-          tma_load_2d(st, &tmap_a, step * kTcK, it.row0, &a_full[stage]);
-          if (halves == 2) tma_load_2d(st + kTileBytes, &tmap_a, step * kTcK, it.row0 + kTcM, &a_full[stage]);
+          mbar_arrive_expect_tx(&act_full[stage], kActTileBytes);
+          tma_load_2d(act_ring + stage * kActTileBytes, &tmap_a, step * kTcK, it.row0, &act_full[stage]);
         }
       }
       // nothing issued may still be in flight when the CTA exits
-      const long long first = g > kAStages ? g - kAStages : 0;
-      for (long long v = first; v < g; ++v) mbar_wait(&a_full[v % kAStages], (uint32_t)((v / kAStages) & 1), p.status);
+      const long long first = g > kActStages ? g - kActStages : 0;
+      for (long long v = first; v < g; ++v)
+        mbar_wait(&act_full[v % kActStages], (uint32_t)((v / kActStages) & 1), p.status);
     } else if (lane == 1) {
-      // packed weights (128 rows x 128 bytes per stage) and each item's scales
+      // ------------------------------------------------------------------ packed weights and scales TMA
       const int Kb = p.K >> 5;
       const int n_raw = (p.K >> 1) / 128;
       long long g = 0, j = 0;
       bool stop = false;
       for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
         const ItemInfo it = decode_item(p, item);
-        // weight rows of this N tile: two blocks of 64 (gate and up rows for gate_up)
-        const int row_a = it.e * p.N + (GATE_UP ? 64 * it.nt : kTcN * it.nt);
+        // weight rows of this tile: two blocks of 64 (gate and up rows for gate_up)
+        const int row_a = it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt);
         const int row_b = GATE_UP ? it.e * p.N + p.I + 64 * it.nt : row_a + 64;
         const int sb = (int)(j & 1);
         if (j >= 2 && !mbar_wait(&sc_empty[sb], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&sc_full[sb], 128 * Kb);
+        mbar_arrive_expect_tx(&sc_full[sb], kTcW * Kb);
         tma_load_2d(sc_buf + sb * kScaleBytes, &tmap_s, 0, row_a, &sc_full[sb]);
         tma_load_2d(sc_buf + sb * kScaleBytes + 64 * Kb, &tmap_s, 0, row_b, &sc_full[sb]);
         for (int rs = 0; rs < n_raw; ++rs, ++g) {
@@ -335,10 +367,11 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      long long ga = 0, gb = 0, j = 0;
+      long long ga = 0, gw = 0, j = 0;
       for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
         const ItemInfo it = decode_item(p, item);
-        const int halves = it.rows > kTcM ? 2 : 1;
+        const int n = (it.rows + 15) & ~15;  // MMA N: the item's rows rounded up to 16
+        const uint32_t idesc = idesc_bf16(kTcW, n);
         const int buf = (int)(j & 1);
         const long long u = j >> 1;
         if (u > 0 && !mbar_wait(&acc_empty[buf], (uint32_t)((u - 1) & 1), p.status)) {
@@ -346,34 +379,31 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem_base + buf * 256, d1 = d0 + 128;
+        const uint32_t d = tmem_base + kAccCol0 + buf * kTcRows;
         bool ok = true;
-        for (int ks = 0; ks < KS && ok; ++ks, ++gb) {
-          const int bs = (int)(gb % kBStages);
-          if (!mbar_wait(&b_full[bs], (uint32_t)((gb / kBStages) & 1), p.status)) {
+        for (int ks = 0; ks < KS && ok; ++ks, ++gw) {
+          const int ws = (int)(gw % kWStages);
+          if (!mbar_wait(&w_full[ws], (uint32_t)((gw / kWStages) & 1), p.status)) {
             ok = false;
             break;
           }
-          const uint64_t b = sw128_desc(smem_u32(b_ring + bs * kTileBytes));
+          tc_fence_after();
+          const uint32_t a = tmem_base + ws * 32;
           for (int part = 0; part < kParts; ++part, ++ga) {
-            const int as = (int)(ga % kAStages);
-            if (!mbar_wait(&a_full[as], (uint32_t)((ga / kAStages) & 1), p.status)) {
+            const int as = (int)(ga % kActStages);
+            if (!mbar_wait(&act_full[as], (uint32_t)((ga / kActStages) & 1), p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t st = smem_u32(a_ring + as * kAStageBytes);
-            const uint64_t a0 = sw128_desc(st), a1 = sw128_desc(st + kTileBytes);
+            const uint64_t b = sw128_desc(smem_u32(act_ring + as * kActTileBytes));
 #pragma unroll
-            for (int k = 0; k < kTcK / 16; ++k) {
-              const uint32_t acc = (ks > 0 || part > 0 || k > 0) ? 1u : 0u;
-              mma_bf16(d0, a0 + 2 * k, b + 2 * k, idesc, acc);
-              if (halves == 2) mma_bf16(d1, a1 + 2 * k, b + 2 * k, idesc, acc);
-            }
-            mma_commit(&a_empty[as]);
+            for (int k = 0; k < kTcK / 16; ++k)
+              mma_bf16_ta(d, a + 8 * k, b + 2 * k, idesc, (ks > 0 || part > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&act_empty[as]);
           }
           if (!ok) break;
-          mma_commit(&b_empty[bs]);
+          mma_commit(&w_empty[ws]);
         }
         if (!ok) {
           *abort_flag = 1;
@@ -385,14 +415,16 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
       mma_commit(drain);
       mbar_wait(drain, 0, p.status);
     }
-  } else if (warp < 6) {
+  } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------------ weight converters
-    const int r = tid - 64;  // B-tile row 0..127
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int hk = (warp - 2) >> 2;          // which 32-element half of each K step
+    const int L = 32 * q + lane;             // TMEM lane = weight row of the tile
+    const int rr = stage_row<GATE_UP>(L);    // its row in the packed and scale stages
     const int Kb = p.K >> 5;
-    long long g = 0, graw = 0, j = 0;
-    uint8_t* const brow_base = b_ring + (r >> 3) * 1024 + (r & 7) * 128;
-    const int sw = r & 7;
     const int n_raw = (p.K >> 1) / 128;
+    const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+    long long gw = 0, graw = 0, j = 0;
     bool stop = false;
     for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
       const int sb = (int)(j & 1);
@@ -400,7 +432,7 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
         *abort_flag = 1;
         break;
       }
-      const uint8_t* srow = sc_buf + sb * kScaleBytes + r * Kb;
+      const uint8_t* srow = sc_buf + sb * kScaleBytes + rr * Kb;
       for (int rs = 0; rs < n_raw && !stop; ++rs, ++graw) {
         const int rstage = (int)(graw % kRawStages);
         if (!mbar_wait(&raw_full[rstage], (uint32_t)((graw / kRawStages) & 1), p.status)) {
@@ -408,32 +440,30 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
           stop = true;
           break;
         }
-        // row r of the packed stage: 128 bytes, 16-byte chunks swizzled by (r & 7)
-        const uint8_t* rrow = raw_ring + rstage * kRawBytes + r * 128;
+        // row rr of the packed stage: 128 bytes, 16-byte chunks swizzled by (rr & 7)
+        const uint8_t* rrow = raw_ring + rstage * kRawBytes + rr * 128;
+        // the 8 scales of this stage's 4 K steps (Kb is a multiple of 8)
+        const uint2 sc8 = *reinterpret_cast<const uint2*>(srow + 8 * rs);
 #pragma unroll
-        for (int q = 0; q < kRawSteps; ++q, ++g) {
-          const int ks = rs * kRawSteps + q;
-          const uint4 q0 = *reinterpret_cast<const uint4*>(rrow + (((2 * q) ^ sw) << 4));
-          const uint4 q1 = *reinterpret_cast<const uint4*>(rrow + (((2 * q + 1) ^ sw) << 4));
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(srow + 2 * ks);
-          const int stage = (int)(g % kBStages);
-          const long long u = g / kBStages;
-          if (u > 0 && !mbar_wait(&b_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+        for (int qs = 0; qs < kRawSteps; ++qs, ++gw) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(rrow + (((2 * qs + hk) ^ (rr & 7)) << 4));
+          const int sh = 8 * (2 * qs + hk);
+          const uint32_t s = ((sh < 32 ? sc8.x >> sh : sc8.y >> (sh - 32)) & 0xFFu);
+          const int ws = (int)(gw % kWStages);
+          const long long u = gw / kWStages;
+          if (u > 0 && !mbar_wait(&w_empty[ws], (uint32_t)((u - 1) & 1), p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
-          uint8_t* brow = brow_base + stage * kTileBytes;
+          tc_fence_after();
           uint4 c[4];
-          dequant_block(q0, sc & 0xFFu, c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + ((i ^ sw) << 4)) = c[i];
-          dequant_block(q1, sc >> 8, c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(brow + (((4 + i) ^ sw) << 4)) = c[i];
-          fence_proxy_async_smem();
+          dequant_block(qv, s, c);
+          tmem_st16(tmem_base + t_lane + ws * 32 + 16 * hk, c);
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&b_full[stage]);
+          if (lane == 0) mbar_arrive(&w_full[ws]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rstage]);
@@ -444,66 +474,60 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int* tab_tok = reinterpret_cast<int*>(epi_tab + (warp - kEpiWarp0) * kTcRows * 8);
+    float* tab_w = reinterpret_cast<float*>(tab_tok + kTcRows);
     long long j = 0;
     for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
       const ItemInfo it = decode_item(p, item);
-      const int halves = it.rows > kTcM ? 2 : 1;
       const int buf = (int)(j & 1);
+      if (!GATE_UP) {
+        // token and router weight of every row of the item
+        __syncwarp();
+        for (int r = lane; r < it.rows; r += 32) {
+          const int pair = p.sorted_pair[it.row0 + r];
+          tab_tok[r] = pair / p.topk;
+          tab_w[r] = p.topk_w[pair];
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(&acc_full[buf], (uint32_t)((j >> 1) & 1), p.status)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      for (int h = 0; h < halves; ++h) {
-        const int lrow = h * kTcM + q * 32 + lane;
-        const bool valid = lrow < it.rows;
-        const int row = it.row0 + lrow;
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256 + h * 128;
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + kAccCol0 + buf * kTcRows;
+      for (int c0 = 0; c0 < it.rows; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c0, v);
+        tmem_ld_wait();
         if (GATE_UP) {
+          // lanes 0-15: gate rows of activations 16q + lane, tokens c0..c0+15;
+          // lanes 16-31: the matching up rows, tokens c0+16..c0+31
+          const bool lo_half = lane < 16;
+          uint16_t* dst = p.act_out + (size_t)(it.row0 + c0 + (lo_half ? 0 : 16)) * (2 * p.I) + 128 * it.nt +
+                          16 * q + (lane & 15);
+          const int nvalid = it.rows - c0 - (lo_half ? 0 : 16);
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t gv[32], uv[32];
-            tmem_ld32(tbase + c0, gv);
-            tmem_ld32(tbase + 64 + c0, uv);
-            tmem_ld_wait();
-            if (valid) {
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t send = lo_half ? v[16 + i] : v[i];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float gt = __uint_as_float(lo_half ? v[i] : recv);
+            const float up = __uint_as_float(lo_half ? recv : v[16 + i]);
+            if (i < nvalid) {
               // a = hi + lo with hi = bf16(a), lo = bf16(a - hi): 16 significant bits
-              uint16_t* dst = p.act_out + (size_t)row * (2 * p.I) + 128 * it.nt + c0;
-#pragma unroll
-              for (int v = 0; v < 32; v += 8) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                  const float a0 = silu(__uint_as_float(gv[v + 2 * z])) * __uint_as_float(uv[v + 2 * z]);
-                  const float a1 = silu(__uint_as_float(gv[v + 2 * z + 1])) * __uint_as_float(uv[v + 2 * z + 1]);
-                  hi[z] = f32x2_to_bf16x2(a0, a1);
-                  lo[z] = f32x2_to_bf16x2(a0 - bf16_lo(hi[z]), a1 - bf16_hi(hi[z]));
-                }
-                *reinterpret_cast<uint4*>(dst + v) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(dst + 64 + v) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-              }
+              const float a = silu(gt) * up;
+              const uint16_t hi = f32_to_bf16_bits(a);
+              const uint16_t lo = f32_to_bf16_bits(a - __uint_as_float((uint32_t)hi << 16));
+              dst[(size_t)i * (2 * p.I)] = hi;
+              dst[(size_t)i * (2 * p.I) + 64] = lo;
             }
           }
         } else {
-          int tok = 0;
-          float wk = 0.f;
-          if (valid) {
-            const int pair = p.sorted_pair[row];
-            tok = pair / p.topk;
-            wk = p.topk_w[pair];
-          }
+          float* dst = p.outacc + kTcW * it.nt + 32 * q + lane;
+          const int nvalid = min(32, it.rows - c0);
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t yv[32];
-            tmem_ld32(tbase + c0, yv);
-            tmem_ld_wait();
-            if (valid) {
-              float* dst = p.outacc + (size_t)tok * p.H + kTcN * it.nt + c0;
-#pragma unroll
-              for (int v = 0; v < 32; v += 4)
-                red_add_v4(dst + v, wk * __uint_as_float(yv[v]), wk * __uint_as_float(yv[v + 1]),
-                           wk * __uint_as_float(yv[v + 2]), wk * __uint_as_float(yv[v + 3]));
-            }
+          for (int i = 0; i < 32; ++i) {
+            if (i < nvalid) red_add(dst + (size_t)tab_tok[c0 + i] * p.H, tab_w[c0 + i] * __uint_as_float(v[i]));
           }
         }
       }
@@ -563,14 +587,14 @@ cudaError_t get_encoder(EncodeTiledFn* fn) {
   return cudaSuccess;
 }
 
-// bf16 [rows][K] row-major, 128 x 64 boxes with 128-byte swizzle.
+// bf16 [rows][K] row-major, kTcRows x 64 boxes with 128-byte swizzle.
 cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K) {
   EncodeTiledFn enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcM};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcRows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -601,7 +625,7 @@ cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaS
   if (e0 != cudaSuccess) return e0;
   e0 = make_u8_map(&map_s, p.ws, (long long)E * p.N, p.K / 32, p.K / 32, false);
   if (e0 != cudaSuccess) return e0;
-  const size_t smem = 1024 + (size_t)kRingBytes + 256;
+  const size_t smem = 1024 + (size_t)kRingBytes + 512;
   auto kern = tc_gemm_kernel<GATE_UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -655,7 +679,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.ws = a.w2_s;
   p2.N = a.H;
   p2.K = a.I;
-  p2.n_tiles = a.H / kTcN;
+  p2.n_tiles = a.H / kTcW;
   timing_mark(3, false, s);
   e = launch_tc<false>(map_a, p2, a.num_sms, s, a.E);
   timing_mark(3, true, s);

@@ -237,10 +237,12 @@ def test_moe_prefill_small(mw, E, H, I, T, topk, bias):
 
 
 def test_moe_prefill_tile_boundaries(mw):
-    # expert 0 gets 257 rows (a full 256-row item plus a 1-row item), expert 1
-    # exactly 256, expert 2 exactly 128, expert 3 none; invalid ids in between
-    E, H, I, topk = 4, 512, 512, 1
-    counts = [257, 256, 128]
+    # work items hold up to 192 rows of one expert: expert 0 gets 193 rows (a
+    # full item plus a 1-row item), expert 1 exactly 192, expert 2 385 (two
+    # full items and one row), expert 3 17 (an MMA N of 32 with 15 idle
+    # columns), expert 4 none; invalid ids in between
+    E, H, I, topk = 5, 512, 512, 1
+    counts = [193, 192, 385, 17]
     ids = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)] + [np.array([-1, 7], np.int32)])
     g = np.random.default_rng(11)
     ids = ids[g.permutation(ids.size)][:, None].astype(np.int32)
