@@ -40,6 +40,8 @@ RouteOut route_view(uint8_t* ws, const Workspace& L) {
   r.pair_pos = reinterpret_cast<int32_t*>(ws + L.pair_pos);
   r.mtiles = reinterpret_cast<int32_t*>(ws + L.mtiles);
   r.n_mtiles = reinterpret_cast<int32_t*>(ws + L.n_mtiles);
+  r.mtiles_dn = reinterpret_cast<int32_t*>(ws + L.mtiles_dn);
+  r.n_mtiles_dn = reinterpret_cast<int32_t*>(ws + L.n_mtiles_dn);
   return r;
 }
 
@@ -153,8 +155,10 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.gprefix = o; o = align256(o + 4 * (E + 1));
   L.sorted_pair = o; o = align256(o + 4 * P);
   L.pair_pos = o; o = align256(o + 4 * P);
-  L.mtiles = o; o = align256(o + 4 * (P / kTcRows + E + 1));
+  L.mtiles = o; o = align256(o + 4 * (P / kTcRowsUp + E + 1));
   L.n_mtiles = o; o = align256(o + 4);
+  L.mtiles_dn = o; o = align256(o + 4 * (P / kTcRowsDown + E + 1));
+  L.n_mtiles_dn = o; o = align256(o + 4);
   if (L.prefill) {
     L.xs = o; o = align256(o + 2 * P * H);
     L.as = o; o = align256(o + 4 * P * I);

@@ -25,16 +25,19 @@ constexpr bool kPrefillAvailable = true;
 
 // Prefill tile sizes (tcgen05, cta_group::1).  The MMA's M side is a tile of
 // 128 dequantised weight rows held in tensor memory; its N side is a tile of
-// up to kTcRows sorted activation rows of one expert in shared memory.
-constexpr int kTcW = 128;     // weight rows per work item (MMA M)
-constexpr int kTcK = 64;      // K per pipeline step (one 128-byte swizzle row of bf16)
-constexpr int kTcRows = 192;  // sorted activation rows per work item (MMA N, at most)
+// up to kTcRowsUp (gate_up) or kTcRowsDown (down) sorted activation rows of
+// one expert in shared memory.
+constexpr int kTcW = 128;        // weight rows per work item (MMA M)
+constexpr int kTcK = 64;         // K per pipeline step (one 128-byte swizzle row of bf16)
+constexpr int kTcRowsUp = 192;   // sorted rows per gate_up work item (MMA N, at most)
+constexpr int kTcRowsDown = 128; // sorted rows per down work item (MMA N, at most)
 
 enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
 
 // Byte offsets of the workspace regions for one problem.
 struct Workspace {
-  size_t status, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles;
+  size_t status, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles, mtiles_dn,
+      n_mtiles_dn;
   size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
   size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 hi/lo [P][2I], f32 [T][H]
   size_t total;
@@ -54,8 +57,12 @@ struct RouteOut {
   int32_t* gprefix;      // [E+1] exclusive prefix over active experts of ceil(count / kMoeGroup)
   int32_t* sorted_pair;  // [P]
   int32_t* pair_pos;     // [P]
-  int32_t* mtiles;       // [max_mtiles] (expert << 20 | tile index), tiles of kTcRows rows, tensor-core path
+  // tensor-core path: (expert << 20 | tile index) per row tile of an expert,
+  // tiles of kTcRowsUp rows for gate_up and of kTcRowsDown rows for down
+  int32_t* mtiles;       // [P / kTcRowsUp + E + 1]
   int32_t* n_mtiles;     // [1]
+  int32_t* mtiles_dn;    // [P / kTcRowsDown + E + 1]
+  int32_t* n_mtiles_dn;  // [1]
 };
 
 // Launch ``kern`` on ``s``; with ``pdl`` the launch may begin before the previous

@@ -12,29 +12,46 @@
 //                                                              (fp32, red.add)
 //   cast:    out = bf16(outacc)
 //
-// Work item = (expert, up to 192 of its sorted rows, one tile of 128 weight
-// rows; gemm1 tiles hold 64 gate rows and the matching 64 up rows).  The MMA
+// Work item = (expert, up to 192 (gate_up) or 128 (down) of its sorted rows,
+// one tile of 128 weight rows; gemm1 tiles hold 64 gate rows and the matching
+// 64 up rows).  The MMA
 // is D[128 weight rows][rows] += W[128][16] X[rows][16]^T: M = 128 from the
 // weight tile in tensor memory, N = the item's row count rounded up to 16
 // from the activation tile in shared memory, so a short item costs only the
-// MMA work of its own rows.  One CTA per SM walks items round-robin.
+// MMA work of its own rows.
+//
+// Two CTAs per SM, each with its own MMA-issuing thread, take turns on the
+// SM's tensor core.  A thread that issues tcgen05.mma leaves the tensor core
+// idle for every cycle it spends elsewhere (a barrier wait, descriptor
+// arithmetic, waiting for its epilogue to drain the accumulator); the other
+// CTA's MMAs fill those gaps.  So each CTA keeps one accumulator and half of
+// the SM's tensor memory and shared memory.  Items go round-robin over all
+// CTAs.  Gate_up items are wider (192 rows) than down items (128) because
+// every item converts its 128 x K weight tile once: more rows per item means
+// fewer conversions per MMA; the down GEMM's two activation parts per step
+// leave shared memory for only 128.
+//
+// The pipeline runs in steps of 64 of K: gate_up issues 4 MMAs per step (one
+// 64-column tile of x), down issues 8 (the hi and the lo part of the
+// activated intermediate).  A step's activation tiles (TMA) and its weight
+// stage in tensor memory (converters) complete one shared mbarrier, so the
+// MMA thread waits once per step.
 // Warp roles per CTA:
-//   warp 0      lane 0: TMA of the 192 x 64 bf16 activation tile of each K
-//               step (SWIZZLE_128B, the canonical K-major layout tcgen05
-//               reads); the down GEMM loads the hi and the lo tile
-//               lane 1: TMA of the packed E2M1 weights (128 rows x 128 bytes
-//               = 4 K steps per stage) and, once per item, the E8M0 scales
+//   warp 0      lane 0: TMA of the step's rows x 64 bf16 activation tile(s)
+//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads);
+//               lane 1: TMA of the packed E2M1 weights (128 rows x 128 bytes =
+//               256 of K per stage) and, once per item, the E8M0 scales
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-9   weight converters: thread = one weight row (its TMEM lane)
-//               and one 32-element half of the K step; reads its packed
+//               and one of the step's two 32-element blocks; reads its packed
 //               bytes and scale from shared memory, converts them exactly to
 //               bf16 (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by
-//               the block scale) and stores them into the tensor-memory
+//               the block scale) and stores them into the step's tensor-memory
 //               weight stage with tcgen05.st
-//   warps 10-13 epilogue: tcgen05.ld of the accumulators, SiLU gating (gemm1)
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator, SiLU gating (gemm1)
 //               or router-weighted scatter-add (gemm2), global stores
-// Tensor memory (512 columns): four 32-column weight stages, then two
-// 192-column accumulators (double-buffered across items).
+// Tensor memory per CTA (256 columns): two 32-column weight stages, then one
+// accumulator of 192 (gate_up) or 128 (down) columns.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -46,20 +63,30 @@ namespace {
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarp0 = 2 + kConvWarps;
 constexpr int kPThreads = (kEpiWarp0 + 4) * 32;
-constexpr int kActTileBytes = kTcRows * 128;  // kTcRows rows x 64 bf16
-constexpr int kActStages = 4;                 // one activation tile (part) per stage
-constexpr int kRawStages = 3;                 // packed weight ring: 128 rows x 128 bytes (4 K steps)
+constexpr int kRawStages = 2;                 // packed weight ring: 128 rows x 128 bytes (256 of K)
 constexpr int kRawBytes = kTcW * 128;
-constexpr int kRawSteps = 4;                  // K steps per packed stage
-constexpr int kScaleBytes = kTcW * 128;       // E8M0 scales of one item: 128 rows x K/32 (<= 128) bytes
-constexpr int kWStages = 4;                   // bf16 weight stages in tensor memory, 32 columns each
-constexpr int kEpiTable = 4 * kTcRows * 8;    // per epilogue warp: (token, router weight) of each row
-constexpr int kRingBytes =
-    kActStages * kActTileBytes + kRawStages * kRawBytes + 2 * kScaleBytes + kEpiTable;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol0 = kWStages * 32;  // first accumulator column
-static_assert(kAccCol0 + 2 * kTcRows <= kTmemCols, "tensor memory budget");
-static_assert(kTcRows % 32 == 0 && kTcRows <= 256, "MMA N limit");
+constexpr int kStepsPerRaw = 4;               // steps (64 of K) per packed-weight stage
+constexpr int kWCols = 32;                    // tensor-memory columns per weight stage (64 of K)
+constexpr uint32_t kTmemCols = 256;
+
+// Tile rows, pipeline depth, tensor-memory and shared-memory layout of one
+// CTA; gate_up stages hold one activation tile, down stages two (hi and lo).
+template <bool GATE_UP>
+struct TcLayout {
+  static constexpr int kRows = GATE_UP ? kTcRowsUp : kTcRowsDown;  // MMA N, at most
+  static constexpr int kBoxBytes = kRows * 128;                   // one tile: kRows rows x 64 bf16
+  static constexpr int kStages = 2;
+  static constexpr int kStageBytes = (GATE_UP ? 1 : 2) * kBoxBytes;
+  static constexpr uint32_t kAccCol0 = kStages * kWCols;          // accumulator columns [kAccCol0, +kRows)
+  static_assert(kAccCol0 + kRows <= kTmemCols, "tensor memory budget");
+  static_assert(kRows % 32 == 0 && kRows <= 256, "MMA N limit");
+  // act ring | raw ring | scales (128 rows x K/32) | mbarriers
+  static constexpr int kRawOff = kStages * kStageBytes;
+  static constexpr int kScaleOff = kRawOff + kRawStages * kRawBytes;
+  static __host__ __device__ int bar_off(int K) { return kScaleOff + kTcW * (K >> 5); }
+  // + 1024 for aligning the base; two CTAs per SM need at most 113 KB each
+  static __host__ __device__ int smem_bytes(int K) { return 1024 + bar_off(K) + 256; }
+};
 
 struct TcParams {
   const uint8_t* w;   // packed [E][N][K/2]
@@ -215,6 +242,7 @@ struct ItemInfo {
   int e, nt, row0, rows;
 };
 
+template <int kRows>
 __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long item) {
   ItemInfo it;
   const int mp = (int)(item / p.n_tiles);
@@ -222,8 +250,8 @@ __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long ite
   const int code = p.mtiles[mp];
   it.e = code >> 20;
   const int mi = code & 0xFFFFF;
-  it.row0 = p.offsets[it.e] + kTcRows * mi;
-  it.rows = min(kTcRows, p.counts[it.e] - kTcRows * mi);
+  it.row0 = p.offsets[it.e] + kRows * mi;
+  it.rows = min(kRows, p.counts[it.e] - kRows * mi);
   return it;
 }
 
@@ -240,53 +268,47 @@ __device__ __forceinline__ int stage_row(int L) {
 }
 
 template <bool GATE_UP>
-__global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                const __grid_constant__ CUtensorMap tmap_w,
                                                                const __grid_constant__ CUtensorMap tmap_s,
                                                                const TcParams p) {
+  using Lay = TcLayout<GATE_UP>;
+  constexpr int kStages = Lay::kStages;
+  constexpr int kRows = Lay::kRows;
+  constexpr int kBoxBytes = Lay::kBoxBytes;
+  constexpr uint32_t kAccCol0 = Lay::kAccCol0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* act_ring = smem;
-  uint8_t* raw_ring = act_ring + kActStages * kActTileBytes;
-  uint8_t* sc_buf = raw_ring + kRawStages * kRawBytes;  // [2][128 rows][K/32]
-  uint8_t* epi_tab = sc_buf + 2 * kScaleBytes;          // [4 warps][kTcRows] (token, weight)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes);
-  uint64_t* act_full = bars;
-  uint64_t* act_empty = act_full + kActStages;
-  uint64_t* raw_full = act_empty + kActStages;
+  uint8_t* raw_ring = smem + Lay::kRawOff;
+  uint8_t* sc_buf = smem + Lay::kScaleOff;  // [128 rows][K/32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::bar_off(p.K));
+  uint64_t* full = bars;               // [kStages] activation tiles landed + weight stage stored
+  uint64_t* empty = full + kStages;    // [kStages] the step's MMAs are done
+  uint64_t* raw_full = empty + kStages;
   uint64_t* raw_empty = raw_full + kRawStages;
   uint64_t* sc_full = raw_empty + kRawStages;
-  uint64_t* sc_empty = sc_full + 2;
-  uint64_t* w_full = sc_empty + 2;
-  uint64_t* w_empty = w_full + kWStages;
-  uint64_t* acc_full = w_empty + kWStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
+  uint64_t* sc_empty = sc_full + 1;
+  uint64_t* acc_full = sc_empty + 1;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kActStages; ++s) {
-      mbar_init(&act_full[s], 1);
-      mbar_init(&act_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1 + kConvWarps);
+      mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], kConvWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sc_full[s], 1);
-      mbar_init(&sc_empty[s], kConvWarps);
-    }
-    for (int s = 0; s < kWStages; ++s) {
-      mbar_init(&w_full[s], kConvWarps);
-      mbar_init(&w_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
-    }
+    mbar_init(sc_full, 1);
+    mbar_init(sc_empty, kConvWarps);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -297,119 +319,135 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const long long n_items = (long long)(*p.n_mtiles) * p.n_tiles;
-  const int KS = p.K / kTcK;
-  // gate_up reads one bf16 activation tile per K step; down reads the hi and
-  // lo bf16 parts of the activated intermediate (interleaved per 64 columns)
-  constexpr int kParts = GATE_UP ? 1 : 2;
+  const int n_items = *p.n_mtiles * p.n_tiles;
+  // a step is 64 of K: gate_up one 64-column tile of x; down the 64-column hi
+  // and lo tiles of the activated intermediate (interleaved per 64 columns)
+  const int n_steps = p.K / 64;
+  const int n_raw = n_steps / kStepsPerRaw;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ activation TMA
-      long long g = 0;
+      uint32_t stage = 0, phase = 0, used = 0;
       bool stop = false;
-      for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
-        const ItemInfo it = decode_item(p, item);
-        for (int step = 0; step < KS * kParts; ++step, ++g) {
-          const int stage = (int)(g % kActStages);
-          const long long u = g / kActStages;
-          if (u > 0 && !mbar_wait(&act_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+      for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
+        const ItemInfo it = decode_item<Lay::kRows>(p, item);
+        for (int step = 0; step < n_steps; ++step) {
+          if (used >= (uint32_t)kStages && !mbar_wait(&empty[stage], phase ^ 1u, p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
-          mbar_arrive_expect_tx(&act_full[stage], kActTileBytes);
-          tma_load_2d(act_ring + stage * kActTileBytes, &tmap_a, step * kTcK, it.row0, &act_full[stage]);
+          uint8_t* st = act_ring + stage * Lay::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
+          if (GATE_UP) {
+            tma_load_2d(st, &tmap_a, 64 * step, it.row0, &full[stage]);
+          } else {
+            tma_load_2d(st, &tmap_a, 128 * step, it.row0, &full[stage]);
+            tma_load_2d(st + kBoxBytes, &tmap_a, 128 * step + 64, it.row0, &full[stage]);
+          }
+          ++used;
+          if (++stage == (uint32_t)kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-      // nothing issued may still be in flight when the CTA exits
-      const long long first = g > kActStages ? g - kActStages : 0;
-      for (long long v = first; v < g; ++v)
-        mbar_wait(&act_full[v % kActStages], (uint32_t)((v / kActStages) & 1), p.status);
+      // nothing issued may still be in flight when the CTA exits: wait for the
+      // last min(used, kStages) stages to land
+      for (uint32_t v = 0; v < (used < (uint32_t)kStages ? used : (uint32_t)kStages); ++v) {
+        stage = stage == 0 ? kStages - 1 : stage - 1;
+        if (stage == (uint32_t)kStages - 1) phase ^= 1u;
+        mbar_wait(&full[stage], phase, p.status);
+      }
     } else if (lane == 1) {
       // ------------------------------------------------------------------ packed weights and scales TMA
       const int Kb = p.K >> 5;
-      const int n_raw = (p.K >> 1) / 128;
-      long long g = 0, j = 0;
+      uint32_t rstage = 0, rphase = 0, rused = 0, j = 0;
       bool stop = false;
-      for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
-        const ItemInfo it = decode_item(p, item);
+      for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
+        const ItemInfo it = decode_item<Lay::kRows>(p, item);
         // weight rows of this tile: two blocks of 64 (gate and up rows for gate_up)
         const int row_a = it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt);
         const int row_b = GATE_UP ? it.e * p.N + p.I + 64 * it.nt : row_a + 64;
-        const int sb = (int)(j & 1);
-        if (j >= 2 && !mbar_wait(&sc_empty[sb], (uint32_t)(((j >> 1) - 1) & 1), p.status)) {
+        if (j >= 1 && !mbar_wait(sc_empty, (j - 1) & 1u, p.status)) {
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&sc_full[sb], kTcW * Kb);
-        tma_load_2d(sc_buf + sb * kScaleBytes, &tmap_s, 0, row_a, &sc_full[sb]);
-        tma_load_2d(sc_buf + sb * kScaleBytes + 64 * Kb, &tmap_s, 0, row_b, &sc_full[sb]);
-        for (int rs = 0; rs < n_raw; ++rs, ++g) {
-          const int stage = (int)(g % kRawStages);
-          const long long u = g / kRawStages;
-          if (u > 0 && !mbar_wait(&raw_empty[stage], (uint32_t)((u - 1) & 1), p.status)) {
+        mbar_arrive_expect_tx(sc_full, kTcW * Kb);
+        tma_load_2d(sc_buf, &tmap_s, 0, row_a, sc_full);
+        tma_load_2d(sc_buf + 64 * Kb, &tmap_s, 0, row_b, sc_full);
+        for (int rs = 0; rs < n_raw; ++rs) {
+          if (rused >= (uint32_t)kRawStages && !mbar_wait(&raw_empty[rstage], rphase ^ 1u, p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
-          uint8_t* st = raw_ring + stage * kRawBytes;
-          mbar_arrive_expect_tx(&raw_full[stage], kRawBytes);
-          tma_load_2d(st, &tmap_w, rs * 128, row_a, &raw_full[stage]);
-          tma_load_2d(st + 64 * 128, &tmap_w, rs * 128, row_b, &raw_full[stage]);
+          uint8_t* st = raw_ring + rstage * kRawBytes;
+          mbar_arrive_expect_tx(&raw_full[rstage], kRawBytes);
+          tma_load_2d(st, &tmap_w, rs * 128, row_a, &raw_full[rstage]);
+          tma_load_2d(st + 64 * 128, &tmap_w, rs * 128, row_b, &raw_full[rstage]);
+          ++rused;
+          if (++rstage == (uint32_t)kRawStages) {
+            rstage = 0;
+            rphase ^= 1u;
+          }
         }
       }
-      const long long first = g > kRawStages ? g - kRawStages : 0;
-      for (long long v = first; v < g; ++v)
-        mbar_wait(&raw_full[v % kRawStages], (uint32_t)((v / kRawStages) & 1), p.status);
-      for (long long v = j > 2 ? j - 2 : 0; v < j; ++v) mbar_wait(&sc_full[v & 1], (uint32_t)((v >> 1) & 1), p.status);
+      for (uint32_t v = 0; v < (rused < (uint32_t)kRawStages ? rused : (uint32_t)kRawStages); ++v) {
+        rstage = rstage == 0 ? kRawStages - 1 : rstage - 1;
+        if (rstage == (uint32_t)kRawStages - 1) rphase ^= 1u;
+        mbar_wait(&raw_full[rstage], rphase, p.status);
+      }
+      if (j >= 1) mbar_wait(sc_full, (j - 1) & 1u, p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      long long ga = 0, gw = 0, j = 0;
-      for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
-        const ItemInfo it = decode_item(p, item);
-        const int n = (it.rows + 15) & ~15;  // MMA N: the item's rows rounded up to 16
-        const uint32_t idesc = idesc_bf16(kTcW, n);
-        const int buf = (int)(j & 1);
-        const long long u = j >> 1;
-        if (u > 0 && !mbar_wait(&acc_empty[buf], (uint32_t)((u - 1) & 1), p.status)) {
+      uint32_t stage = 0, phase = 0, j = 0;
+      int item = blockIdx.x;
+      ItemInfo it{};
+      if (item < n_items) it = decode_item<Lay::kRows>(p, item);
+      const uint32_t act0 = smem_u32(act_ring);
+      const uint32_t d = tmem_base + kAccCol0;
+      for (; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
+        // the next item's routing fields, loaded a whole item ahead
+        const ItemInfo nxt = item + (int)gridDim.x < n_items ? decode_item<Lay::kRows>(p, item + gridDim.x) : it;
+        const uint32_t idesc = idesc_bf16(kTcW, (it.rows + 15) & ~15);  // N: the rows rounded up to 16
+        // the epilogue must have read the previous item's accumulator
+        if (j >= 1 && !mbar_wait(acc_empty, (j - 1) & 1u, p.status)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + kAccCol0 + buf * kTcRows;
         bool ok = true;
-        for (int ks = 0; ks < KS && ok; ++ks, ++gw) {
-          const int ws = (int)(gw % kWStages);
-          if (!mbar_wait(&w_full[ws], (uint32_t)((gw / kWStages) & 1), p.status)) {
+        for (int step = 0; step < n_steps; ++step) {
+          if (!mbar_wait(&full[stage], phase, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = tmem_base + ws * 32;
-          for (int part = 0; part < kParts; ++part, ++ga) {
-            const int as = (int)(ga % kActStages);
-            if (!mbar_wait(&act_full[as], (uint32_t)((ga / kActStages) & 1), p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t b = sw128_desc(smem_u32(act_ring + as * kActTileBytes));
+          const uint32_t a = tmem_base + stage * kWCols;
+          const uint64_t b0 = sw128_desc(act0 + stage * Lay::kStageBytes);
 #pragma unroll
-            for (int k = 0; k < kTcK / 16; ++k)
-              mma_bf16_ta(d, a + 8 * k, b + 2 * k, idesc, (ks > 0 || part > 0 || k > 0) ? 1u : 0u);
-            mma_commit(&act_empty[as]);
+          for (int k = 0; k < 4; ++k) mma_bf16_ta(d, a + 8 * k, b0 + 2 * k, idesc, (step > 0 || k > 0) ? 1u : 0u);
+          if (!GATE_UP) {
+            const uint64_t b1 = b0 + (kBoxBytes >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_bf16_ta(d, a + 8 * k, b1 + 2 * k, idesc, 1u);
           }
-          if (!ok) break;
-          mma_commit(&w_empty[ws]);
+          mma_commit(&empty[stage]);
+          if (++stage == (uint32_t)kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
         if (!ok) {
           *abort_flag = 1;
           break;
         }
-        mma_commit(&acc_full[buf]);
+        mma_commit(acc_full);
+        it = nxt;
       }
       // all issued MMAs complete before TMEM is released
       mma_commit(drain);
@@ -418,85 +456,95 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------------ weight converters
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int hk = (warp - 2) >> 2;          // which 32-element half of each K step
+    const int hk = (warp - 2) >> 2;          // which of the step's two blocks
     const int L = 32 * q + lane;             // TMEM lane = weight row of the tile
     const int rr = stage_row<GATE_UP>(L);    // its row in the packed and scale stages
     const int Kb = p.K >> 5;
-    const int n_raw = (p.K >> 1) / 128;
-    const uint32_t t_lane = (uint32_t)(32 * q) << 16;
-    long long gw = 0, graw = 0, j = 0;
+    const uint32_t tl = tmem_base + ((uint32_t)(32 * q) << 16) + 16 * hk;
+    const uint8_t* srow = sc_buf + rr * Kb;
+    uint32_t stage = 0, phase = 0, used = 0, rstage = 0, rphase = 0, j = 0;
     bool stop = false;
-    for (long long item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
-      const int sb = (int)(j & 1);
-      if (!mbar_wait(&sc_full[sb], (uint32_t)((j >> 1) & 1), p.status)) {
+    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
+      if (!mbar_wait(sc_full, j & 1u, p.status)) {
         *abort_flag = 1;
         break;
       }
-      const uint8_t* srow = sc_buf + sb * kScaleBytes + rr * Kb;
-      for (int rs = 0; rs < n_raw && !stop; ++rs, ++graw) {
-        const int rstage = (int)(graw % kRawStages);
-        if (!mbar_wait(&raw_full[rstage], (uint32_t)((graw / kRawStages) & 1), p.status)) {
+      for (int rs = 0; rs < n_raw && !stop; ++rs) {
+        if (!mbar_wait(&raw_full[rstage], rphase, p.status)) {
           *abort_flag = 1;
           stop = true;
           break;
         }
-        // row rr of the packed stage: 128 bytes, 16-byte chunks swizzled by (rr & 7)
+        // row rr of the packed stage: 128 bytes = 8 blocks, 16-byte chunks swizzled by (rr & 7)
         const uint8_t* rrow = raw_ring + rstage * kRawBytes + rr * 128;
-        // the 8 scales of this stage's 4 K steps (Kb is a multiple of 8)
+        // the 8 scales of this stage's 8 blocks (Kb is a multiple of 8)
         const uint2 sc8 = *reinterpret_cast<const uint2*>(srow + 8 * rs);
 #pragma unroll
-        for (int qs = 0; qs < kRawSteps; ++qs, ++gw) {
-          const uint4 qv = *reinterpret_cast<const uint4*>(rrow + (((2 * qs + hk) ^ (rr & 7)) << 4));
-          const int sh = 8 * (2 * qs + hk);
-          const uint32_t s = ((sh < 32 ? sc8.x >> sh : sc8.y >> (sh - 32)) & 0xFFu);
-          const int ws = (int)(gw % kWStages);
-          const long long u = gw / kWStages;
-          if (u > 0 && !mbar_wait(&w_empty[ws], (uint32_t)((u - 1) & 1), p.status)) {
+        for (int qs = 0; qs < kStepsPerRaw; ++qs) {
+          const int c = 2 * qs + hk;  // block of the stage: this step's first or second half
+          const uint4 qv = *reinterpret_cast<const uint4*>(rrow + ((c ^ (rr & 7)) << 4));
+          const uint32_t s = ((qs < 2 ? sc8.x >> (8 * c) : sc8.y >> (8 * (c - 4))) & 0xFFu);
+          uint4 cv[4];
+          dequant_block(qv, s, cv);
+          if (used >= (uint32_t)kStages && !mbar_wait(&empty[stage], phase ^ 1u, p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
           tc_fence_after();
-          uint4 c[4];
-          dequant_block(qv, s, c);
-          tmem_st16(tmem_base + t_lane + ws * 32 + 16 * hk, c);
+          tmem_st16(tl + stage * kWCols, cv);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&w_full[ws]);
+          if (lane == 0) mbar_arrive(&full[stage]);
+          ++used;
+          if (++stage == (uint32_t)kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rstage]);
+        if (++rstage == (uint32_t)kRawStages) {
+          rstage = 0;
+          rphase ^= 1u;
+        }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sc_empty[sb]);
+      if (lane == 0) mbar_arrive(sc_empty);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    int* tab_tok = reinterpret_cast<int*>(epi_tab + (warp - kEpiWarp0) * kTcRows * 8);
-    float* tab_w = reinterpret_cast<float*>(tab_tok + kTcRows);
-    long long j = 0;
-    for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
-      const ItemInfo it = decode_item(p, item);
-      const int buf = (int)(j & 1);
+    uint32_t j = 0;
+    for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
+      const ItemInfo it = decode_item<Lay::kRows>(p, item);
+      // down: token and router weight of rows lane, lane + 32, ... (loaded
+      // before the accumulator wait, handed out with shuffles below)
+      int tok[kRows / 32];
+      float wgt[kRows / 32];
       if (!GATE_UP) {
-        // token and router weight of every row of the item
-        __syncwarp();
-        for (int r = lane; r < it.rows; r += 32) {
-          const int pair = p.sorted_pair[it.row0 + r];
-          tab_tok[r] = pair / p.topk;
-          tab_w[r] = p.topk_w[pair];
+#pragma unroll
+        for (int c = 0; c < kRows / 32; ++c) {
+          tok[c] = 0;
+          wgt[c] = 0.f;
+          if (32 * c + lane < it.rows) {
+            const int pair = p.sorted_pair[it.row0 + 32 * c + lane];
+            tok[c] = pair / p.topk;
+            wgt[c] = p.topk_w[pair];
+          }
         }
-        __syncwarp();
       }
-      if (!mbar_wait(&acc_full[buf], (uint32_t)((j >> 1) & 1), p.status)) {
+      if (!mbar_wait(acc_full, j & 1u, p.status)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + kAccCol0 + buf * kTcRows;
-      for (int c0 = 0; c0 < it.rows; c0 += 32) {
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + kAccCol0;
+#pragma unroll
+      for (int c = 0; c < kRows / 32; ++c) {
+        const int c0 = 32 * c;
+        if (c0 >= it.rows) break;
         uint32_t v[32];
         tmem_ld32(tbase + c0, v);
         tmem_ld_wait();
@@ -527,13 +575,15 @@ __global__ void __launch_bounds__(kPThreads, 1) tc_gemm_kernel(const __grid_cons
           const int nvalid = min(32, it.rows - c0);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (i < nvalid) red_add(dst + (size_t)tab_tok[c0 + i] * p.H, tab_w[c0 + i] * __uint_as_float(v[i]));
+            const int t = __shfl_sync(0xffffffffu, tok[c], i);
+            const float wk = __shfl_sync(0xffffffffu, wgt[c], i);
+            if (i < nvalid) red_add(dst + (size_t)t * p.H, wk * __uint_as_float(v[i]));
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) mbar_arrive(acc_empty);
     }
   }
 
@@ -587,14 +637,14 @@ cudaError_t get_encoder(EncodeTiledFn* fn) {
   return cudaSuccess;
 }
 
-// bf16 [rows][K] row-major, kTcRows x 64 boxes with 128-byte swizzle.
-cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K) {
+// bf16 [rows][K] row-major, box_rows x 64 boxes with 128-byte swizzle.
+cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
   EncodeTiledFn enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcRows};
+  const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -625,7 +675,7 @@ cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaS
   if (e0 != cudaSuccess) return e0;
   e0 = make_u8_map(&map_s, p.ws, (long long)E * p.N, p.K / 32, p.K / 32, false);
   if (e0 != cudaSuccess) return e0;
-  const size_t smem = 1024 + (size_t)kRingBytes + 512;
+  const size_t smem = (size_t)TcLayout<GATE_UP>::smem_bytes(p.K);
   auto kern = tc_gemm_kernel<GATE_UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -638,9 +688,9 @@ cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaS
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   const long long P = (long long)a.T * a.topk;
   CUtensorMap map_x, map_a;
-  cudaError_t e = make_act_map(&map_x, a.xs, P, a.H);
+  cudaError_t e = make_act_map(&map_x, a.xs, P, a.H, kTcRowsUp);
   if (e != cudaSuccess) return e;
-  e = make_act_map(&map_a, a.as, P, 2 * a.I);
+  e = make_act_map(&map_a, a.as, P, 2 * a.I, kTcRowsDown);
   if (e != cudaSuccess) return e;
 
   timing_mark(1, false, s);
@@ -669,7 +719,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.outacc = a.outacc;
   p.status = a.status;
   timing_mark(2, false, s);
-  e = launch_tc<true>(map_x, p, a.num_sms, s, a.E);
+  e = launch_tc<true>(map_x, p, 2 * a.num_sms, s, a.E);
   timing_mark(2, true, s);
   if (e != cudaSuccess) return e;
 
@@ -680,8 +730,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.N = a.H;
   p2.K = a.I;
   p2.n_tiles = a.H / kTcW;
+  p2.mtiles = a.route.mtiles_dn;
+  p2.n_mtiles = a.route.n_mtiles_dn;
   timing_mark(3, false, s);
-  e = launch_tc<false>(map_a, p2, a.num_sms, s, a.E);
+  e = launch_tc<false>(map_a, p2, 2 * a.num_sms, s, a.E);
   timing_mark(3, true, s);
   if (e != cudaSuccess) return e;
 

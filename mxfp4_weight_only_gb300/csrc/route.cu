@@ -105,11 +105,27 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
 
   if (make_mtiles) {
-    const int nt = (v + kTcRows - 1) / kTcRows;
-    int n_tiles = 0;
-    const int tpos = block_excl_scan(nt, scratch, &n_tiles);
-    for (int i = 0; i < nt; ++i) r.mtiles[tpos + i] = (tid << 20) | i;
-    if (tid == 0) *r.n_mtiles = n_tiles;
+    // row tiles of each expert for the two tensor-core GEMMs (counts < 2^16
+    // per list here: one packed scan serves both)
+    const int nt = (v + kTcRowsUp - 1) / kTcRowsUp;
+    const int nd = (v + kTcRowsDown - 1) / kTcRowsDown;
+    int tot = 0;
+    if (P < (1 << 16)) {
+      const int packed = block_excl_scan(nt | (nd << 16), scratch, &tot);
+      for (int i = 0; i < nt; ++i) r.mtiles[(packed & 0xFFFF) + i] = (tid << 20) | i;
+      for (int i = 0; i < nd; ++i) r.mtiles_dn[(packed >> 16) + i] = (tid << 20) | i;
+      if (tid == 0) {
+        *r.n_mtiles = tot & 0xFFFF;
+        *r.n_mtiles_dn = tot >> 16;
+      }
+    } else {
+      const int tpos = block_excl_scan(nt, scratch, &tot);
+      for (int i = 0; i < nt; ++i) r.mtiles[tpos + i] = (tid << 20) | i;
+      if (tid == 0) *r.n_mtiles = tot;
+      const int dpos = block_excl_scan(nd, scratch, &tot);
+      for (int i = 0; i < nd; ++i) r.mtiles_dn[dpos + i] = (tid << 20) | i;
+      if (tid == 0) *r.n_mtiles_dn = tot;
+    }
   }
   __syncthreads();
 

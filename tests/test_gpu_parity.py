@@ -237,12 +237,13 @@ def test_moe_prefill_small(mw, E, H, I, T, topk, bias):
 
 
 def test_moe_prefill_tile_boundaries(mw):
-    # work items hold up to 192 rows of one expert: expert 0 gets 193 rows (a
-    # full item plus a 1-row item), expert 1 exactly 192, expert 2 385 (two
-    # full items and one row), expert 3 17 (an MMA N of 32 with 15 idle
-    # columns), expert 4 none; invalid ids in between
-    E, H, I, topk = 5, 512, 512, 1
-    counts = [193, 192, 385, 17]
+    # gate_up items hold up to 192 rows of one expert, down items 128: expert 0
+    # gets 193 rows (192 + 1 and 128 + 65), expert 1 exactly 192 (one item;
+    # 128 + 64), expert 2 129 (one item; 128 + 1), expert 3 385 (192 + 192 + 1;
+    # 3 x 128 + 1), expert 4 17 (an MMA N of 32 with 15 idle columns), expert
+    # 5 none; invalid ids in between
+    E, H, I, topk = 6, 512, 512, 1
+    counts = [193, 192, 129, 385, 17]
     ids = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)] + [np.array([-1, 7], np.int32)])
     g = np.random.default_rng(11)
     ids = ids[g.permutation(ids.size)][:, None].astype(np.int32)
