@@ -14,8 +14,8 @@
 //
 // Work item = (expert, up to 192 (gate_up) or 128 (down) of its sorted rows,
 // one tile of 128 weight rows; gemm1 tiles hold 64 gate rows and the matching
-// 64 up rows).  The MMA
-// is D[128 weight rows][rows] += W[128][16] X[rows][16]^T: M = 128 from the
+// 64 up rows).  The MMA is D[128 weight rows][rows] += W[128][16] X[rows][16]^T:
+// M = 128 from the
 // weight tile in tensor memory, N = the item's row count rounded up to 16
 // from the activation tile in shared memory, so a short item costs only the
 // MMA work of its own rows.
@@ -33,25 +33,24 @@
 //
 // The pipeline runs in steps of 64 of K: gate_up issues 4 MMAs per step (one
 // 64-column tile of x), down issues 8 (the hi and the lo part of the
-// activated intermediate).  A step's activation tiles (TMA) and its weight
-// stage in tensor memory (converters) complete one shared mbarrier, so the
-// MMA thread waits once per step.
+// activated intermediate).  Shared memory holds only the activation ring
+// (four gate_up or three down steps deep, enough to cover the L2 latency of
+// the TMA loads); the converters read the packed weights and scales straight
+// from global memory, one group of four steps ahead, into registers.
 // Warp roles per CTA:
 //   warp 0      lane 0: TMA of the step's rows x 64 bf16 activation tile(s)
-//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads);
-//               lane 1: TMA of the packed E2M1 weights (128 rows x 128 bytes =
-//               256 of K per stage) and, once per item, the E8M0 scales
+//               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads)
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-9   weight converters: thread = one weight row (its TMEM lane)
-//               and one of the step's two 32-element blocks; reads its packed
-//               bytes and scale from shared memory, converts them exactly to
-//               bf16 (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by
-//               the block scale) and stores them into the step's tensor-memory
+//               and one of the step's two 32-element blocks; loads its 16
+//               packed bytes and its scale, converts them exactly to bf16
+//               (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by the
+//               block scale) and stores them into the step's tensor-memory
 //               weight stage with tcgen05.st
 //   warps 10-13 epilogue: tcgen05.ld of the accumulator, SiLU gating (gemm1)
 //               or router-weighted scatter-add (gemm2), global stores
-// Tensor memory per CTA (256 columns): two 32-column weight stages, then one
-// accumulator of 192 (gate_up) or 128 (down) columns.
+// Tensor memory per CTA (256 columns): two (gate_up) or four (down) 32-column
+// weight stages, then one accumulator of 192 (gate_up) or 128 (down) columns.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -63,29 +62,27 @@ namespace {
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarp0 = 2 + kConvWarps;
 constexpr int kPThreads = (kEpiWarp0 + 4) * 32;
-constexpr int kRawStages = 2;                 // packed weight ring: 128 rows x 128 bytes (256 of K)
-constexpr int kRawBytes = kTcW * 128;
-constexpr int kStepsPerRaw = 4;               // steps (64 of K) per packed-weight stage
 constexpr int kWCols = 32;                    // tensor-memory columns per weight stage (64 of K)
+constexpr int kGroupSteps = 4;                // steps per converter load group (256 of K)
 constexpr uint32_t kTmemCols = 256;
 
-// Tile rows, pipeline depth, tensor-memory and shared-memory layout of one
-// CTA; gate_up stages hold one activation tile, down stages two (hi and lo).
+// Tile rows, pipeline depths, tensor-memory and shared-memory layout of one
+// CTA; gate_up activation stages hold one tile, down stages two (hi and lo).
 template <bool GATE_UP>
 struct TcLayout {
   static constexpr int kRows = GATE_UP ? kTcRowsUp : kTcRowsDown;  // MMA N, at most
   static constexpr int kBoxBytes = kRows * 128;                   // one tile: kRows rows x 64 bf16
-  static constexpr int kStages = 2;
+  static constexpr int kActStages = GATE_UP ? 4 : 3;
   static constexpr int kStageBytes = (GATE_UP ? 1 : 2) * kBoxBytes;
-  static constexpr uint32_t kAccCol0 = kStages * kWCols;          // accumulator columns [kAccCol0, +kRows)
+  static constexpr int kWStages = GATE_UP ? 2 : 4;
+  static constexpr uint32_t kAccCol0 = kWStages * kWCols;         // accumulator columns [kAccCol0, +kRows)
   static_assert(kAccCol0 + kRows <= kTmemCols, "tensor memory budget");
   static_assert(kRows % 32 == 0 && kRows <= 256, "MMA N limit");
-  // act ring | raw ring | scales (128 rows x K/32) | mbarriers
-  static constexpr int kRawOff = kStages * kStageBytes;
-  static constexpr int kScaleOff = kRawOff + kRawStages * kRawBytes;
-  static __host__ __device__ int bar_off(int K) { return kScaleOff + kTcW * (K >> 5); }
-  // + 1024 for aligning the base; two CTAs per SM need at most 113 KB each
-  static __host__ __device__ int smem_bytes(int K) { return 1024 + bar_off(K) + 256; }
+  // activation ring | mbarriers; + 1024 for aligning the base: two CTAs per
+  // SM need at most 113 KB each
+  static constexpr int kBarOff = kActStages * kStageBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOff + 256;
+  static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
 struct TcParams {
@@ -255,41 +252,24 @@ __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long ite
   return it;
 }
 
-// Row of the packed-weight (and scale) stage that feeds TMEM lane L.  The
-// stage holds the item's 128 weight rows as two TMA boxes of 64: for gate_up
-// the 64 gate rows then the matching 64 up rows.  Gate_up puts, in every
-// 32-lane quadrant q, 16 gate rows (lanes 0-15) and their up rows (lanes
-// 16-31), so one epilogue warp sees both halves of its 16 activations.
-template <bool GATE_UP>
-__device__ __forceinline__ int stage_row(int L) {
-  if (!GATE_UP) return L;
-  const int q = L >> 5, l = L & 31;
-  return l < 16 ? 16 * q + l : 64 + 16 * q + (l - 16);
-}
-
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                                                               const __grid_constant__ CUtensorMap tmap_w,
-                                                               const __grid_constant__ CUtensorMap tmap_s,
                                                                const TcParams p) {
   using Lay = TcLayout<GATE_UP>;
-  constexpr int kStages = Lay::kStages;
+  constexpr int kActStages = Lay::kActStages;
+  constexpr int kWStages = Lay::kWStages;
   constexpr int kRows = Lay::kRows;
   constexpr int kBoxBytes = Lay::kBoxBytes;
   constexpr uint32_t kAccCol0 = Lay::kAccCol0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* act_ring = smem;
-  uint8_t* raw_ring = smem + Lay::kRawOff;
-  uint8_t* sc_buf = smem + Lay::kScaleOff;  // [128 rows][K/32]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::bar_off(p.K));
-  uint64_t* full = bars;               // [kStages] activation tiles landed + weight stage stored
-  uint64_t* empty = full + kStages;    // [kStages] the step's MMAs are done
-  uint64_t* raw_full = empty + kStages;
-  uint64_t* raw_empty = raw_full + kRawStages;
-  uint64_t* sc_full = raw_empty + kRawStages;
-  uint64_t* sc_empty = sc_full + 1;
-  uint64_t* acc_full = sc_empty + 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+  uint64_t* act_full = bars;                  // [kActStages] activation tiles landed
+  uint64_t* act_empty = act_full + kActStages;  // [kActStages] their MMAs are done
+  uint64_t* w_full = act_empty + kActStages;  // [kWStages] weight stage stored by all converters
+  uint64_t* w_empty = w_full + kWStages;      // [kWStages] its MMAs are done
+  uint64_t* acc_full = w_empty + kWStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -297,16 +277,14 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + kConvWarps);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kActStages; ++s) {
+      mbar_init(&act_full[s], 1);
+      mbar_init(&act_empty[s], 1);
     }
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kConvWarps);
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&w_full[s], kConvWarps);
+      mbar_init(&w_empty[s], 1);
     }
-    mbar_init(sc_full, 1);
-    mbar_init(sc_empty, kConvWarps);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
     mbar_init(drain, 1);
@@ -323,7 +301,6 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
   // a step is 64 of K: gate_up one 64-column tile of x; down the 64-column hi
   // and lo tiles of the activated intermediate (interleaved per 64 columns)
   const int n_steps = p.K / 64;
-  const int n_raw = n_steps / kStepsPerRaw;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -331,88 +308,48 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0, used = 0;
       bool stop = false;
       for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
-        const ItemInfo it = decode_item<Lay::kRows>(p, item);
+        const ItemInfo it = decode_item<kRows>(p, item);
         for (int step = 0; step < n_steps; ++step) {
-          if (used >= (uint32_t)kStages && !mbar_wait(&empty[stage], phase ^ 1u, p.status)) {
+          if (used >= (uint32_t)kActStages && !mbar_wait(&act_empty[stage], phase ^ 1u, p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
           uint8_t* st = act_ring + stage * Lay::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], Lay::kStageBytes);
+          mbar_arrive_expect_tx(&act_full[stage], Lay::kStageBytes);
           if (GATE_UP) {
-            tma_load_2d(st, &tmap_a, 64 * step, it.row0, &full[stage]);
+            tma_load_2d(st, &tmap_a, 64 * step, it.row0, &act_full[stage]);
           } else {
-            tma_load_2d(st, &tmap_a, 128 * step, it.row0, &full[stage]);
-            tma_load_2d(st + kBoxBytes, &tmap_a, 128 * step + 64, it.row0, &full[stage]);
+            tma_load_2d(st, &tmap_a, 128 * step, it.row0, &act_full[stage]);
+            tma_load_2d(st + kBoxBytes, &tmap_a, 128 * step + 64, it.row0, &act_full[stage]);
           }
           ++used;
-          if (++stage == (uint32_t)kStages) {
+          if (++stage == (uint32_t)kActStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       // nothing issued may still be in flight when the CTA exits: wait for the
-      // last min(used, kStages) stages to land
-      for (uint32_t v = 0; v < (used < (uint32_t)kStages ? used : (uint32_t)kStages); ++v) {
-        stage = stage == 0 ? kStages - 1 : stage - 1;
-        if (stage == (uint32_t)kStages - 1) phase ^= 1u;
-        mbar_wait(&full[stage], phase, p.status);
+      // last min(used, kActStages) stages to land
+      for (uint32_t v = 0; v < (used < (uint32_t)kActStages ? used : (uint32_t)kActStages); ++v) {
+        stage = stage == 0 ? kActStages - 1 : stage - 1;
+        if (stage == (uint32_t)kActStages - 1) phase ^= 1u;
+        mbar_wait(&act_full[stage], phase, p.status);
       }
-    } else if (lane == 1) {
-      // ------------------------------------------------------------------ packed weights and scales TMA
-      const int Kb = p.K >> 5;
-      uint32_t rstage = 0, rphase = 0, rused = 0, j = 0;
-      bool stop = false;
-      for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
-        const ItemInfo it = decode_item<Lay::kRows>(p, item);
-        // weight rows of this tile: two blocks of 64 (gate and up rows for gate_up)
-        const int row_a = it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt);
-        const int row_b = GATE_UP ? it.e * p.N + p.I + 64 * it.nt : row_a + 64;
-        if (j >= 1 && !mbar_wait(sc_empty, (j - 1) & 1u, p.status)) {
-          *abort_flag = 1;
-          break;
-        }
-        mbar_arrive_expect_tx(sc_full, kTcW * Kb);
-        tma_load_2d(sc_buf, &tmap_s, 0, row_a, sc_full);
-        tma_load_2d(sc_buf + 64 * Kb, &tmap_s, 0, row_b, sc_full);
-        for (int rs = 0; rs < n_raw; ++rs) {
-          if (rused >= (uint32_t)kRawStages && !mbar_wait(&raw_empty[rstage], rphase ^ 1u, p.status)) {
-            *abort_flag = 1;
-            stop = true;
-            break;
-          }
-          uint8_t* st = raw_ring + rstage * kRawBytes;
-          mbar_arrive_expect_tx(&raw_full[rstage], kRawBytes);
-          tma_load_2d(st, &tmap_w, rs * 128, row_a, &raw_full[rstage]);
-          tma_load_2d(st + 64 * 128, &tmap_w, rs * 128, row_b, &raw_full[rstage]);
-          ++rused;
-          if (++rstage == (uint32_t)kRawStages) {
-            rstage = 0;
-            rphase ^= 1u;
-          }
-        }
-      }
-      for (uint32_t v = 0; v < (rused < (uint32_t)kRawStages ? rused : (uint32_t)kRawStages); ++v) {
-        rstage = rstage == 0 ? kRawStages - 1 : rstage - 1;
-        if (rstage == (uint32_t)kRawStages - 1) rphase ^= 1u;
-        mbar_wait(&raw_full[rstage], rphase, p.status);
-      }
-      if (j >= 1) mbar_wait(sc_full, (j - 1) & 1u, p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, j = 0;
+      uint32_t as = 0, aph = 0, ws = 0, wph = 0, j = 0;
       int item = blockIdx.x;
       ItemInfo it{};
-      if (item < n_items) it = decode_item<Lay::kRows>(p, item);
+      if (item < n_items) it = decode_item<kRows>(p, item);
       const uint32_t act0 = smem_u32(act_ring);
       const uint32_t d = tmem_base + kAccCol0;
       for (; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
         // the next item's routing fields, loaded a whole item ahead
-        const ItemInfo nxt = item + (int)gridDim.x < n_items ? decode_item<Lay::kRows>(p, item + gridDim.x) : it;
+        const ItemInfo nxt = item + (int)gridDim.x < n_items ? decode_item<kRows>(p, item + gridDim.x) : it;
         const uint32_t idesc = idesc_bf16(kTcW, (it.rows + 15) & ~15);  // N: the rows rounded up to 16
         // the epilogue must have read the previous item's accumulator
         if (j >= 1 && !mbar_wait(acc_empty, (j - 1) & 1u, p.status)) {
@@ -422,13 +359,13 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
         tc_fence_after();
         bool ok = true;
         for (int step = 0; step < n_steps; ++step) {
-          if (!mbar_wait(&full[stage], phase, p.status)) {
+          if (!mbar_wait(&w_full[ws], wph, p.status) || !mbar_wait(&act_full[as], aph, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = tmem_base + stage * kWCols;
-          const uint64_t b0 = sw128_desc(act0 + stage * Lay::kStageBytes);
+          const uint32_t a = tmem_base + ws * kWCols;
+          const uint64_t b0 = sw128_desc(act0 + as * Lay::kStageBytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_bf16_ta(d, a + 8 * k, b0 + 2 * k, idesc, (step > 0 || k > 0) ? 1u : 0u);
           if (!GATE_UP) {
@@ -436,10 +373,15 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_bf16_ta(d, a + 8 * k, b1 + 2 * k, idesc, 1u);
           }
-          mma_commit(&empty[stage]);
-          if (++stage == (uint32_t)kStages) {
-            stage = 0;
-            phase ^= 1u;
+          mma_commit(&act_empty[as]);
+          mma_commit(&w_empty[ws]);
+          if (++as == (uint32_t)kActStages) {
+            as = 0;
+            aph ^= 1u;
+          }
+          if (++ws == (uint32_t)kWStages) {
+            ws = 0;
+            wph ^= 1u;
           }
         }
         if (!ok) {
@@ -458,60 +400,56 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
     const int hk = (warp - 2) >> 2;          // which of the step's two blocks
     const int L = 32 * q + lane;             // TMEM lane = weight row of the tile
-    const int rr = stage_row<GATE_UP>(L);    // its row in the packed and scale stages
-    const int Kb = p.K >> 5;
+    const int Kb = p.K >> 5, Kh = p.K >> 1;
     const uint32_t tl = tmem_base + ((uint32_t)(32 * q) << 16) + 16 * hk;
-    const uint8_t* srow = sc_buf + rr * Kb;
-    uint32_t stage = 0, phase = 0, used = 0, rstage = 0, rphase = 0, j = 0;
+    // weight row of TMEM lane L within a tile: for gate_up, every 32-lane
+    // quadrant holds 16 gate rows (lanes 0-15) and their 16 up rows (lanes
+    // 16-31), so one epilogue warp sees both halves of its 16 activations
+    const int lrow = GATE_UP ? ((L & 31) < 16 ? 16 * q + (L & 31) : p.I + 16 * q + (L & 31) - 16) : L;
+    const int n_groups = n_steps / kGroupSteps;
+    uint32_t ws = 0, wph = 0, used = 0;
     bool stop = false;
-    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++j) {
-      if (!mbar_wait(sc_full, j & 1u, p.status)) {
-        *abort_flag = 1;
-        break;
-      }
-      for (int rs = 0; rs < n_raw && !stop; ++rs) {
-        if (!mbar_wait(&raw_full[rstage], rphase, p.status)) {
-          *abort_flag = 1;
-          stop = true;
-          break;
-        }
-        // row rr of the packed stage: 128 bytes = 8 blocks, 16-byte chunks swizzled by (rr & 7)
-        const uint8_t* rrow = raw_ring + rstage * kRawBytes + rr * 128;
-        // the 8 scales of this stage's 8 blocks (Kb is a multiple of 8)
-        const uint2 sc8 = *reinterpret_cast<const uint2*>(srow + 8 * rs);
+    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
+      const ItemInfo it = decode_item<kRows>(p, item);
+      const size_t row = (size_t)it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt) + lrow;
+      const uint8_t* wrow = p.w + row * Kh + 16 * hk;  // block 2 * step + hk at + 32 * step
+      const uint8_t* srow = p.ws + row * Kb;
+      // one group = 4 steps = 8 blocks of the row: 4 blocks of this thread, 8
+      // scale bytes.  qb[i] holds the block of step i of the current group and
+      // is reloaded with the next group's as soon as it is converted.
+      uint4 qb[kGroupSteps];
 #pragma unroll
-        for (int qs = 0; qs < kStepsPerRaw; ++qs) {
-          const int c = 2 * qs + hk;  // block of the stage: this step's first or second half
-          const uint4 qv = *reinterpret_cast<const uint4*>(rrow + ((c ^ (rr & 7)) << 4));
-          const uint32_t s = ((qs < 2 ? sc8.x >> (8 * c) : sc8.y >> (8 * (c - 4))) & 0xFFu);
+      for (int i = 0; i < kGroupSteps; ++i) qb[i] = __ldg(reinterpret_cast<const uint4*>(wrow + 32 * i));
+      uint2 ns = __ldg(reinterpret_cast<const uint2*>(srow));
+      for (int g = 0; g < n_groups && !stop; ++g) {
+        const uint2 cs = ns;
+        const bool more = g + 1 < n_groups;
+        if (more) ns = __ldg(reinterpret_cast<const uint2*>(srow + 8 * (g + 1)));
+#pragma unroll
+        for (int i = 0; i < kGroupSteps; ++i) {
+          const int c = 2 * i + hk;  // block of the group
+          const uint32_t s = ((i < 2 ? cs.x >> (8 * c) : cs.y >> (8 * (c - 4))) & 0xFFu);
           uint4 cv[4];
-          dequant_block(qv, s, cv);
-          if (used >= (uint32_t)kStages && !mbar_wait(&empty[stage], phase ^ 1u, p.status)) {
+          dequant_block(qb[i], s, cv);
+          if (more) qb[i] = __ldg(reinterpret_cast<const uint4*>(wrow + 128 * (g + 1) + 32 * i));
+          if (used >= (uint32_t)kWStages && !mbar_wait(&w_empty[ws], wph ^ 1u, p.status)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
           tc_fence_after();
-          tmem_st16(tl + stage * kWCols, cv);
+          tmem_st16(tl + ws * kWCols, cv);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&full[stage]);
+          if (lane == 0) mbar_arrive(&w_full[ws]);
           ++used;
-          if (++stage == (uint32_t)kStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (++ws == (uint32_t)kWStages) {
+            ws = 0;
+            wph ^= 1u;
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[rstage]);
-        if (++rstage == (uint32_t)kRawStages) {
-          rstage = 0;
-          rphase ^= 1u;
-        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sc_empty);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -555,19 +493,24 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           uint16_t* dst = p.act_out + (size_t)(it.row0 + c0 + (lo_half ? 0 : 16)) * (2 * p.I) + 128 * it.nt +
                           16 * q + (lane & 15);
           const int nvalid = it.rows - c0 - (lo_half ? 0 : 16);
+          // exchange in place: afterwards v[i] is the gate and v[16 + i] the up
+          // value of this lane's token i (all shuffles first, then independent math)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const uint32_t send = lo_half ? v[16 + i] : v[i];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float gt = __uint_as_float(lo_half ? v[i] : recv);
-            const float up = __uint_as_float(lo_half ? recv : v[16 + i]);
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, lo_half ? v[16 + i] : v[i], 16);
+            if (lo_half) v[16 + i] = recv;
+            else v[i] = recv;
+          }
+          const size_t rs = 2 * (size_t)p.I;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
             if (i < nvalid) {
               // a = hi + lo with hi = bf16(a), lo = bf16(a - hi): 16 significant bits
-              const float a = silu(gt) * up;
+              const float a = silu(__uint_as_float(v[i])) * __uint_as_float(v[16 + i]);
               const uint16_t hi = f32_to_bf16_bits(a);
               const uint16_t lo = f32_to_bf16_bits(a - __uint_as_float((uint32_t)hi << 16));
-              dst[(size_t)i * (2 * p.I)] = hi;
-              dst[(size_t)i * (2 * p.I) + 64] = lo;
+              dst[i * rs] = hi;
+              dst[i * rs + 64] = lo;
             }
           }
         } else {
@@ -652,34 +595,13 @@ cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Packed weights or scales, uint8 [rows][cols], boxes of box_cols x 64 rows
-// (128-byte swizzle for the 128-byte packed-weight boxes).
-cudaError_t make_u8_map(CUtensorMap* m, const void* base, long long rows, int cols, int box_cols, bool swizzle) {
-  EncodeTiledFn enc;
-  cudaError_t e = get_encoder(&enc);
-  if (e != cudaSuccess) return e;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, 64u};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <bool GATE_UP>
-cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s, int E) {
-  CUtensorMap map_w, map_s;
-  cudaError_t e0 = make_u8_map(&map_w, p.w, (long long)E * p.N, p.K / 2, 128, true);
-  if (e0 != cudaSuccess) return e0;
-  e0 = make_u8_map(&map_s, p.ws, (long long)E * p.N, p.K / 32, p.K / 32, false);
-  if (e0 != cudaSuccess) return e0;
-  const size_t smem = (size_t)TcLayout<GATE_UP>::smem_bytes(p.K);
+cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
+  const size_t smem = (size_t)TcLayout<GATE_UP>::kSmemBytes;
   auto kern = tc_gemm_kernel<GATE_UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kPThreads, smem, s>>>(map, map_w, map_s, p);
+  kern<<<grid, kPThreads, smem, s>>>(map, p);
   return cudaGetLastError();
 }
 
@@ -719,7 +641,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.outacc = a.outacc;
   p.status = a.status;
   timing_mark(2, false, s);
-  e = launch_tc<true>(map_x, p, 2 * a.num_sms, s, a.E);
+  e = launch_tc<true>(map_x, p, 2 * a.num_sms, s);
   timing_mark(2, true, s);
   if (e != cudaSuccess) return e;
 
@@ -733,7 +655,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.mtiles = a.route.mtiles_dn;
   p2.n_mtiles = a.route.n_mtiles_dn;
   timing_mark(3, false, s);
-  e = launch_tc<false>(map_a, p2, 2 * a.num_sms, s, a.E);
+  e = launch_tc<false>(map_a, p2, 2 * a.num_sms, s);
   timing_mark(3, true, s);
   if (e != cudaSuccess) return e;
 
