@@ -76,8 +76,11 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
   const RouteOut r = route_view(ws, L);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
 
+  // small decode batches are grouped inside the decode kernels
+  const bool route_kernel = L.prefill || (long long)d->T * d->topk > kMaxLocalRoutePairs;
   timing_mark(0, false, s);
-  if (launch_route(ids, d->E, d->T, d->topk, r, L.prefill ? 1 : 0, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (route_kernel && launch_route(ids, d->E, d->T, d->topk, r, L.prefill ? 1 : 0, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   timing_mark(0, true, s);
   cudaError_t e;
   if (L.prefill) {

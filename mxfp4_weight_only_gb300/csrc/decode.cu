@@ -9,6 +9,9 @@
 //   gemm2:  y = W2[e] a  -> ybuf (fp32, rows by flat pair index)
 //   combine: out[t] = bf16( sum_k topk_w[t,k] * y[t*topk + k] ), k ascending.
 //
+// Grouping: the routing kernel's lists, or for up to 128 pairs a grouping
+// every CTA builds itself in shared memory (then no routing kernel runs).
+//
 // Work unit = (active expert, group of up to 8 of its pairs, 32 weight rows x
 // all of K).  For gemm1 the 32 rows are 16 gate rows j..j+15 and the matching
 // 16 up rows I+j.., so the activation is local to the unit.  Units are split
@@ -45,6 +48,14 @@ constexpr int kGroup = 8;             // pair columns per group (one 8-column MM
 constexpr int kRedFloats = kConsumerWarps * kRows * kGroup;  // one reduction buffer
 constexpr int kRedBufs = 3;                                  // reduction ring depth
 static_assert(kGroup == kMoeGroup, "routing and the decode kernels must agree on the group size");
+// Batches of at most kLocalRoute pairs are grouped by every CTA itself, in
+// shared memory, at the start of both kernels: no routing kernel runs before
+// them.  Region: active experts, their first sorted position, their group
+// prefix, sorted pairs, count.
+constexpr int kLocalRoute = 128;
+constexpr int kRouteBytes = 2304;
+static_assert(kRouteBytes >= (4 * kLocalRoute + 3) * 4 && kRouteBytes % 256 == 0, "local grouping region");
+static_assert(kLocalRoute == kMaxLocalRoutePairs, "api and decode kernels must agree on the local routing limit");
 constexpr int kSmemBudget = 226 * 1024;
 
 struct GemmParams {
@@ -59,6 +70,9 @@ struct GemmParams {
   const int32_t* gprefix;  // [n_active+1] exclusive prefix of 8-pair groups over active experts
   const int32_t* sorted_pair;
   int topk;
+  const int32_t* ids;      // topk ids [P], for grouping inside the kernel
+  int E, P;
+  int local;               // 1: group the pairs in shared memory (P <= kLocalRoute)
   float* dst;              // gemm1: abuf [P][I]; gemm2: ybuf [P][N]
   uint32_t* status;
   int row_stride;          // bytes between staged weight rows (K/2 + 16)
@@ -118,14 +132,14 @@ __device__ __forceinline__ void load8(const void* row, int k0, float (&v)[8]) {
 // over the calling warp's blocks [wb0, wb0 + cnt), as f16 scaled by a power of
 // two per pair; inv receives the undo factors for accumulator columns 2t, 2t+1.
 template <WeightKind KIND, bool GATE_UP, int NBW>
-__device__ __forceinline__ void load_frags(const GemmParams& p, int slot0, int base, int npairs, int wb0, int cnt,
-                                           int g, int t, uint32_t (&xf)[NBW][4], float (&inv)[2]) {
+__device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* spair, int slot0, int base, int npairs,
+                                           int wb0, int cnt, int g, int t, uint32_t (&xf)[NBW][4], float (&inv)[2]) {
   const int slot = slot0 + g;
   const bool valid = slot < npairs;
   const void* row = nullptr;
   if (valid) {
     if (GATE_UP) {
-      const int tok = p.sorted_pair[base + slot] / p.topk;
+      const int tok = spair[base + slot] / p.topk;
       row = reinterpret_cast<const uint16_t*>(p.src) + (size_t)tok * p.K;
     } else {
       row = reinterpret_cast<const float*>(p.src) + (size_t)(base + slot) * p.K;
@@ -209,8 +223,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   uint64_t* red_full = empty + S;            // [kRedBufs]
   uint64_t* red_empty = red_full + kRedBufs;  // [kRedBufs]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + kRedBufs);
-  float* red = reinterpret_cast<float*>(smem + 1024);  // [kRedBufs][warps][32 rows][8 pair columns]
-  uint8_t* stages = smem + 1024 + kRedBufs * kRedFloats * sizeof(float);
+  int32_t* r_act = reinterpret_cast<int32_t*>(smem + 1024);  // local grouping, see kLocalRoute
+  int32_t* r_base = r_act + kLocalRoute;
+  int32_t* r_gpre = r_base + kLocalRoute + 1;
+  int32_t* r_pair = r_gpre + kLocalRoute + 1;
+  int32_t* r_n = r_pair + kLocalRoute;
+  float* red = reinterpret_cast<float*>(smem + 1024 + kRouteBytes);  // [kRedBufs][warps][32 rows][8 pair columns]
+  uint8_t* stages = smem + 1024 + kRouteBytes + kRedBufs * kRedFloats * sizeof(float);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -230,12 +249,77 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   if (GATE_UP) grid_dep_wait();
   grid_dep_launch_dependents();
 
+  if (p.local) {
+    // Group the P <= kLocalRoute pairs by expert: stable order (expert
+    // ascending, pair index ascending), active experts ascending, 8-pair
+    // groups per active expert.  Scratch lives in the weight stages, which
+    // nothing uses yet.
+    int32_t* ids_s = reinterpret_cast<int32_t*>(stages);       // [P] expert or -1
+    int32_t* first_g = ids_s + kLocalRoute;                    // [P] groups of its expert at its first pair, else 0
+    const int P = p.P;
+    if (tid < P) {
+      const int e = p.ids[tid];
+      ids_s[tid] = (unsigned)e < (unsigned)p.E ? e : -1;
+    }
+    __syncthreads();
+    int e = -1, less = 0, rank = 0, cnt = 0;
+    if (tid < P) {
+      e = ids_s[tid];
+      if (e >= 0) {
+        for (int q = 0; q < P; ++q) {
+          const int f = ids_s[q];
+          less += (f >= 0 && f < e) ? 1 : 0;
+          cnt += f == e ? 1 : 0;
+          rank += (f == e && q < tid) ? 1 : 0;
+        }
+      }
+      first_g[tid] = (e >= 0 && rank == 0) ? (cnt + kGroup - 1) / kGroup : 0;
+    }
+    __syncthreads();
+    if (tid < P && e >= 0) {
+      r_pair[less + rank] = tid;
+      if (rank == 0) {
+        int dd = 0, gp = 0;
+        for (int q = 0; q < P; ++q) {
+          const int fg = first_g[q];
+          if (fg > 0 && ids_s[q] < e) {
+            ++dd;
+            gp += fg;
+          }
+        }
+        r_act[dd] = e;
+        r_base[dd] = less;
+        r_gpre[dd] = gp;
+      }
+    }
+    if (tid == 0) {
+      int n = 0, tot = 0, gt = 0;
+      for (int q = 0; q < P; ++q) {
+        if (first_g[q] > 0) {
+          ++n;
+          gt += first_g[q];
+        }
+        if (ids_s[q] >= 0) ++tot;
+      }
+      r_base[n] = tot;
+      r_gpre[n] = gt;
+      *r_n = n;
+    }
+    __syncthreads();
+  }
+  // grouping views: shared memory (indexed by active expert) or the routing
+  // kernel's output (offsets indexed by expert id)
+  const bool local = p.local != 0;
+  const int32_t* act = local ? r_act : p.active;
+  const int32_t* gpre = local ? r_gpre : p.gprefix;
+  const int32_t* spair = local ? r_pair : p.sorted_pair;
+
   // Work units: (active expert d, 8-pair group, weight tile j), group-major
   // within an expert, so a CTA's contiguous run reloads activations only at
   // group boundaries.  Experts with more than 8 pairs stream their weights
   // once per group.
-  const int n_act = *p.n_active;
-  const long long n_units = (long long)p.gprefix[n_act] * p.tiles;
+  const int n_act = local ? *r_n : *p.n_active;
+  const long long n_units = (long long)gpre[n_act] * p.tiles;
   const long long u0 = n_units * blockIdx.x / gridDim.x;
   const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
   const int Kh = p.K >> 1;
@@ -246,7 +330,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     int lo = 0, hi = n_act;  // largest d with gprefix[d] * tiles <= u0
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if ((long long)p.gprefix[mid] * p.tiles <= u0) lo = mid; else hi = mid;
+      if ((long long)gpre[mid] * p.tiles <= u0) lo = mid; else hi = mid;
     }
     d0 = lo;
   }
@@ -258,15 +342,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     int d = d0;
     for (long long u = u0; u < u1; ++u, ++issued) {
       if (*abort_flag) break;
-      while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
-      const int j = (int)((u - (long long)p.gprefix[d] * p.tiles) % p.tiles);
+      while ((long long)gpre[d + 1] * p.tiles <= u) ++d;
+      const int j = (int)((u - (long long)gpre[d] * p.tiles) % p.tiles);
       const int stage = (int)(issued % S);
       const long long use = issued / S;
       if (use > 0 && !mbar_wait(&empty[stage], (uint32_t)((use - 1) & 1), p.status)) {
         *abort_flag = 1;
         break;
       }
-      const int e = p.active[d];
+      const int e = act[d];
       uint8_t* sw = stages + (size_t)stage * p.stage_bytes;
       uint8_t* ss = sw + kRows * p.row_stride;
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], kRows * (Kh + p.srow_bytes));
@@ -297,12 +381,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     long long it = 0;
     int d = d0;
     for (long long u = u0; u < u1; ++u, ++it) {
-      while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
-      const long long rem = u - (long long)p.gprefix[d] * p.tiles;
+      while ((long long)gpre[d + 1] * p.tiles <= u) ++d;
+      const long long rem = u - (long long)gpre[d] * p.tiles;
       const int grp = (int)(rem / p.tiles), j = (int)(rem % p.tiles);
-      const int e = p.active[d];
-      const int base = p.offsets[e];
-      const int npairs = p.offsets[e + 1] - base;
+      const int e = act[d];
+      const int base = local ? r_base[d] : p.offsets[e];
+      const int npairs = (local ? r_base[d + 1] : p.offsets[e + 1]) - base;
       const int rbuf = (int)(it % kRedBufs);
       if (!mbar_wait(&red_full[rbuf], (uint32_t)((it / kRedBufs) & 1), p.status)) {
         *abort_flag = 1;
@@ -334,7 +418,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
           for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + r * kGroup + c];
           const int slot = grp * kGroup + c;
           if (slot < npairs) {
-            const int pair = p.sorted_pair[base + slot];
+            const int pair = spair[base + slot];
             p.dst[(size_t)pair * p.N + kRows * j + r] = y;
           }
         }
@@ -361,15 +445,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   int d = d0;
   for (long long u = u0; u < u1; ++u, ++it) {
     if (*abort_flag) break;
-    while ((long long)p.gprefix[d + 1] * p.tiles <= u) ++d;
-    const long long rem = u - (long long)p.gprefix[d] * p.tiles;
+    while ((long long)gpre[d + 1] * p.tiles <= u) ++d;
+    const long long rem = u - (long long)gpre[d] * p.tiles;
     const int grp = (int)(rem / p.tiles);
     const int stage = (int)(it % S);
-    const int e = p.active[d];
-    const int base = p.offsets[e];
-    const int npairs = p.offsets[e + 1] - base;
+    const int e = act[d];
+    const int base = local ? r_base[d] : p.offsets[e];
+    const int npairs = (local ? r_base[d + 1] : p.offsets[e + 1]) - base;
     if (e != cur_e || grp != cur_grp) {
-      load_frags<KIND, GATE_UP, NBW>(p, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
+      load_frags<KIND, GATE_UP, NBW>(p, spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
       cur_e = e;
       cur_grp = grp;
     }
@@ -477,7 +561,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 
 template <WeightKind KIND, bool GATE_UP, int NBW>
 cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
-  const size_t smem = 1024 + kRedBufs * kRedFloats * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
+  const size_t smem = 1024 + kRouteBytes + kRedBufs * kRedFloats * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -498,7 +582,7 @@ void fill_stage_geometry(GemmParams& gp, WeightKind kind) {
   gp.srow_bytes = (gp.K >> 5) * (kind == WeightKind::kMxfp4 ? 1 : 4);
   const int raw = kRows * gp.row_stride + kRows * gp.srow_bytes;
   gp.stage_bytes = (raw + 127) & ~127;
-  const int avail = kSmemBudget - 1024 - kRedBufs * kRedFloats * (int)sizeof(float);
+  const int avail = kSmemBudget - 1024 - kRouteBytes - kRedBufs * kRedFloats * (int)sizeof(float);
   int st = avail / gp.stage_bytes;
   gp.n_stages = st > 8 ? 8 : st;
 }
@@ -520,6 +604,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g1.gprefix = a.route.gprefix;
   g1.sorted_pair = a.route.sorted_pair;
   g1.topk = a.topk;
+  g1.ids = a.topk_ids;
+  g1.E = a.E;
+  g1.P = a.T * a.topk;
+  g1.local = g1.P <= kLocalRoute ? 1 : 0;
   g1.dst = a.abuf;
   g1.status = a.status;
   fill_stage_geometry(g1, a.kind);

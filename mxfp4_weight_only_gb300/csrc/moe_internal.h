@@ -18,6 +18,9 @@ constexpr int kRouteThreads = 1024;
 // Pairs per activation group of the weight-streaming kernels.
 constexpr int kMoeGroup = 8;
 
+// Pairs (tokens x topk) up to which the decode kernels group the pairs
+// themselves and no routing kernel runs.
+constexpr int kMaxLocalRoutePairs = 128;
 // Tokens at or above which MOE_PATH_AUTO picks the tensor-core kernels.
 constexpr int kPrefillMinTokens = 64;
 // Whether the tensor-core (prefill) kernels are built into this library.
