@@ -502,25 +502,48 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
             else v[i] = recv;
           }
           const size_t rs = 2 * (size_t)p.I;
+          // a = hi + lo with hi = bf16(a), lo = bf16(a - hi): 16 significant
+          // bits; all 16 values first, then the stores (predicated only in a
+          // partial chunk)
+          uint32_t hl[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            if (i < nvalid) {
-              // a = hi + lo with hi = bf16(a), lo = bf16(a - hi): 16 significant bits
-              const float a = silu(__uint_as_float(v[i])) * __uint_as_float(v[16 + i]);
-              const uint16_t hi = f32_to_bf16_bits(a);
-              const uint16_t lo = f32_to_bf16_bits(a - __uint_as_float((uint32_t)hi << 16));
-              dst[i * rs] = hi;
-              dst[i * rs + 64] = lo;
+            const float a = silu(__uint_as_float(v[i])) * __uint_as_float(v[16 + i]);
+            const uint32_t hi = f32_to_bf16_bits(a);
+            hl[i] = hi | ((uint32_t)f32_to_bf16_bits(a - __uint_as_float(hi << 16)) << 16);
+          }
+          if (nvalid >= 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              dst[i * rs] = (uint16_t)hl[i];
+              dst[i * rs + 64] = (uint16_t)(hl[i] >> 16);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (i < nvalid) {
+                dst[i * rs] = (uint16_t)hl[i];
+                dst[i * rs + 64] = (uint16_t)(hl[i] >> 16);
+              }
             }
           }
         } else {
           float* dst = p.outacc + kTcW * it.nt + 32 * q + lane;
           const int nvalid = min(32, it.rows - c0);
+          if (nvalid == 32) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int t = __shfl_sync(0xffffffffu, tok[c], i);
-            const float wk = __shfl_sync(0xffffffffu, wgt[c], i);
-            if (i < nvalid) red_add(dst + (size_t)t * p.H, wk * __uint_as_float(v[i]));
+            for (int i = 0; i < 32; ++i) {
+              const int t = __shfl_sync(0xffffffffu, tok[c], i);
+              const float wk = __shfl_sync(0xffffffffu, wgt[c], i);
+              red_add(dst + (size_t)t * p.H, wk * __uint_as_float(v[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int t = __shfl_sync(0xffffffffu, tok[c], i);
+              const float wk = __shfl_sync(0xffffffffu, wgt[c], i);
+              if (i < nvalid) red_add(dst + (size_t)t * p.H, wk * __uint_as_float(v[i]));
+            }
           }
         }
       }
