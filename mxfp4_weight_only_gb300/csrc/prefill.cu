@@ -359,7 +359,8 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
         tc_fence_after();
         bool ok = true;
         for (int step = 0; step < n_steps; ++step) {
-          if (!mbar_wait(&w_full[ws], wph, p.status) || !mbar_wait(&act_full[as], aph, p.status)) {
+          if (!mbar_try_wait2(&w_full[ws], wph, &act_full[as], aph) &&
+              (!mbar_wait(&w_full[ws], wph, p.status) || !mbar_wait(&act_full[as], aph, p.status))) {
             ok = false;
             break;
           }
