@@ -81,6 +81,14 @@ struct GemmParams {
   int n_stages;
 };
 
+// (c0, c1) += s * (x0, x1) as one packed f32x2 FMA (same rounding as two fmaf).
+__device__ __forceinline__ void fma_f32x2_bcast(float& c0, float& c1, float s, float x0, float x1) {
+  asm("{\n .reg .b64 d, a, b, c;\n mov.b64 a, {%2, %2};\n mov.b64 b, {%3, %4};\n mov.b64 c, {%0, %1};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(s), "f"(x0), "f"(x1));
+}
+
 __device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -487,10 +495,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
             float dd[4];
             mma_f16_16816(dd, a0, c0, a1, c1, xf[bb + h][0], xf[bb + h][1], zero);
             mma_f16_16816(dd, a2, c2, a3, c3, xf[bb + h][2], xf[bb + h][3], dd);
-            acc[tl][0] = fmaf(sc[0][h], dd[0], acc[tl][0]);
-            acc[tl][1] = fmaf(sc[0][h], dd[1], acc[tl][1]);
-            acc[tl][2] = fmaf(sc[1][h], dd[2], acc[tl][2]);
-            acc[tl][3] = fmaf(sc[1][h], dd[3], acc[tl][3]);
+            fma_f32x2_bcast(acc[tl][0], acc[tl][1], sc[0][h], dd[0], dd[1]);
+            fma_f32x2_bcast(acc[tl][2], acc[tl][3], sc[1][h], dd[2], dd[3]);
           }
         }
       }
