@@ -221,6 +221,32 @@ __device__ __forceinline__ void weights_to_f16(uint32_t w, uint32_t& o0, uint32_
   else int4x8_to_f16x8(w, o0, o1, o2, o3);
 }
 
+// Position in a contiguous run of work units (active expert d, 8-pair group
+// grp, weight tile j), advanced without divisions (one at the start).
+struct UnitCursor {
+  int d, grp, j, end;  // end = first unit of expert d + 1
+  __device__ __forceinline__ void init(const int32_t* gpre, int tiles, int d0, int u0) {
+    d = d0;
+    const int rem = u0 - gpre[d] * tiles;
+    grp = rem / tiles;
+    j = rem - grp * tiles;
+    end = gpre[d + 1] * tiles;
+  }
+  // step to unit u_next (= the current unit + 1); call only for u_next < the run's end
+  __device__ __forceinline__ void next(const int32_t* gpre, int tiles, int u_next) {
+    if (++j == tiles) {
+      j = 0;
+      ++grp;
+    }
+    if (u_next == end) {  // every active expert has at least one unit
+      ++d;
+      grp = 0;
+      j = 0;
+      end = gpre[d + 1] * tiles;
+    }
+  }
+};
+
 template <WeightKind KIND, bool GATE_UP, int NBW>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -327,9 +353,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   // group boundaries.  Experts with more than 8 pairs stream their weights
   // once per group.
   const int n_act = local ? *r_n : *p.n_active;
-  const long long n_units = (long long)gpre[n_act] * p.tiles;
-  const long long u0 = n_units * blockIdx.x / gridDim.x;
-  const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
+  const int n_units = gpre[n_act] * p.tiles;
+  const int u0 = (int)((long long)n_units * blockIdx.x / gridDim.x);
+  const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x);
   const int Kh = p.K >> 1;
   const int nb = p.K >> 5;
   // first active expert whose units reach u0
@@ -338,7 +364,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     int lo = 0, hi = n_act;  // largest d with gprefix[d] * tiles <= u0
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if ((long long)gpre[mid] * p.tiles <= u0) lo = mid; else hi = mid;
+      if (gpre[mid] * p.tiles <= u0) lo = mid; else hi = mid;
     }
     d0 = lo;
   }
@@ -346,19 +372,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
-    long long issued = 0;
-    int d = d0;
-    for (long long u = u0; u < u1; ++u, ++issued) {
+    int issued = 0, stage = 0;
+    uint32_t phase = 0;
+    UnitCursor cur;
+    if (u0 < u1) cur.init(gpre, p.tiles, d0, u0);
+    for (int u = u0; u < u1; ++u, ++issued) {
       if (*abort_flag) break;
-      while ((long long)gpre[d + 1] * p.tiles <= u) ++d;
-      const int j = (int)((u - (long long)gpre[d] * p.tiles) % p.tiles);
-      const int stage = (int)(issued % S);
-      const long long use = issued / S;
-      if (use > 0 && !mbar_wait(&empty[stage], (uint32_t)((use - 1) & 1), p.status)) {
+      if (u > u0) cur.next(gpre, p.tiles, u);
+      const int j = cur.j;
+      if (issued >= S && !mbar_wait(&empty[stage], phase ^ 1u, p.status)) {
         *abort_flag = 1;
         break;
       }
-      const int e = act[d];
+      const int e = act[cur.d];
       uint8_t* sw = stages + (size_t)stage * p.stage_bytes;
       uint8_t* ss = sw + kRows * p.row_stride;
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], kRows * (Kh + p.srow_bytes));
@@ -374,11 +400,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws) + ((size_t)e * p.N + row0) * p.srow_bytes;
         bulk_g2s(ss + lane * (kRows / 2) * p.srow_bytes, src, rows * p.srow_bytes, &full[stage], policy);
       }
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
-    // make sure nothing issued is still in flight before the CTA can exit
-    const long long first = issued > S ? issued - S : 0;
-    for (long long v = first; v < issued; ++v)
-      mbar_wait(&full[v % S], (uint32_t)((v / S) & 1), p.status);
+    // make sure nothing issued is still in flight before the CTA can exit:
+    // wait for the last min(issued, S) fills, walking the ring backwards
+    for (int v = 0; v < (issued < S ? issued : S); ++v) {
+      if (stage == 0) {
+        stage = S - 1;
+        phase ^= 1u;
+      } else {
+        --stage;
+      }
+      mbar_wait(&full[stage], phase, p.status);
+    }
     return;
   }
 
@@ -386,17 +423,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     // ------------------------------------------------------------ epilogue
     // Sums the consumer warps' partials of each unit and writes the results,
     // while the consumers already work on the next units.
-    long long it = 0;
-    int d = d0;
-    for (long long u = u0; u < u1; ++u, ++it) {
-      while ((long long)gpre[d + 1] * p.tiles <= u) ++d;
-      const long long rem = u - (long long)gpre[d] * p.tiles;
-      const int grp = (int)(rem / p.tiles), j = (int)(rem % p.tiles);
+    int rbuf = 0;
+    uint32_t rph = 0;
+    UnitCursor cur;
+    if (u0 < u1) cur.init(gpre, p.tiles, d0, u0);
+    for (int u = u0; u < u1; ++u) {
+      if (u > u0) cur.next(gpre, p.tiles, u);
+      const int d = cur.d, grp = cur.grp, j = cur.j;
       const int e = act[d];
       const int base = local ? r_base[d] : p.offsets[e];
       const int npairs = (local ? r_base[d + 1] : p.offsets[e + 1]) - base;
-      const int rbuf = (int)(it % kRedBufs);
-      if (!mbar_wait(&red_full[rbuf], (uint32_t)((it / kRedBufs) & 1), p.status)) {
+      if (!mbar_wait(&red_full[rbuf], rph, p.status)) {
         *abort_flag = 1;
         break;
       }
@@ -433,6 +470,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[rbuf]);
+      if (++rbuf == kRedBufs) {
+        rbuf = 0;
+        rph ^= 1u;
+      }
     }
     return;
   }
@@ -449,14 +490,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   int cur_e = -1, cur_grp = -1;
   if (!GATE_UP) grid_dep_wait();  // the activations come from the gate_up kernel
 
-  long long it = 0;
-  int d = d0;
-  for (long long u = u0; u < u1; ++u, ++it) {
+  int it = 0, stage = 0, rbuf = 0;
+  uint32_t phase = 0, rph = 0;
+  UnitCursor cur;
+  if (u0 < u1) cur.init(gpre, p.tiles, d0, u0);
+  for (int u = u0; u < u1; ++u, ++it) {
     if (*abort_flag) break;
-    while ((long long)gpre[d + 1] * p.tiles <= u) ++d;
-    const long long rem = u - (long long)gpre[d] * p.tiles;
-    const int grp = (int)(rem / p.tiles);
-    const int stage = (int)(it % S);
+    if (u > u0) cur.next(gpre, p.tiles, u);
+    const int d = cur.d, grp = cur.grp;
     const int e = act[d];
     const int base = local ? r_base[d] : p.offsets[e];
     const int npairs = (local ? r_base[d + 1] : p.offsets[e + 1]) - base;
@@ -465,7 +506,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
       cur_e = e;
       cur_grp = grp;
     }
-    if (!mbar_wait(&full[stage], (uint32_t)((it / S) & 1), p.status)) {
+    if (!mbar_wait(&full[stage], phase, p.status)) {
       *abort_flag = 1;
       break;
     }
@@ -503,10 +544,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
 
     // ---- hand the partial sums to the epilogue warp
-    const int rbuf = (int)(it % kRedBufs);
-    if (it >= kRedBufs && !mbar_wait(&red_empty[rbuf], (uint32_t)((it / kRedBufs - 1) & 1), p.status)) {
+    if (it >= kRedBufs && !mbar_wait(&red_empty[rbuf], rph ^ 1u, p.status)) {
       *abort_flag = 1;
       break;
     }
@@ -520,6 +564,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&red_full[rbuf]);
+    if (++rbuf == kRedBufs) {
+      rbuf = 0;
+      rph ^= 1u;
+    }
   }
 }
 
