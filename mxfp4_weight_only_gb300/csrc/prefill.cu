@@ -240,10 +240,10 @@ struct ItemInfo {
 };
 
 template <int kRows>
-__device__ __forceinline__ ItemInfo decode_item(const TcParams& p, long long item) {
+__device__ __forceinline__ ItemInfo decode_item(const TcParams& p, int item) {
   ItemInfo it;
-  const int mp = (int)(item / p.n_tiles);
-  it.nt = (int)(item % p.n_tiles);
+  const int mp = item / p.n_tiles;
+  it.nt = item - mp * p.n_tiles;
   const int code = p.mtiles[mp];
   it.e = code >> 20;
   const int mi = code & 0xFFFFF;

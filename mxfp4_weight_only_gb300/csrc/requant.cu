@@ -13,7 +13,7 @@
 // fl32(c / fl32(cmax / 7)) -- the power of two cancels exactly.  The quotient
 // therefore depends only on the two codes, and a 8x8 table of q, built with
 // the same IEEE round-to-nearest divisions at kernel start, replaces the 32
-// divisions.  Groups whose scale byte puts values near the subnormal range or
+// divisions; likewise fl32(amax / 7) = fl32(cmax / 7) * 2^(s-127).  Groups whose scale byte puts values near the subnormal range or
 // near overflow take the per-element division path, so results are bit-exact
 // for every scale byte in [0, 252].
 #include "common.cuh"
@@ -52,17 +52,75 @@ __device__ __forceinline__ uint32_t lookup4(uint32_t nib4, uint32_t pos0, uint32
 // bytes [q0 q1 q2 q3] (each < 16) -> 16-bit value q0 | q1<<4 | q2<<8 | q3<<12 (in bytes 0 and 2)
 __device__ __forceinline__ uint32_t squeeze(uint32_t q4) { return q4 | (q4 >> 4); }
 
+// One group: 16 packed bytes v and scale byte s -> 16 bytes of int4 codes and
+// the fp32 scale.  lut[cmax]: q and (-q)&15 by code; lut_s[cmax] = fl32(cmax/7).
+__device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const uint4* lut, const float* lut_s,
+                                              uint4& q_out, float& s_out) {
+  const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+  // largest magnitude code in the group
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t mg = wd[i] & 0x77777777u;
+    m = __vmaxu4(m, __vmaxu4(mg & 0x0F0F0F0Fu, (mg >> 4) & 0x0F0F0F0Fu));
+  }
+  m = __vmaxu4(m, m >> 16);
+  m = __vmaxu4(m, m >> 8);
+  const uint32_t cmax = m & 0xFu;
+  const float sc_unit = e8m0_to_float(s);
+  uint32_t oq[4];
+  float oscale;
+  if (cmax == 0) {
+    oq[0] = oq[1] = oq[2] = oq[3] = 0u;
+    oscale = 0.f;
+  } else if (s >= kFastLo && s <= kFastHi) {
+    // fl32(cmax * 2^(s-127) / 7) = fl32(cmax / 7) * 2^(s-127): the product is a
+    // normal float for these scale bytes, so the power of two commutes with
+    // the rounding
+    oscale = lut_s[cmax] * sc_unit;
+    const uint4 t = lut[cmax];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = squeeze(lookup4(wd[i], t.x, t.y, t.z, t.w));
+      const uint32_t hi = squeeze(lookup4(wd[i] >> 16, t.x, t.y, t.z, t.w));
+      oq[i] = prmt(lo, hi, 0x6420u);
+    }
+  } else {
+    // exact per-element path (values near the subnormal range or near overflow)
+    const float amax = e2m1_mag(cmax) * sc_unit;
+    oscale = __fdiv_rn(amax, 7.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t r = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t c = (wd[i] >> (4 * j)) & 0xFu;
+        float val = e2m1_mag(c) * sc_unit;
+        val = (c & 8u) ? -val : val;
+        int q = oscale > 0.f ? __float2int_rn(__fdiv_rn(val, oscale)) : 0;
+        q = min(max(q, -8), 7);
+        r |= uint32_t(q & 0xF) << (4 * j);
+      }
+      oq[i] = r;
+    }
+  }
+  q_out = make_uint4(oq[0], oq[1], oq[2], oq[3]);
+  s_out = oscale;
+}
+
 __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t* __restrict__ w,
                                                                   const uint8_t* __restrict__ scale,
                                                                   uint8_t* __restrict__ out_q,
                                                                   float* __restrict__ out_s,
                                                                   long long n_groups) {
   __shared__ uint4 lut[8];  // per cmax: q by code (2 words), (-q)&15 by code (2 words)
+  __shared__ float lut_s[8];  // per cmax: fl32(cmax / 7)
   if (threadIdx.x < 8) {
     const uint32_t cm = threadIdx.x;
     uint32_t pos[2] = {0, 0}, neg[2] = {0, 0};
+    float sc = 0.f;
     if (cm > 0) {
-      const float sc = __fdiv_rn(e2m1_mag(cm), 7.0f);
+      sc = __fdiv_rn(e2m1_mag(cm), 7.0f);
       for (uint32_t c = 0; c < 8; ++c) {
         int q = __float2int_rn(__fdiv_rn(e2m1_mag(c), sc));
         q = min(max(q, -8), 7);
@@ -71,60 +129,35 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
       }
     }
     lut[cm] = make_uint4(pos[0], pos[1], neg[0], neg[1]);
+    lut_s[cm] = sc;
   }
   __syncthreads();
 
+  // two groups per thread and iteration: both loads are in flight together
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups; g += stride) {
-    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(w) + g);
-    const uint32_t s = scale[g];
-    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-    // largest magnitude code in the group
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t mg = wd[i] & 0x77777777u;
-      m = __vmaxu4(m, __vmaxu4(mg & 0x0F0F0F0Fu, (mg >> 4) & 0x0F0F0F0Fu));
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups; g += 2 * stride) {
+    const long long g2 = g + stride;
+    const bool two = g2 < n_groups;
+    const uint4 v0 = __ldcs(reinterpret_cast<const uint4*>(w) + g);
+    const uint32_t s0 = scale[g];
+    uint4 v1 = make_uint4(0, 0, 0, 0);
+    uint32_t s1 = 0;
+    if (two) {
+      v1 = __ldcs(reinterpret_cast<const uint4*>(w) + g2);
+      s1 = scale[g2];
     }
-    m = __vmaxu4(m, m >> 16);
-    m = __vmaxu4(m, m >> 8);
-    const uint32_t cmax = m & 0xFu;
-    const float sc_unit = e8m0_to_float(s);
-    uint32_t oq[4];
-    float oscale;
-    if (cmax == 0) {
-      oq[0] = oq[1] = oq[2] = oq[3] = 0u;
-      oscale = 0.f;
-    } else if (s >= kFastLo && s <= kFastHi) {
-      oscale = __fdiv_rn(e2m1_mag(cmax) * sc_unit, 7.0f);
-      const uint4 t = lut[cmax];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = squeeze(lookup4(wd[i], t.x, t.y, t.z, t.w));
-        const uint32_t hi = squeeze(lookup4(wd[i] >> 16, t.x, t.y, t.z, t.w));
-        oq[i] = prmt(lo, hi, 0x6420u);
-      }
-    } else {
-      // exact per-element path (values near the subnormal range or near overflow)
-      const float amax = e2m1_mag(cmax) * sc_unit;
-      oscale = __fdiv_rn(amax, 7.0f);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t r = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t c = (wd[i] >> (4 * j)) & 0xFu;
-          float val = e2m1_mag(c) * sc_unit;
-          val = (c & 8u) ? -val : val;
-          int q = oscale > 0.f ? __float2int_rn(__fdiv_rn(val, oscale)) : 0;
-          q = min(max(q, -8), 7);
-          r |= uint32_t(q & 0xF) << (4 * j);
-        }
-        oq[i] = r;
-      }
+    uint4 q0;
+    float o0;
+    requant_group(v0, s0, lut, lut_s, q0, o0);
+    __stcs(reinterpret_cast<uint4*>(out_q) + g, q0);
+    __stcs(out_s + g, o0);
+    if (two) {
+      uint4 q1;
+      float o1;
+      requant_group(v1, s1, lut, lut_s, q1, o1);
+      __stcs(reinterpret_cast<uint4*>(out_q) + g2, q1);
+      __stcs(out_s + g2, o1);
     }
-    __stcs(reinterpret_cast<uint4*>(out_q) + g, make_uint4(oq[0], oq[1], oq[2], oq[3]));
-    __stcs(out_s + g, oscale);
   }
 }
 
