@@ -369,23 +369,23 @@ def run_ours(args, rank: int, world: int):
     # ---- e2e through the Python binding, host buffers, copies in the timed region
     T = 1
     hb = [host_batch(1000 + i, T) for i in range(ROTATE)]
-    pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
-    hx = [pin(b[0].view(np.int16)) for b in hb]
-    hids = [pin(b[1]) for b in hb]
-    hw = [pin(b[2]) for b in hb]
+    # one pinned host buffer per step holds x | topk ids | topk weights, so a
+    # step's inputs travel in one host-to-device copy
+    nbx, nbi = T * SHAPE.H * 2, T * SHAPE.topk * 4
+    hin = [torch.from_numpy(np.concatenate([b[0].view(np.uint8).ravel(), b[1].view(np.uint8).ravel(),
+                                            b[2].view(np.uint8).ravel()])).pin_memory() for b in hb]
     hout = [torch.empty((T, SHAPE.H), dtype=torch.int16).pin_memory() for _ in range(ROTATE)]
-    dx = torch.empty((T, SHAPE.H), dtype=torch.int16, device=dev)
-    dids = torch.empty((T, SHAPE.topk), dtype=torch.int32, device=dev)
-    dw = torch.empty((T, SHAPE.topk), dtype=torch.float32, device=dev)
+    din = torch.empty(nbx + 2 * nbi, dtype=torch.uint8, device=dev)
+    dx = din[:nbx].view(torch.bfloat16).view(T, SHAPE.H)
+    dids = din[nbx:nbx + nbi].view(torch.int32).view(T, SHAPE.topk)
+    dw = din[nbx + nbi:].view(torch.float32).view(T, SHAPE.topk)
     dout = torch.empty((T, SHAPE.H), dtype=torch.bfloat16, device=dev)
 
     def e2e_steps(n):
         for i in range(n):
             r = i % ROTATE
-            dx.copy_(hx[r], non_blocking=True)
-            dids.copy_(hids[r], non_blocking=True)
-            dw.copy_(hw[r], non_blocking=True)
-            m.moe_a16w4_mxfp4(dx.view(torch.bfloat16), dids, dw, *copies[i % len(copies)], out=dout, workspace=ws1)
+            din.copy_(hin[r], non_blocking=True)
+            m.moe_a16w4_mxfp4(dx, dids, dw, *copies[i % len(copies)], out=dout, workspace=ws1)
             hout[r].copy_(dout.view(torch.int16), non_blocking=True)
 
     with torch.cuda.stream(stream):
