@@ -307,8 +307,11 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       // ------------------------------------------------------------------ activation TMA
       uint32_t stage = 0, phase = 0, used = 0;
       bool stop = false;
+      ItemInfo nxt{};
+      if ((int)blockIdx.x < n_items) nxt = decode_item<kRows>(p, blockIdx.x);
       for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
-        const ItemInfo it = decode_item<kRows>(p, item);
+        const ItemInfo it = nxt;  // this item's routing fields were loaded an item ahead
+        if (item + (int)gridDim.x < n_items) nxt = decode_item<kRows>(p, item + gridDim.x);
         for (int step = 0; step < n_steps; ++step) {
           if (used >= (uint32_t)kActStages && !mbar_wait(&act_empty[stage], phase ^ 1u, p.status)) {
             *abort_flag = 1;
@@ -410,29 +413,43 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     const int n_groups = n_steps / kGroupSteps;
     uint32_t ws = 0, wph = 0, used = 0;
     bool stop = false;
-    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
-      const ItemInfo it = decode_item<kRows>(p, item);
+    // weight and scale rows of this thread for an item
+    auto rows_of = [&](const ItemInfo& it, const uint8_t*& wr, const uint8_t*& sr) {
       const size_t row = (size_t)it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt) + lrow;
-      const uint8_t* wrow = p.w + row * Kh + 16 * hk;  // block 2 * step + hk at + 32 * step
-      const uint8_t* srow = p.ws + row * Kb;
-      // one group = 4 steps = 8 blocks of the row: 4 blocks of this thread, 8
-      // scale bytes.  qb[i] holds the block of step i of the current group and
-      // is reloaded with the next group's as soon as it is converted.
-      uint4 qb[kGroupSteps];
+      wr = p.w + row * Kh + 16 * hk;  // block 2 * step + hk at + 32 * step
+      sr = p.ws + row * Kb;
+    };
+    // one group = 4 steps = 8 blocks of the row: 4 blocks of this thread, 8
+    // scale bytes.  qb[i] holds the block of step i of the current group and
+    // is reloaded with the next group's -- the next item's first group at the
+    // end of an item -- as soon as it is converted.
+    uint4 qb[kGroupSteps];
+    uint2 ns = make_uint2(0u, 0u);
+    const uint8_t *wrow = nullptr, *srow = nullptr;
+    if ((int)blockIdx.x < n_items) {
+      rows_of(decode_item<kRows>(p, blockIdx.x), wrow, srow);
 #pragma unroll
       for (int i = 0; i < kGroupSteps; ++i) qb[i] = __ldg(reinterpret_cast<const uint4*>(wrow + 32 * i));
-      uint2 ns = __ldg(reinterpret_cast<const uint2*>(srow));
+      ns = __ldg(reinterpret_cast<const uint2*>(srow));
+    }
+    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
+      // the following item's rows, for the loads issued during our last group
+      const bool has_next = item + (int)gridDim.x < n_items;
+      const uint8_t *wrow_n = wrow, *srow_n = srow;
+      if (has_next) rows_of(decode_item<kRows>(p, item + gridDim.x), wrow_n, srow_n);
       for (int g = 0; g < n_groups && !stop; ++g) {
         const uint2 cs = ns;
-        const bool more = g + 1 < n_groups;
-        if (more) ns = __ldg(reinterpret_cast<const uint2*>(srow + 8 * (g + 1)));
+        const bool last = g + 1 == n_groups;
+        const bool more = !last || has_next;
+        const uint8_t* wnext = last ? wrow_n : wrow + 128 * (g + 1);
+        if (more) ns = __ldg(reinterpret_cast<const uint2*>(last ? srow_n : srow + 8 * (g + 1)));
 #pragma unroll
         for (int i = 0; i < kGroupSteps; ++i) {
           const int c = 2 * i + hk;  // block of the group
           const uint32_t s = ((i < 2 ? cs.x >> (8 * c) : cs.y >> (8 * (c - 4))) & 0xFFu);
           uint4 cv[4];
           dequant_block(qb[i], s, cv);
-          if (more) qb[i] = __ldg(reinterpret_cast<const uint4*>(wrow + 128 * (g + 1) + 32 * i));
+          if (more) qb[i] = __ldg(reinterpret_cast<const uint4*>(wnext + 32 * i));
           if (used >= (uint32_t)kWStages && !mbar_wait(&w_empty[ws], wph ^ 1u, p.status)) {
             *abort_flag = 1;
             stop = true;
@@ -451,6 +468,8 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           }
         }
       }
+      wrow = wrow_n;
+      srow = srow_n;
     }
   } else {
     // ------------------------------------------------------------------ epilogue
