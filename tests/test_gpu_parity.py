@@ -121,6 +121,20 @@ def test_moe_ragged_shapes_decode(mw, E, H, I, T, topk):
     assert_moe_close(run_gpu(mw, prob, path=1), ref)
 
 
+@pytest.mark.parametrize("T,topk", [(16, 8), (43, 3), (129, 1)])
+def test_moe_decode_grouping_limit(mw, T, topk):
+    # the weight-streaming kernels group up to 128 pairs themselves and use the
+    # routing kernel above that: P = 128 and P = 129 on either side, with a few
+    # invalid ids, must both match the oracle
+    E, H, I = 24, 512, 256
+    prob = list(gaussian_problem(T * 31 + topk, E, H, I, T, topk))
+    ids = prob[1].copy()
+    ids.reshape(-1)[::17] = -1
+    prob[1] = ids
+    ref = moe.moe_forward(*prob)
+    assert_moe_close(run_gpu(mw, prob, path=1), ref)
+
+
 def test_moe_invalid_and_duplicate_ids(mw):
     prob = list(gaussian_problem(5, 8, 256, 128, 6, 3))
     ids = prob[1]
