@@ -577,6 +577,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
                                                       int H, uint16_t* __restrict__ out) {
   __shared__ int s_ids[64];
   __shared__ float s_w[64];
+  // the next kernel on the stream may start its prologue now; it waits
+  // (griddepcontrol.wait) for this grid to complete before using anything
+  grid_dep_launch_dependents();
   grid_dep_wait();  // ybuf comes from the down kernel
   const int t = blockIdx.y;
   if (threadIdx.x < topk) {
