@@ -439,7 +439,7 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
-def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens):
+def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="mxfp4"):
     """Tensor-core (prefill) path: skewed routing, median of 4 timed calls."""
     rows = {}
     T = prefill_tokens
@@ -460,8 +460,8 @@ def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens):
             arr = (ctypes.c_void_p * 10)(*[ev.cuda_event for ev in kev])
             m._native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 5))
         s_ev.record()
-        m.moe_a16w4_mxfp4(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws,
-                          path=m.MOE_PATH_PREFILL)
+        fn = m.moe_a16w4_mxfp4 if kind == "mxfp4" else m.moe_a16w4_int4g32
+        fn(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws, path=m.MOE_PATH_PREFILL)
         e_ev.record()
         e_ev.synchronize()
         if i >= 2:
@@ -470,7 +470,7 @@ def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens):
     tf = flops / (ms * 1e-3) / 1e12
     names = ["route", "gather", "gemm1_gate_up_tc", "gemm2_down_tc", "cast"]
     kms = {n: round(kev[2 * q].elapsed_time(kev[2 * q + 1]), 3) for q, n in enumerate(names)}
-    rows[f"mxfp4_prefill_T{T}_skewed"] = {
+    rows[f"{'mxfp4' if kind == 'mxfp4' else 'int4g32'}_prefill_T{T}_skewed"] = {
         "ms_per_call": round(ms, 3), "TFLOPs_useful": round(tf, 1), "kernels_ms": kms,
         "bf16_frac_burst": round(tf / peaks["bf16_tflops"], 3),
         "bf16_frac_sustained": round(tf / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]), 3),
@@ -529,6 +529,8 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
         i4[f"T{T}"] = {"us_per_call": round(ms * 1000 / 8, 2), "GBps": round(gbs, 1),
                        "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
     rows["int4g32_decode"] = i4
+    if "prefill" in which:
+        rows.update(prefill_row(torch, m, dev, q_copies, peaks, dev_batch, prefill_tokens, kind="int4"))
     del q_copies
     torch.cuda.empty_cache()
     return rows

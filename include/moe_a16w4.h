@@ -103,8 +103,9 @@ int moe_a16w4_mxfp4(const moe_dims_t* d, const void* x, const int32_t* topk_ids,
  *   w13_q  uint8 [E, 2I, H/2]  two's-complement int4, element 2j low    16-byte aligned
  *   w13_s  float32 [E, 2I, H/32] one scale per 32-group                  16-byte aligned
  *   w2_q   uint8 [E, H, I/2],  w2_s float32 [E, H, I/32]                 16-byte aligned
- * Weight value = q * s.  Only the weight-streaming kernels implement this
- * format; ``d->path`` must be MOE_PATH_AUTO or MOE_PATH_DECODE.
+ * Weight value = q * s.  The weight-streaming kernels apply s to each group's
+ * partial sum in fp32; the tensor-core kernels (large batches, same rules as
+ * moe_a16w4_mxfp4 for ``d->path``) multiply with bf16(fl32(q * s)).
  */
 int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_ids,
                       const float* topk_w, const uint8_t* w13_q, const float* w13_s,

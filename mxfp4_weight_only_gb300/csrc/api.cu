@@ -51,7 +51,6 @@ int common_checks(const moe_dims_t* d, const void* x, const int32_t* ids, const 
   if (!d) return MOE_ERR_NULL;
   if (d->act != MOE_ACT_SWIGLU) return MOE_ERR_UNSUPPORTED_ACT;
   if (!dims_valid(d)) return MOE_ERR_BAD_DIMS;
-  if (kind == WeightKind::kInt4 && d->path == MOE_PATH_PREFILL) return MOE_ERR_BAD_DIMS;
   if (d->path == MOE_PATH_PREFILL && !use_prefill(d, kind)) return MOE_ERR_BAD_DIMS;
   if (d->T == 0) return MOE_OK;
   if (!x || !ids || !tw || !w13 || !s13 || !w2 || !s2 || !out || !ws) return MOE_ERR_NULL;
@@ -87,8 +86,9 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
     PrefillArgs a{};
     a.E = d->E; a.H = d->H; a.I = d->I; a.topk = d->topk; a.T = d->T;
     a.x = x; a.topk_w = tw; a.topk_ids = ids;
-    a.w13 = w13; a.w13_s = reinterpret_cast<const uint8_t*>(s13);
-    a.w2 = w2; a.w2_s = reinterpret_cast<const uint8_t*>(s2);
+    a.kind = kind;
+    a.w13 = w13; a.w13_s = s13;
+    a.w2 = w2; a.w2_s = s2;
     a.out = out; a.route = r;
     a.xs = ws + L.xs; a.as = ws + L.as;
     a.outacc = reinterpret_cast<float*>(ws + L.outacc);
@@ -136,9 +136,9 @@ bool dims_valid(const moe_dims_t* d) {
 }
 
 bool use_prefill(const moe_dims_t* d, WeightKind kind) {
-  if (kind != WeightKind::kMxfp4) return false;
-  // the tensor-core kernels stage a 128-byte-wide K slice of packed weights
-  // and one item's scales (K/32 <= 128 bytes per row) in shared memory
+  (void)kind;  // both weight formats have tensor-core kernels
+  // the tensor-core kernels load packed weights and scales in 256-of-K groups
+  // and their gather kernel handles rows of at most 4096 elements
   const bool ok = (d->H % 512 == 0) && (d->I % 512 == 0) && d->H <= 4096 && d->I <= 4096 && kPrefillAvailable;
   if (d->path == MOE_PATH_PREFILL) return ok;
   if (d->path == MOE_PATH_DECODE) return false;

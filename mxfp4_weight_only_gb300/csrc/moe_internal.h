@@ -122,10 +122,11 @@ struct PrefillArgs {
   const void* x;
   const float* topk_w;
   const int32_t* topk_ids;
+  WeightKind kind;
   const uint8_t* w13;
-  const uint8_t* w13_s;
+  const void* w13_s;  // E8M0 bytes (MXFP4) or fp32 (int4) [E][2I][H/32]
   const uint8_t* w2;
-  const uint8_t* w2_s;
+  const void* w2_s;   // [E][H][I/32]
   void* out;
   RouteOut route;
   void* xs;       // bf16 [P][H]

@@ -47,6 +47,8 @@
 //               (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by the
 //               block scale) and stores them into the step's tensor-memory
 //               weight stage with tcgen05.st
+//               int4_per_group_32 weights: q exact to f16 by a mantissa
+//               trick, then bf16(fl32(q * s)) with the group's fp32 scale
 //   warps 10-13 epilogue: tcgen05.ld of the accumulator, SiLU gating (gemm1)
 //               or router-weighted scatter-add (gemm2), global stores
 // Tensor memory per CTA (256 columns): two (gate_up) or four (down) 32-column
@@ -87,7 +89,7 @@ struct TcLayout {
 
 struct TcParams {
   const uint8_t* w;   // packed [E][N][K/2]
-  const uint8_t* ws;  // E8M0 [E][N][K/32]
+  const void* ws;     // scales [E][N][K/32]: E8M0 bytes (MXFP4) or fp32 (int4)
   int N, K, I, H;
   int n_tiles;        // weight tiles per expert
   const int32_t* mtiles;
@@ -235,6 +237,38 @@ __device__ __forceinline__ void dequant_block(const uint4& q, uint32_t s, uint4 
   }
 }
 
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// 32 int4 values (16 packed bytes, two's complement, element 2j in the low
+// nibble of byte j) of one group with fp32 scale s -> 16 words of two bf16
+// (K order, lower element in the low half): bf16(fl32(q * s)).  Byte j goes
+// to bytes 0 and 2 of a word; masking keeps its low nibble in the low half
+// and its high nibble 4 bits up in the high half, placed in the mantissa of
+// f16 1024; one f16x2 FMA (x1, x1/16 and -1032, -72) leaves the two exact q.
+__device__ __forceinline__ void dequant_block_int4(const uint4& q, float s, uint4 (&out)[4]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] ^ 0x88888888u;  // offset binary: q + 8
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = prmt(u, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
+      const uint32_t h = f16x2_fma((v & 0x00F0000Fu) | 0x64006400u, 0x2C003C00u, 0xD480E408u);
+      float lo, hi;
+      asm("{\n .reg .f16 l, u;\n mov.b32 {l, u}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, u;\n}"
+          : "=f"(lo), "=f"(hi)
+          : "r"(h));
+      o[j] = f32x2_to_bf16x2(lo * s, hi * s);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 struct ItemInfo {
   int e, nt, row0, rows;
 };
@@ -252,7 +286,7 @@ __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, int item) {
   return it;
 }
 
-template <bool GATE_UP>
+template <WeightKind KIND, bool GATE_UP>
 __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                const TcParams p) {
   using Lay = TcLayout<GATE_UP>;
@@ -414,10 +448,22 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     uint32_t ws = 0, wph = 0, used = 0;
     bool stop = false;
     // weight and scale rows of this thread for an item
+    constexpr int kSB = KIND == WeightKind::kMxfp4 ? 1 : 4;  // bytes per scale
     auto rows_of = [&](const ItemInfo& it, const uint8_t*& wr, const uint8_t*& sr) {
       const size_t row = (size_t)it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt) + lrow;
       wr = p.w + row * Kh + 16 * hk;  // block 2 * step + hk at + 32 * step
-      sr = p.ws + row * Kb;
+      sr = reinterpret_cast<const uint8_t*>(p.ws) + row * Kb * kSB;
+    };
+    // scales of one load group: MXFP4 the group's 8 E8M0 bytes; int4 this
+    // thread's 4 fp32 scales (blocks hk, 2 + hk, 4 + hk, 6 + hk of the group)
+    auto load_scales = [&](const uint8_t* sr, int g, uint2& e8, float (&f4)[4]) {
+      if (KIND == WeightKind::kMxfp4) {
+        e8 = __ldg(reinterpret_cast<const uint2*>(sr + 8 * g));
+      } else {
+        const float* sf = reinterpret_cast<const float*>(sr) + 8 * g + hk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f4[i] = __ldg(sf + 2 * i);
+      }
     };
     // one group = 4 steps = 8 blocks of the row: 4 blocks of this thread, 8
     // scale bytes.  qb[i] holds the block of step i of the current group and
@@ -425,12 +471,13 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     // end of an item -- as soon as it is converted.
     uint4 qb[kGroupSteps];
     uint2 ns = make_uint2(0u, 0u);
+    float nf[4] = {0.f, 0.f, 0.f, 0.f};
     const uint8_t *wrow = nullptr, *srow = nullptr;
     if ((int)blockIdx.x < n_items) {
       rows_of(decode_item<kRows>(p, blockIdx.x), wrow, srow);
 #pragma unroll
       for (int i = 0; i < kGroupSteps; ++i) qb[i] = __ldg(reinterpret_cast<const uint4*>(wrow + 32 * i));
-      ns = __ldg(reinterpret_cast<const uint2*>(srow));
+      load_scales(srow, 0, ns, nf);
     }
     for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
       // the following item's rows, for the loads issued during our last group
@@ -439,16 +486,23 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       if (has_next) rows_of(decode_item<kRows>(p, item + gridDim.x), wrow_n, srow_n);
       for (int g = 0; g < n_groups && !stop; ++g) {
         const uint2 cs = ns;
+        float cf[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cf[i] = nf[i];
         const bool last = g + 1 == n_groups;
         const bool more = !last || has_next;
         const uint8_t* wnext = last ? wrow_n : wrow + 128 * (g + 1);
-        if (more) ns = __ldg(reinterpret_cast<const uint2*>(last ? srow_n : srow + 8 * (g + 1)));
+        if (more) load_scales(last ? srow_n : srow, last ? 0 : g + 1, ns, nf);
 #pragma unroll
         for (int i = 0; i < kGroupSteps; ++i) {
           const int c = 2 * i + hk;  // block of the group
-          const uint32_t s = ((i < 2 ? cs.x >> (8 * c) : cs.y >> (8 * (c - 4))) & 0xFFu);
           uint4 cv[4];
-          dequant_block(qb[i], s, cv);
+          if (KIND == WeightKind::kMxfp4) {
+            const uint32_t s = ((i < 2 ? cs.x >> (8 * c) : cs.y >> (8 * (c - 4))) & 0xFFu);
+            dequant_block(qb[i], s, cv);
+          } else {
+            dequant_block_int4(qb[i], cf[i], cv);
+          }
           if (more) qb[i] = __ldg(reinterpret_cast<const uint4*>(wnext + 32 * i));
           if (used >= (uint32_t)kWStages && !mbar_wait(&w_empty[ws], wph ^ 1u, p.status)) {
             *abort_flag = 1;
@@ -638,10 +692,10 @@ cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool GATE_UP>
+template <WeightKind KIND, bool GATE_UP>
 cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
   const size_t smem = (size_t)TcLayout<GATE_UP>::kSmemBytes;
-  auto kern = tc_gemm_kernel<GATE_UP>;
+  auto kern = tc_gemm_kernel<KIND, GATE_UP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kPThreads, smem, s>>>(map, p);
@@ -684,7 +738,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.outacc = a.outacc;
   p.status = a.status;
   timing_mark(2, false, s);
-  e = launch_tc<true>(map_x, p, 2 * a.num_sms, s);
+  e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, true>(map_x, p, 2 * a.num_sms, s)
+                                   : launch_tc<WeightKind::kInt4, true>(map_x, p, 2 * a.num_sms, s);
   timing_mark(2, true, s);
   if (e != cudaSuccess) return e;
 
@@ -698,7 +753,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.mtiles = a.route.mtiles_dn;
   p2.n_mtiles = a.route.n_mtiles_dn;
   timing_mark(3, false, s);
-  e = launch_tc<false>(map_a, p2, 2 * a.num_sms, s);
+  e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, false>(map_a, p2, 2 * a.num_sms, s)
+                                   : launch_tc<WeightKind::kInt4, false>(map_a, p2, 2 * a.num_sms, s);
   timing_mark(3, true, s);
   if (e != cudaSuccess) return e;
 

@@ -250,6 +250,16 @@ def test_moe_prefill_small(mw, E, H, I, T, topk, bias):
     assert_moe_close(run_gpu(mw, prob, path=2), ref)
 
 
+@pytest.mark.parametrize("E,H,I,T,topk,bias", [(8, 512, 512, 200, 4, None), (5, 1024, 512, 130, 3, 2.0)])
+def test_moe_int4_prefill_small(mw, E, H, I, T, topk, bias):
+    x, ids, w, w13, s13, w2, s2 = gaussian_problem(E * 11 + T, E, H, I, T, topk, bias)
+    q13, f13 = requant.requant_mxfp4_to_int4g32(w13, s13)
+    q2, f2 = requant.requant_mxfp4_to_int4g32(w2, s2)
+    prob = (x, ids, w, q13, f13, q2, f2)
+    ref = moe.moe_forward(*prob, kind="int4g32")
+    assert_moe_close(run_gpu(mw, prob, path=2, kind="int4"), ref)
+
+
 def test_moe_prefill_tile_boundaries(mw):
     # gate_up items hold up to 192 rows of one expert, down items 128: expert 0
     # gets 193 rows (192 + 1 and 128 + 65), expert 1 exactly 192 (one item;
@@ -280,6 +290,35 @@ def test_prefill_and_decode_paths_agree_with_oracle(mw):
     assert_moe_close(b, ref)
     c = run_gpu(mw, prob, path=0)  # T >= 64: the automatic choice is the tensor-core path
     assert_moe_close(c, ref)  # the tensor-core combine adds in arrival order: equal within tolerance
+
+
+def test_moe_k3_int4_prefill_sampled(mw, k3_weights):
+    (w13, s13, w2, s2), (dw13, ds13, dw2, ds2) = k3_weights
+    q13, f13 = mw.requant_mxfp4_to_int4g32(dw13, ds13)
+    q2, f2 = mw.requant_mxfp4_to_int4g32(dw2, ds2)
+    T = 1024
+    S = synth.k3(T)
+    g = synth.rng(410)
+    x = synth.activations_bf16(g, T, S.H)
+    ids, w = synth.router_topk(g, T, S.E, S.topk, expert_bias_std=2.0)
+    out = mw.moe_a16w4_int4g32(x_dev(x), dev(ids), dev(w), q13, f13, q2, f2)  # T >= 64: tensor-core path
+    torch.cuda.synchronize()
+    got = formats.bf16_to_f64(out_host(out))
+    toks = np.array([0, T - 1])
+    cols = np.sort(g.choice(S.H, 64, replace=False))
+    need = sorted({int(e) for t in toks for e in ids[t]})
+    oq13 = np.zeros_like(w13[:1]).repeat(S.E, 0)
+    of13 = np.zeros((S.E,) + s13.shape[1:], np.float32)
+    oq2 = np.zeros_like(w2[:1]).repeat(S.E, 0)
+    of2 = np.zeros((S.E,) + s2.shape[1:], np.float32)
+    for e in need:
+        a, b = requant.requant_mxfp4_to_int4g32(w13[e:e + 1], s13[e:e + 1])
+        oq13[e], of13[e] = a[0], b[0]
+        a, b = requant.requant_mxfp4_to_int4g32(w2[e:e + 1], s2[e:e + 1])
+        oq2[e], of2[e] = a[0], b[0]
+    ref = moe.moe_forward_sampled(x, ids, w, oq13, of13, oq2, of2, toks, cols, kind="int4g32")
+    assert_moe_close(got[np.ix_(toks, cols)], ref)
+    assert np.isfinite(got).all()
 
 
 def test_moe_k3_prefill_sampled(mw, k3_weights):
