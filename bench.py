@@ -140,10 +140,18 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def fused_decode(H, I):
+    """True when the library runs both decode GEMMs in one launch: its fused
+    kernel holds activation fragments for at most 8 blocks of 32 per consumer
+    warp (14 warps), i.e. H and I at most 3584."""
+    nbw = lambda K: 2 * ((K // 32 + 27) // 28)
+    return nbw(H) <= 8 and nbw(I) <= 8
+
+
 def committed_traffic():
-    """Per-launch DRAM bytes of the gate_up decode kernel from the committed ncu
+    """Per-launch DRAM bytes of the fused decode kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "decode_gemm1_traffic.json")
+    p = os.path.join(ROOT, "profiles", "decode_fused_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -355,16 +363,22 @@ def run_ours(args, rank: int, world: int):
     ms = max_over_ranks(ms, world, dev)
     us_per_call = ms * 1000.0 / (K * world)
     # per-kernel durations from the last ``timing`` steps of the timed replay
-    names = ["route", "gemm1_gate_up", "gemm2_down", "combine"]
-    kt = {n: [] for n in names}
+    fused = fused_decode(SHAPE.H, SHAPE.I)
+    names = ["route", "gemm_fused_gate_up_down" if fused else "gemm1_gate_up", None if fused else "gemm2_down",
+             "combine"]
+    kt = {n: [] for n in names if n}
     g1_bytes = 0
     for evs, dd in kev:
         for j, n in enumerate(names):
-            kt[n].append(evs[2 * j].elapsed_time(evs[2 * j + 1]) * 1000.0)
-        g1_bytes += dd * W13_BYTES
+            if n:
+                kt[n].append(evs[2 * j].elapsed_time(evs[2 * j + 1]) * 1000.0)
+        g1_bytes += dd * (W13_BYTES + W2_BYTES if fused else W13_BYTES)
     kavg = {n: statistics.mean(v) for n, v in kt.items()}
-    g1_gbs = g1_bytes / (sum(kt["gemm1_gate_up"]) * 1e-6) / 1e9
+    g1_gbs = g1_bytes / (sum(kt[names[1]]) * 1e-6) / 1e9
     layer_gbs = bytes_main / (ms * 1e-3) / 1e9
+    # launches of one T=1 step: grouping inside the GEMM kernels (15 pairs), the
+    # GEMM launch(es), the combine
+    launches_per_step = (1 if SHAPE.topk > 128 else 0) + (1 if fused else 2) + 1
 
     # ---- e2e through the Python binding, host buffers, copies in the timed region
     T = 1
@@ -426,12 +440,16 @@ def run_ours(args, rank: int, world: int):
         "config": workload_config(args.copies),
         "weight_stream_TBps": round(layer_gbs / 1000.0, 3),
         "hbm_frac_layer": round(layer_gbs / peaks["hbm_gbs"], 3),
-        "roofline": {"bound": "hbm", "kernel": "decode_gemm gate_up (mxfp4)", "achieved": round(g1_gbs, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_fused gate_up+down (mxfp4)" if fused else "decode_gemm gate_up (mxfp4)",
+                     "achieved": round(g1_gbs, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(g1_gbs / peaks["hbm_gbs"], 3),
-                     "traffic": traffic, "peak_source": peaks["source"],
-                     "algorithmic_bytes": "distinct active experts x 11,698,176 B (w13 + E8M0 scales) per launch"},
+                     "traffic": traffic if fused else None, "peak_source": peaks["source"],
+                     "algorithmic_bytes": ("distinct active experts x 17,547,264 B (w13 + w2 + E8M0 scales) "
+                                           "per launch" if fused else
+                                           "distinct active experts x 11,698,176 B (w13 + E8M0 scales) per launch")},
         "kernels_us": {k: round(v, 2) for k, v in kavg.items()},
-        "gpu_launches": 4 * K,
+        "gpu_launches": launches_per_step * K,
         "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks, "status": status, "wall_s": round(wall, 4),
         "cpu_baseline": cpu, "rows": rows,

@@ -57,14 +57,14 @@ extern "C" {
 /*
  * Problem size of one MoE layer call.
  *   E     experts held by this GPU (ids 0..E-1)            1 <= E <= 1024
- *   H     hidden size (K of the gate_up GEMM)              multiple of 64, 64 <= H <= 8192
- *   I     intermediate size per expert (K of the down GEMM) multiple of 64, 64 <= I <= 8192
+ *   H     hidden size (K of the gate_up GEMM)              multiple of 64, 64 <= H <= 4096
+ *   I     intermediate size per expert (K of the down GEMM) multiple of 64, 64 <= I <= 4096
  *   topk  experts per token                                1 <= topk <= 64
  *   T     tokens                                           0 <= T, T*topk <= 2^24
  *   act   MOE_ACT_SWIGLU
  *   path  MOE_PATH_*; the tensor-core path additionally needs H and I to be
- *         multiples of 512 and at most 4096 (MOE_PATH_AUTO falls back to the
- *         weight-streaming kernels otherwise)
+ *         multiples of 512 (MOE_PATH_AUTO falls back to the weight-streaming
+ *         kernels otherwise)
  */
 typedef struct moe_dims {
   int32_t E, H, I, topk, T;
@@ -75,7 +75,11 @@ typedef struct moe_dims {
 /* Bytes of scratch that moe_a16w4_mxfp4 / moe_a16w4_int4g32 need for ``d``
  * (0 if ``d`` is invalid).  The caller allocates it (256-byte aligned) and may
  * reuse it across calls that are ordered on one stream; calls that can run
- * concurrently need separate workspaces. */
+ * concurrently need separate workspaces.  The outputs do not depend on what the
+ * workspace held before: the words the kernels synchronise through carry a
+ * per-call value that leftovers do not match.  Only the status word (its
+ * first 4 bytes) reads back what the memory held until it is first cleared:
+ * zero those bytes, or call moe_read_status once, after allocating. */
 size_t moe_workspace_bytes(const moe_dims_t* d);
 
 /*
@@ -143,7 +147,9 @@ int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int
               int32_t* sorted_pair, int32_t* pair_pos, void* stream);
 
 /* Copy the device status word of ``workspace`` (MOE_STATUS_* bits, 0 = clean)
- * into *status and clear it.  Synchronises ``stream``. */
+ * into *status and clear it, together with the words the decode kernels
+ * synchronise through (after a wait that gave up, those may be inconsistent;
+ * read the status before reusing such a workspace).  Synchronises ``stream``. */
 int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream);
 
 /*
@@ -180,10 +186,14 @@ int moe_a16w4_mxfp4_noalloc(const moe_dims_t* d, const void* x, const int32_t* t
  * moe_a16w4_mxfp4 / moe_a16w4_int4g32 call made from this host thread records
  * events[2i] just before and events[2i+1] just after its i-th kernel launch
  * (i < n) on the call's stream; the hook is then cleared.  Kernel order:
- * weight-streaming path 0 grouping, 1 gate_up GEMM, 2 down GEMM, 3 combine;
- * tensor-core path 0 grouping, 1 row gather, 2 gate_up GEMM, 3 down GEMM,
- * 4 combine.  n = 0 clears the hook.  Returns MOE_ERR_BAD_DIMS for n outside
- * [0, 8] and MOE_ERR_NULL for a NULL ``events`` with n > 0.
+ * weight-streaming path 0 grouping, 1 gate_up GEMM, 2 down GEMM, 3 combine,
+ * where H and I are at most 3584 one launch runs both GEMMs (index 1) and
+ * the index-2 events are recorded back to back; tensor-core path 0 grouping,
+ * 1 row gather, 2 gate_up GEMM, 3 down GEMM, 4 combine.  Slots without a
+ * launch (grouping of at most 128 pairs, done inside the decode kernels) are
+ * recorded back to back too.  n = 0 clears the hook.  Returns
+ * MOE_ERR_BAD_DIMS for n outside [0, 8] and MOE_ERR_NULL for a NULL
+ * ``events`` with n > 0.
  */
 int moe_set_timing_events(void* const* events, int32_t n);
 

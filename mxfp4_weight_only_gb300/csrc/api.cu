@@ -104,6 +104,7 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
     a.abuf = reinterpret_cast<float*>(ws + L.abuf);
     a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
     a.status = status; a.num_sms = sms;
+    a.sync = reinterpret_cast<uint32_t*>(ws + L.sync);
     e = launch_decode(a, s);
   }
   g_timing.n = 0;
@@ -127,8 +128,10 @@ void timing_mark(int index, bool end, cudaStream_t s) {
 bool dims_valid(const moe_dims_t* d) {
   if (!d) return false;
   if (d->E < 1 || d->E > kMaxExperts) return false;
-  if (d->H < 64 || d->H > 8192 || d->H % 64) return false;
-  if (d->I < 64 || d->I > 8192 || d->I % 64) return false;
+  // the weight-streaming kernels stage 32 weight rows of the whole K per
+  // pipeline slot and need two slots in shared memory: K <= 4096
+  if (d->H < 64 || d->H > 4096 || d->H % 64) return false;
+  if (d->I < 64 || d->I > 4096 || d->I % 64) return false;
   if (d->topk < 1 || d->topk > 64) return false;
   if (d->T < 0 || (long long)d->T * d->topk > (1ll << 24)) return false;
   if (d->path < MOE_PATH_AUTO || d->path > MOE_PATH_PREFILL) return false;
@@ -151,6 +154,7 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.prefill = use_prefill(d, kind);
   size_t o = 0;
   L.status = o; o = align256(o + 256);
+  L.sync = o; o = align256(o + 4 * kSyncWords);
   L.counts = o; o = align256(o + 4 * E);
   L.offsets = o; o = align256(o + 4 * (E + 1));
   L.active = o; o = align256(o + 4 * E);
@@ -249,7 +253,11 @@ int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the status word, and the fused decode kernel's epoch and flags (a kernel
+  // that gave up a wait may have left them inconsistent)
+  const Workspace L = workspace_layout(d, WeightKind::kMxfp4);
   if (cudaMemsetAsync(ws, 0, sizeof(v), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws + L.sync, 0, 4 * kSyncWords, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   *status = v;
   return MOE_OK;

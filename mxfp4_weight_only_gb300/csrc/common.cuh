@@ -128,6 +128,44 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ---------------------------------------------------------------- flags between CTAs of one grid
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Value that CTA ``slot`` publishes for ``token``: distinct per slot, so no
+// constant fill of the flag array matches, and a bijection of the token
+// (odd multiplier), so flags left by another token never match.
+__device__ __forceinline__ uint32_t published_value(uint32_t token, int slot) {
+  return token * 0x9E3779B1u + (uint32_t)slot;
+}
+
+// One warp waits until every flags[q], q < n, holds published_value(token, q)
+// (acquire), giving up after kWaitLimitNs like mbar_wait.  Every lane returns
+// the same value.
+__device__ __forceinline__ bool wait_all_published(const uint32_t* flags, int n, uint32_t token, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    bool ok = true;
+    for (int q = lane; q < n && ok; q += 32) ok = ld_acquire_gpu(flags + q) == published_value(token, q);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    const bool late = (i & 15u) == 15u && global_ns() - t0 > kWaitLimitNs;
+    if (__any_sync(0xffffffffu, late)) {
+      if (lane == 0) atomicOr(status, kStatusWaitTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 // ---------------------------------------------------------------- numeric helpers
 
 // E8M0 byte -> 2^(s-127) as float (s = 0 gives the subnormal 2^-127).

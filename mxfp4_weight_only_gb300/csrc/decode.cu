@@ -75,6 +75,8 @@ struct GemmParams {
   int local;               // 1: group the pairs in shared memory (P <= kLocalRoute)
   float* dst;              // gemm1: abuf [P][I]; gemm2: ybuf [P][N]
   uint32_t* status;
+  uint32_t* epoch;         // fused kernel: call counter and one publication flag per CTA
+  uint32_t* flags;
   int row_stride;          // bytes between staged weight rows (K/2 + 16)
   int srow_bytes;          // scale bytes per weight row
   int stage_bytes;
@@ -259,239 +261,304 @@ struct UnitCursor {
   }
 };
 
-template <WeightKind KIND, bool GATE_UP, int NBW>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = p.n_stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + S;
-  uint64_t* red_full = empty + S;            // [kRedBufs]
-  uint64_t* red_empty = red_full + kRedBufs;  // [kRedBufs]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red_empty + kRedBufs);
-  int32_t* r_act = reinterpret_cast<int32_t*>(smem + 1024);  // local grouping, see kLocalRoute
-  int32_t* r_base = r_act + kLocalRoute;
-  int32_t* r_gpre = r_base + kLocalRoute + 1;
-  int32_t* r_pair = r_gpre + kLocalRoute + 1;
-  int32_t* r_n = r_pair + kLocalRoute;
-  float* red = reinterpret_cast<float*>(smem + 1024 + kRouteBytes);  // [kRedBufs][warps][32 rows][8 pair columns]
-  uint8_t* stages = smem + 1024 + kRouteBytes + kRedBufs * kRedFloats * sizeof(float);
+// ------------------------------------------------------------------ per-CTA state
 
-  if (tid == 0) {
+constexpr int kMaxStages = 8;  // weight stages at most (fill_stage_geometry caps the count)
+
+// Shared-memory carve-up used by both decode kernels: barriers and flags in
+// the first 1 KiB, the local grouping, the reduction ring, the weight stages.
+struct CtaSmem {
+  uint64_t* full;       // [kMaxStages] weight stage filled
+  uint64_t* empty;      // [kMaxStages] weight stage released by every consumer warp
+  uint64_t* red_full;   // [kRedBufs] partial sums of one unit handed in by every consumer warp
+  uint64_t* red_empty;  // [kRedBufs] reduction buffer drained by the epilogue warp
+  volatile int* abort_flag;
+  uint32_t* token;      // fused kernel: the value this call publishes
+  int32_t* r_act;       // local grouping (batches of at most kLocalRoute pairs)
+  int32_t* r_base;
+  int32_t* r_gpre;
+  int32_t* r_pair;
+  int32_t* r_n;
+  float* red;           // [kRedBufs][warps][32 rows][8 pair columns]
+  uint8_t* stages;
+};
+
+__device__ __forceinline__ CtaSmem carve_smem(uint8_t* smem) {
+  CtaSmem c;
+  c.full = reinterpret_cast<uint64_t*>(smem);
+  c.empty = c.full + kMaxStages;
+  c.red_full = c.empty + kMaxStages;
+  c.red_empty = c.red_full + kRedBufs;
+  c.abort_flag = reinterpret_cast<volatile int*>(c.red_empty + kRedBufs);
+  c.token = reinterpret_cast<uint32_t*>(c.red_empty + kRedBufs) + 1;
+  c.r_act = reinterpret_cast<int32_t*>(smem + 1024);
+  c.r_base = c.r_act + kLocalRoute;
+  c.r_gpre = c.r_base + kLocalRoute + 1;
+  c.r_pair = c.r_gpre + kLocalRoute + 1;
+  c.r_n = c.r_pair + kLocalRoute;
+  c.red = reinterpret_cast<float*>(smem + 1024 + kRouteBytes);
+  c.stages = smem + 1024 + kRouteBytes + kRedBufs * kRedFloats * sizeof(float);
+  return c;
+}
+static_assert((2 * kMaxStages + 2 * kRedBufs) * 8 + 8 <= 1024, "barrier region");
+constexpr int kSmemFixed = 1024 + kRouteBytes + kRedBufs * kRedFloats * (int)sizeof(float);
+
+__device__ __forceinline__ void init_barriers(const CtaSmem& c, int S) {
+  if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], kConsumerWarps);
     }
     for (int b = 0; b < kRedBufs; ++b) {
-      mbar_init(&red_full[b], kConsumerWarps);
-      mbar_init(&red_empty[b], 1);
+      mbar_init(&c.red_full[b], kConsumerWarps);
+      mbar_init(&c.red_empty[b], 1);
     }
-    *abort_flag = 0;
+    *c.abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
-  // gate_up reads the grouping of the kernel before it; down reads only
-  // weights and grouping here and waits for gate_up's activations further down
-  if (GATE_UP) grid_dep_wait();
-  grid_dep_launch_dependents();
+}
 
-  if (p.local) {
-    // Group the P <= kLocalRoute pairs by expert: stable order (expert
-    // ascending, pair index ascending), active experts ascending, 8-pair
-    // groups per active expert.  Scratch lives in the weight stages, which
-    // nothing uses yet.
-    int32_t* ids_s = reinterpret_cast<int32_t*>(stages);       // [P] expert or -1
-    int32_t* first_g = ids_s + kLocalRoute;                    // [P] groups of its expert at its first pair, else 0
-    const int P = p.P;
-    if (tid < P) {
-      const int e = p.ids[tid];
-      ids_s[tid] = (unsigned)e < (unsigned)p.E ? e : -1;
-    }
-    __syncthreads();
-    int e = -1, less = 0, rank = 0, cnt = 0;
-    if (tid < P) {
-      e = ids_s[tid];
-      if (e >= 0) {
-        for (int q = 0; q < P; ++q) {
-          const int f = ids_s[q];
-          less += (f >= 0 && f < e) ? 1 : 0;
-          cnt += f == e ? 1 : 0;
-          rank += (f == e && q < tid) ? 1 : 0;
-        }
-      }
-      first_g[tid] = (e >= 0 && rank == 0) ? (cnt + kGroup - 1) / kGroup : 0;
-    }
-    __syncthreads();
-    if (tid < P && e >= 0) {
-      r_pair[less + rank] = tid;
-      if (rank == 0) {
-        int dd = 0, gp = 0;
-        for (int q = 0; q < P; ++q) {
-          const int fg = first_g[q];
-          if (fg > 0 && ids_s[q] < e) {
-            ++dd;
-            gp += fg;
-          }
-        }
-        r_act[dd] = e;
-        r_base[dd] = less;
-        r_gpre[dd] = gp;
-      }
-    }
-    if (tid == 0) {
-      int n = 0, tot = 0, gt = 0;
+// Group the P <= kLocalRoute pairs by expert (whole CTA): stable order (expert
+// ascending, pair index ascending), active experts ascending, 8-pair groups
+// per active expert.  Scratch lives in the weight stages, which nothing uses
+// yet.  Ends with a CTA barrier.
+__device__ void local_grouping(const GemmParams& p, const CtaSmem& c) {
+  const int tid = threadIdx.x;
+  int32_t* ids_s = reinterpret_cast<int32_t*>(c.stages);  // [P] expert or -1
+  int32_t* first_g = ids_s + kLocalRoute;                 // [P] groups of its expert at its first pair, else 0
+  const int P = p.P;
+  if (tid < P) {
+    const int e = p.ids[tid];
+    ids_s[tid] = (unsigned)e < (unsigned)p.E ? e : -1;
+  }
+  __syncthreads();
+  int e = -1, less = 0, rank = 0, cnt = 0;
+  if (tid < P) {
+    e = ids_s[tid];
+    if (e >= 0) {
       for (int q = 0; q < P; ++q) {
-        if (first_g[q] > 0) {
-          ++n;
-          gt += first_g[q];
-        }
-        if (ids_s[q] >= 0) ++tot;
+        const int f = ids_s[q];
+        less += (f >= 0 && f < e) ? 1 : 0;
+        cnt += f == e ? 1 : 0;
+        rank += (f == e && q < tid) ? 1 : 0;
       }
-      r_base[n] = tot;
-      r_gpre[n] = gt;
-      *r_n = n;
     }
-    __syncthreads();
+    first_g[tid] = (e >= 0 && rank == 0) ? (cnt + kGroup - 1) / kGroup : 0;
   }
-  // grouping views: shared memory (indexed by active expert) or the routing
-  // kernel's output (offsets indexed by expert id)
-  const bool local = p.local != 0;
-  const int32_t* act = local ? r_act : p.active;
-  const int32_t* gpre = local ? r_gpre : p.gprefix;
-  const int32_t* spair = local ? r_pair : p.sorted_pair;
-
-  // Work units: (active expert d, 8-pair group, weight tile j), group-major
-  // within an expert, so a CTA's contiguous run reloads activations only at
-  // group boundaries.  Experts with more than 8 pairs stream their weights
-  // once per group.
-  const int n_act = local ? *r_n : *p.n_active;
-  const int n_units = gpre[n_act] * p.tiles;
-  const int u0 = (int)((long long)n_units * blockIdx.x / gridDim.x);
-  const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x);
-  const int Kh = p.K >> 1;
-  const int nb = p.K >> 5;
-  // first active expert whose units reach u0
-  int d0 = 0;
-  {
-    int lo = 0, hi = n_act;  // largest d with gprefix[d] * tiles <= u0
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (gpre[mid] * p.tiles <= u0) lo = mid; else hi = mid;
-    }
-    d0 = lo;
-  }
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_policy_evict_first();
-    int issued = 0, stage = 0;
-    uint32_t phase = 0;
-    UnitCursor cur;
-    if (u0 < u1) cur.init(gpre, p.tiles, d0, u0);
-    for (int u = u0; u < u1; ++u, ++issued) {
-      if (*abort_flag) break;
-      if (u > u0) cur.next(gpre, p.tiles, u);
-      const int j = cur.j;
-      if (issued >= S && !mbar_wait(&empty[stage], phase ^ 1u, p.status)) {
-        *abort_flag = 1;
-        break;
-      }
-      const int e = act[cur.d];
-      uint8_t* sw = stages + (size_t)stage * p.stage_bytes;
-      uint8_t* ss = sw + kRows * p.row_stride;
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], kRows * (Kh + p.srow_bytes));
-      __syncwarp();
-      {
-        const int row = item_row<GATE_UP>(lane, j, p.I);
-        bulk_g2s(sw + lane * p.row_stride, p.w + ((size_t)e * p.N + row) * Kh, Kh, &full[stage], policy);
-      }
-      if (lane < (GATE_UP ? 2 : 1)) {
-        // scales: gemm1 gate rows then up rows (each contiguous); gemm2 all rows
-        const int rows = GATE_UP ? kRows / 2 : kRows;
-        const int row0 = item_row<GATE_UP>(lane * (kRows / 2), j, p.I);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws) + ((size_t)e * p.N + row0) * p.srow_bytes;
-        bulk_g2s(ss + lane * (kRows / 2) * p.srow_bytes, src, rows * p.srow_bytes, &full[stage], policy);
-      }
-      if (++stage == S) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    // make sure nothing issued is still in flight before the CTA can exit:
-    // wait for the last min(issued, S) fills, walking the ring backwards
-    for (int v = 0; v < (issued < S ? issued : S); ++v) {
-      if (stage == 0) {
-        stage = S - 1;
-        phase ^= 1u;
-      } else {
-        --stage;
-      }
-      mbar_wait(&full[stage], phase, p.status);
-    }
-    return;
-  }
-
-  if (warp == kEpilogueWarp) {
-    // ------------------------------------------------------------ epilogue
-    // Sums the consumer warps' partials of each unit and writes the results,
-    // while the consumers already work on the next units.
-    int rbuf = 0;
-    uint32_t rph = 0;
-    UnitCursor cur;
-    if (u0 < u1) cur.init(gpre, p.tiles, d0, u0);
-    for (int u = u0; u < u1; ++u) {
-      if (u > u0) cur.next(gpre, p.tiles, u);
-      const int d = cur.d, grp = cur.grp, j = cur.j;
-      const int e = act[d];
-      const int base = local ? r_base[d] : p.offsets[e];
-      const int npairs = (local ? r_base[d + 1] : p.offsets[e + 1]) - base;
-      if (!mbar_wait(&red_full[rbuf], rph, p.status)) {
-        *abort_flag = 1;
-        break;
-      }
-      const float* rb = red + rbuf * kRedFloats;
-      if (GATE_UP) {
-        constexpr int kOut = kRows / 2;  // activated outputs per unit
-#pragma unroll
-        for (int q = 0; q < kOut * kGroup / 32; ++q) {
-          const int idx = lane + 32 * q;
-          const int r = idx / kGroup, c = idx % kGroup;
-          float hg = 0.f, hu = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            hg += rb[w * kRows * kGroup + r * kGroup + c];
-            hu += rb[w * kRows * kGroup + (r + kOut) * kGroup + c];
-          }
-          const int slot = grp * kGroup + c;
-          if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + kOut * j + r] = silu(hg) * hu;
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < kRows * kGroup / 32; ++q) {
-          const int idx = lane + 32 * q;
-          const int r = idx / kGroup, c = idx % kGroup;
-          float y = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + r * kGroup + c];
-          const int slot = grp * kGroup + c;
-          if (slot < npairs) {
-            const int pair = spair[base + slot];
-            p.dst[(size_t)pair * p.N + kRows * j + r] = y;
-          }
+  __syncthreads();
+  if (tid < P && e >= 0) {
+    c.r_pair[less + rank] = tid;
+    if (rank == 0) {
+      int dd = 0, gp = 0;
+      for (int q = 0; q < P; ++q) {
+        const int fg = first_g[q];
+        if (fg > 0 && ids_s[q] < e) {
+          ++dd;
+          gp += fg;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_empty[rbuf]);
-      if (++rbuf == kRedBufs) {
-        rbuf = 0;
-        rph ^= 1u;
+      c.r_act[dd] = e;
+      c.r_base[dd] = less;
+      c.r_gpre[dd] = gp;
+    }
+  }
+  if (tid == 0) {
+    int n = 0, tot = 0, gt = 0;
+    for (int q = 0; q < P; ++q) {
+      if (first_g[q] > 0) {
+        ++n;
+        gt += first_g[q];
+      }
+      if (ids_s[q] >= 0) ++tot;
+    }
+    c.r_base[n] = tot;
+    c.r_gpre[n] = gt;
+    *c.r_n = n;
+  }
+  __syncthreads();
+}
+
+// The grouping as the kernels read it: shared memory (indexed by active
+// expert) or the routing kernel's output (offsets indexed by expert id).
+struct Grouping {
+  bool local;
+  const int32_t* act;
+  const int32_t* gpre;
+  const int32_t* spair;
+  const int32_t* r_base;
+  const int32_t* offsets;
+  int n_act;
+  __device__ __forceinline__ int base(int d, int e) const { return local ? r_base[d] : offsets[e]; }
+  __device__ __forceinline__ int end(int d, int e) const { return local ? r_base[d + 1] : offsets[e + 1]; }
+};
+
+__device__ __forceinline__ Grouping grouping_view(const GemmParams& p, const CtaSmem& c) {
+  Grouping g;
+  g.local = p.local != 0;
+  g.act = g.local ? c.r_act : p.active;
+  g.gpre = g.local ? c.r_gpre : p.gprefix;
+  g.spair = g.local ? c.r_pair : p.sorted_pair;
+  g.r_base = c.r_base;
+  g.offsets = p.offsets;
+  g.n_act = g.local ? *c.r_n : *p.n_active;
+  return g;
+}
+
+// This CTA's contiguous run [u0, u1) of a phase's work units (active expert d,
+// 8-pair group, weight tile j; group-major within an expert, so a run reloads
+// activations only at group boundaries; experts with more than 8 pairs stream
+// their weights once per group), and the active expert d0 holding unit u0.
+struct UnitRange {
+  int u0, u1, d0;
+};
+
+__device__ __forceinline__ UnitRange cta_units(const Grouping& gr, int tiles) {
+  UnitRange r;
+  const int n_units = gr.gpre[gr.n_act] * tiles;
+  r.u0 = (int)((long long)n_units * blockIdx.x / gridDim.x);
+  r.u1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x);
+  int lo = 0, hi = gr.n_act;  // largest d with gpre[d] * tiles <= u0
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (gr.gpre[mid] * tiles <= r.u0) lo = mid; else hi = mid;
+  }
+  r.d0 = lo;
+  return r;
+}
+
+// Position in an mbarrier ring, carried from one phase into the next.
+struct RingPos {
+  int n;           // slots taken so far
+  int slot;
+  uint32_t parity;
+  __device__ __forceinline__ void advance(int size) {
+    ++n;
+    if (++slot == size) {
+      slot = 0;
+      parity ^= 1u;
+    }
+  }
+};
+
+// ------------------------------------------------------------------ roles
+
+// Producer warp: one cp.async.bulk per weight row of each unit into the next
+// free stage, plus the unit's scale rows.
+template <bool GATE_UP>
+__device__ void produce_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
+                              uint64_t policy, RingPos& ring) {
+  const int lane = threadIdx.x & 31;
+  const int S = p.n_stages, Kh = p.K >> 1;
+  UnitCursor cur;
+  if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
+  for (int u = r.u0; u < r.u1; ++u) {
+    if (*c.abort_flag) return;
+    if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
+    const int j = cur.j;
+    if (ring.n >= S && !mbar_wait(&c.empty[ring.slot], ring.parity ^ 1u, p.status)) {
+      *c.abort_flag = 1;
+      return;
+    }
+    const int e = gr.act[cur.d];
+    uint8_t* sw = c.stages + (size_t)ring.slot * p.stage_bytes;
+    uint8_t* ss = sw + kRows * p.row_stride;
+    if (lane == 0) mbar_arrive_expect_tx(&c.full[ring.slot], kRows * (Kh + p.srow_bytes));
+    __syncwarp();
+    {
+      const int row = item_row<GATE_UP>(lane, j, p.I);
+      bulk_g2s(sw + lane * p.row_stride, p.w + ((size_t)e * p.N + row) * Kh, Kh, &c.full[ring.slot], policy);
+    }
+    if (lane < (GATE_UP ? 2 : 1)) {
+      // scales: gemm1 gate rows then up rows (each contiguous); gemm2 all rows
+      const int rows = GATE_UP ? kRows / 2 : kRows;
+      const int row0 = item_row<GATE_UP>(lane * (kRows / 2), j, p.I);
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws) + ((size_t)e * p.N + row0) * p.srow_bytes;
+      bulk_g2s(ss + lane * (kRows / 2) * p.srow_bytes, src, rows * p.srow_bytes, &c.full[ring.slot], policy);
+    }
+    ring.advance(S);
+  }
+}
+
+// Before the CTA may exit: wait for the last min(fills, S) fills, walking the
+// ring backwards (earlier ones were consumed).
+__device__ void producer_drain(const CtaSmem& c, int S, RingPos ring, uint32_t* status) {
+  for (int v = 0; v < (ring.n < S ? ring.n : S); ++v) {
+    if (ring.slot == 0) {
+      ring.slot = S - 1;
+      ring.parity ^= 1u;
+    } else {
+      --ring.slot;
+    }
+    mbar_wait(&c.full[ring.slot], ring.parity, status);
+  }
+}
+
+// Epilogue warp: sums the consumer warps' partials of each unit and writes
+// the results while the consumers go on with the next units.
+template <bool GATE_UP>
+__device__ void reduce_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
+                             RingPos& rr) {
+  const int lane = threadIdx.x & 31;
+  UnitCursor cur;
+  if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
+  for (int u = r.u0; u < r.u1; ++u) {
+    if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
+    const int d = cur.d, grp = cur.grp, j = cur.j;
+    const int e = gr.act[d];
+    const int base = gr.base(d, e);
+    const int npairs = gr.end(d, e) - base;
+    if (!mbar_wait(&c.red_full[rr.slot], rr.parity, p.status)) {
+      *c.abort_flag = 1;
+      return;
+    }
+    const float* rb = c.red + rr.slot * kRedFloats;
+    if (GATE_UP) {
+      constexpr int kOut = kRows / 2;  // activated outputs per unit
+#pragma unroll
+      for (int q = 0; q < kOut * kGroup / 32; ++q) {
+        const int idx = lane + 32 * q;
+        const int row = idx / kGroup, col = idx % kGroup;
+        float hg = 0.f, hu = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          hg += rb[w * kRows * kGroup + row * kGroup + col];
+          hu += rb[w * kRows * kGroup + (row + kOut) * kGroup + col];
+        }
+        const int slot = grp * kGroup + col;
+        if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + kOut * j + row] = silu(hg) * hu;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kRows * kGroup / 32; ++q) {
+        const int idx = lane + 32 * q;
+        const int row = idx / kGroup, col = idx % kGroup;
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + row * kGroup + col];
+        const int slot = grp * kGroup + col;
+        if (slot < npairs) {
+          const int pair = gr.spair[base + slot];
+          p.dst[(size_t)pair * p.N + kRows * j + row] = y;
+        }
       }
     }
-    return;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.red_empty[rr.slot]);
+    rr.advance(kRedBufs);
   }
+}
 
-  // -------------------------------------------------------------- consumers
+// Consumer warps: split K, MMA each unit's weight rows against up to 8
+// activation columns held in registers, hand the partial sums to the
+// epilogue warp.
+template <WeightKind KIND, bool GATE_UP, int NBW>
+__device__ void consume_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
+                              RingPos& wr, RingPos& rr) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  const int S = p.n_stages;
+  const int nb = p.K >> 5;
   // even number of blocks per warp, so blocks are processed in pairs
   const int nbw = 2 * ((nb + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps));
   const int wb0 = min(nb, warp * nbw);
@@ -500,29 +567,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   uint32_t xf[NBW][4];
   float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1
   int cur_e = -1, cur_grp = -1;
-  if (!GATE_UP) grid_dep_wait();  // the activations come from the gate_up kernel
-
-  int it = 0, stage = 0, rbuf = 0;
-  uint32_t phase = 0, rph = 0;
   UnitCursor cur;
-  if (u0 < u1) cur.init(gpre, p.tiles, d0, u0);
-  for (int u = u0; u < u1; ++u, ++it) {
-    if (*abort_flag) break;
-    if (u > u0) cur.next(gpre, p.tiles, u);
+  if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
+  for (int u = r.u0; u < r.u1; ++u) {
+    if (*c.abort_flag) return;
+    if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
     const int d = cur.d, grp = cur.grp;
-    const int e = act[d];
-    const int base = local ? r_base[d] : p.offsets[e];
-    const int npairs = (local ? r_base[d + 1] : p.offsets[e + 1]) - base;
+    const int e = gr.act[d];
+    const int base = gr.base(d, e);
+    const int npairs = gr.end(d, e) - base;
     if (e != cur_e || grp != cur_grp) {
-      load_frags<KIND, GATE_UP, NBW>(p, spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
+      load_frags<KIND, GATE_UP, NBW>(p, gr.spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
       cur_e = e;
       cur_grp = grp;
     }
-    if (!mbar_wait(&full[stage], phase, p.status)) {
-      *abort_flag = 1;
-      break;
+    if (!mbar_wait(&c.full[wr.slot], wr.parity, p.status)) {
+      *c.abort_flag = 1;
+      return;
     }
-    const uint8_t* sw = stages + (size_t)stage * p.stage_bytes;
+    const uint8_t* sw = c.stages + (size_t)wr.slot * p.stage_bytes;
     const uint8_t* ss = sw + kRows * p.row_stride;
 
     // ---- main loop over this warp's 32-element blocks, two at a time
@@ -536,12 +599,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
         const int b = wb0 + bb;
 #pragma unroll
         for (int tl = 0; tl < kTiles; ++tl) {
-          const int r = 16 * tl + g;
-          float sc[2][2];  // [row r / r+8][block b / b+1]
-          load_scales2<KIND>(ss, p.srow_bytes, r, b, sc);
+          const int row = 16 * tl + g;
+          float sc[2][2];  // [row / row+8][block b / b+1]
+          load_scales2<KIND>(ss, p.srow_bytes, row, b, sc);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint8_t* rg = sw + r * p.row_stride + (b + h) * 16 + 4 * t;
+            const uint8_t* rg = sw + row * p.row_stride + (b + h) * 16 + 4 * t;
             uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
             weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg), a0, a1, a2, a3);
             weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg + 8 * p.row_stride), c0, c1, c2, c3);
@@ -555,31 +618,110 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == S) {
-      stage = 0;
-      phase ^= 1u;
-    }
+    if (lane == 0) mbar_arrive(&c.empty[wr.slot]);
+    wr.advance(S);
 
     // ---- hand the partial sums to the epilogue warp
-    if (it >= kRedBufs && !mbar_wait(&red_empty[rbuf], rph ^ 1u, p.status)) {
-      *abort_flag = 1;
-      break;
+    if (rr.n >= kRedBufs && !mbar_wait(&c.red_empty[rr.slot], rr.parity ^ 1u, p.status)) {
+      *c.abort_flag = 1;
+      return;
     }
-    float* rw = red + rbuf * kRedFloats + warp * (kRows * kGroup);
+    float* rw = c.red + rr.slot * kRedFloats + warp * (kRows * kGroup);
 #pragma unroll
     for (int tl = 0; tl < kTiles; ++tl) {
-      const int r = 16 * tl + g;
-      *reinterpret_cast<float2*>(rw + r * kGroup + 2 * t) = make_float2(acc[tl][0] * inv[0], acc[tl][1] * inv[1]);
-      *reinterpret_cast<float2*>(rw + (r + 8) * kGroup + 2 * t) =
+      const int row = 16 * tl + g;
+      *reinterpret_cast<float2*>(rw + row * kGroup + 2 * t) = make_float2(acc[tl][0] * inv[0], acc[tl][1] * inv[1]);
+      *reinterpret_cast<float2*>(rw + (row + 8) * kGroup + 2 * t) =
           make_float2(acc[tl][2] * inv[0], acc[tl][3] * inv[1]);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&red_full[rbuf]);
-    if (++rbuf == kRedBufs) {
-      rbuf = 0;
-      rph ^= 1u;
+    if (lane == 0) mbar_arrive(&c.red_full[rr.slot]);
+    rr.advance(kRedBufs);
+  }
+}
+
+// ------------------------------------------------------------------ kernels
+
+// One GEMM stage (gate_up with the activation, or down) as its own launch.
+template <WeightKind KIND, bool GATE_UP, int NBW>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const CtaSmem c = carve_smem(smem);
+  const int warp = threadIdx.x >> 5;
+  init_barriers(c, p.n_stages);
+  // gate_up reads the grouping of the kernel before it; down reads only
+  // weights and grouping here and waits for gate_up's activations further down
+  if (GATE_UP) grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (p.local) local_grouping(p, c);
+  const Grouping gr = grouping_view(p, c);
+  const UnitRange r = cta_units(gr, p.tiles);
+  RingPos wr{0, 0, 0u}, rr{0, 0, 0u};
+  if (warp == kProducerWarp) {
+    produce_units<GATE_UP>(p, gr, r, c, l2_policy_evict_first(), wr);
+    producer_drain(c, p.n_stages, wr, p.status);
+    return;
+  }
+  if (warp == kEpilogueWarp) {
+    reduce_units<GATE_UP>(p, gr, r, c, rr);
+    return;
+  }
+  if (!GATE_UP) grid_dep_wait();  // the activations come from the gate_up kernel
+  consume_units<KIND, GATE_UP, NBW>(p, gr, r, c, wr, rr);
+}
+
+// Both GEMM stages in one persistent launch (grid = one CTA per SM, all
+// resident).  The weight stream runs on from the gate_up units into the down
+// units without a gap; the down units' activations come from every CTA, so
+// before its first down unit a CTA waits until all CTAs have published their
+// gate_up results.  Publication: each CTA's epilogue warp writes the call's
+// token into its own flag (release) after its last activation store; the
+// waiting warp reads all flags (acquire).  The token is epoch + 1, the epoch
+// word being advanced by CTA 0 once every CTA has published (so every CTA
+// read it before); the published values differ per CTA and per token, so
+// flags left by earlier calls (or any constant fill) never match: the flags
+// and the epoch need no clearing between calls.
+template <WeightKind KIND, int NBW>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const GemmParams p1, const GemmParams p2) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const CtaSmem c = carve_smem(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  init_barriers(c, p1.n_stages);
+  grid_dep_wait();  // the grouping of the routing kernel; the previous call's epoch
+  grid_dep_launch_dependents();
+  if (threadIdx.x == 0) *c.token = ld_acquire_gpu(p1.epoch) + 1u;
+  if (p1.local) local_grouping(p1, c);
+  __syncthreads();
+  const uint32_t token = *c.token;
+  const Grouping gr = grouping_view(p1, c);
+  const UnitRange r1 = cta_units(gr, p1.tiles);
+  const UnitRange r2 = cta_units(gr, p2.tiles);
+  RingPos wr{0, 0, 0u}, rr{0, 0, 0u};
+  if (warp == kProducerWarp) {
+    const uint64_t policy = l2_policy_evict_first();
+    produce_units<true>(p1, gr, r1, c, policy, wr);
+    produce_units<false>(p2, gr, r2, c, policy, wr);
+    producer_drain(c, p1.n_stages, wr, p1.status);
+    return;
+  }
+  if (warp == kEpilogueWarp) {
+    reduce_units<true>(p1, gr, r1, c, rr);
+    // publish (also after an abort, so the other CTAs do not wait it out)
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release_gpu(p1.flags + blockIdx.x, published_value(token, blockIdx.x));
+    reduce_units<false>(p2, gr, r2, c, rr);
+    return;
+  }
+  consume_units<KIND, true, NBW>(p1, gr, r1, c, wr, rr);
+  // CTA 0 always waits: it advances the epoch
+  if (r2.u0 < r2.u1 || blockIdx.x == 0) {
+    if (warp == 0) {
+      if (!wait_all_published(p1.flags, gridDim.x, token, p1.status) && lane == 0) *c.abort_flag = 1;
+      if (blockIdx.x == 0 && lane == 0) *p1.epoch = token;
     }
+    named_bar_sync(1, kConsumerWarps * 32);
+    consume_units<KIND, false, NBW>(p2, gr, r2, c, wr, rr);
   }
 }
 
@@ -630,30 +772,55 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 
 template <WeightKind KIND, bool GATE_UP, int NBW>
 cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
-  const size_t smem = 1024 + kRouteBytes + kRedBufs * kRedFloats * sizeof(float) + (size_t)gp.n_stages * gp.stage_bytes;
+  const size_t smem = kSmemFixed + (size_t)gp.n_stages * gp.stage_bytes;
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, gp);
 }
 
+// activation blocks of 32 per consumer warp (even), which sizes the register fragments
+int blocks_per_warp(int K) { return 2 * (((K >> 5) + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps)); }
+
 template <WeightKind KIND, bool GATE_UP>
 cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
-  const int nbw = 2 * (((gp.K >> 5) + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps));
+  const int nbw = blocks_per_warp(gp.K);
   if (nbw <= 8) return launch_gemm<KIND, GATE_UP, 8>(gp, grid, s);
   if (nbw <= 16) return launch_gemm<KIND, GATE_UP, 16>(gp, grid, s);
-  if (nbw <= 24) return launch_gemm<KIND, GATE_UP, 24>(gp, grid, s);
-  return launch_gemm<KIND, GATE_UP, 38>(gp, grid, s);
+  return cudaErrorInvalidValue;  // K above 7168: outside the size limits
 }
 
-void fill_stage_geometry(GemmParams& gp, WeightKind kind) {
-  gp.row_stride = (gp.K >> 1) + 16;
-  gp.srow_bytes = (gp.K >> 5) * (kind == WeightKind::kMxfp4 ? 1 : 4);
-  const int raw = kRows * gp.row_stride + kRows * gp.srow_bytes;
-  gp.stage_bytes = (raw + 127) & ~127;
-  const int avail = kSmemBudget - 1024 - kRouteBytes - kRedBufs * kRedFloats * (int)sizeof(float);
-  int st = avail / gp.stage_bytes;
-  gp.n_stages = st > 8 ? 8 : st;
+// The fused kernel holds fragments for up to 8 blocks per warp (K <= 3584 in
+// both GEMMs).
+constexpr int kFusedNbw = 8;
+
+template <WeightKind KIND>
+cudaError_t launch_fused(const GemmParams& g1, const GemmParams& g2, int grid, cudaStream_t s) {
+  const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
+  auto kern = decode_fused_kernel<KIND, kFusedNbw>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, g1, g2);
+}
+
+int stage_bytes_for(int K, WeightKind kind, int* row_stride, int* srow_bytes) {
+  *row_stride = (K >> 1) + 16;
+  *srow_bytes = (K >> 5) * (kind == WeightKind::kMxfp4 ? 1 : 4);
+  const int raw = kRows * *row_stride + kRows * *srow_bytes;
+  return (raw + 127) & ~127;
+}
+
+// Stage size and count; with ``other`` (fused kernel) one ring serves both
+// GEMMs, its stages sized for the larger.
+void fill_stage_geometry(GemmParams& gp, WeightKind kind, const GemmParams* other = nullptr) {
+  int stage = stage_bytes_for(gp.K, kind, &gp.row_stride, &gp.srow_bytes);
+  if (other) {
+    int rs, sb;
+    stage = max(stage, stage_bytes_for(other->K, kind, &rs, &sb));
+  }
+  gp.stage_bytes = stage;
+  const int st = (kSmemBudget - kSmemFixed) / stage;
+  gp.n_stages = st > kMaxStages ? kMaxStages : st;
 }
 
 }  // namespace
@@ -679,7 +846,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g1.local = g1.P <= kLocalRoute ? 1 : 0;
   g1.dst = a.abuf;
   g1.status = a.status;
-  fill_stage_geometry(g1, a.kind);
+  g1.epoch = a.sync;
+  g1.flags = a.sync ? a.sync + kSyncFlagsOffset : nullptr;
 
   GemmParams g2 = g1;
   g2.w = a.w2;
@@ -689,21 +857,37 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g2.tiles = a.H / kRows;
   g2.src = a.abuf;
   g2.dst = a.ybuf;
-  fill_stage_geometry(g2, a.kind);
+
+  // one launch for both GEMMs when both fit the fused kernel's fragments and
+  // its grid fits the flag array
+  const bool fused = a.sync != nullptr && blocks_per_warp(a.H) <= kFusedNbw && blocks_per_warp(a.I) <= kFusedNbw &&
+                     a.num_sms <= kMaxSyncCtas;
+  fill_stage_geometry(g1, a.kind, fused ? &g2 : nullptr);
+  fill_stage_geometry(g2, a.kind, fused ? &g1 : nullptr);
   if (g1.n_stages < 2 || g2.n_stages < 2) return cudaErrorInvalidValue;
 
   cudaError_t e;
   const bool fp4 = a.kind == WeightKind::kMxfp4;
-  timing_mark(1, false, s);
-  e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, true>(g1, a.num_sms, s)
-          : dispatch_nbw<WeightKind::kInt4, true>(g1, a.num_sms, s);
-  timing_mark(1, true, s);
-  if (e != cudaSuccess) return e;
-  timing_mark(2, false, s);
-  e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, false>(g2, a.num_sms, s)
-          : dispatch_nbw<WeightKind::kInt4, false>(g2, a.num_sms, s);
-  timing_mark(2, true, s);
-  if (e != cudaSuccess) return e;
+  if (fused) {
+    timing_mark(1, false, s);
+    e = fp4 ? launch_fused<WeightKind::kMxfp4>(g1, g2, a.num_sms, s)
+            : launch_fused<WeightKind::kInt4>(g1, g2, a.num_sms, s);
+    timing_mark(1, true, s);
+    if (e != cudaSuccess) return e;
+    timing_mark(2, false, s);
+    timing_mark(2, true, s);
+  } else {
+    timing_mark(1, false, s);
+    e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, true>(g1, a.num_sms, s)
+            : dispatch_nbw<WeightKind::kInt4, true>(g1, a.num_sms, s);
+    timing_mark(1, true, s);
+    if (e != cudaSuccess) return e;
+    timing_mark(2, false, s);
+    e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, false>(g2, a.num_sms, s)
+            : dispatch_nbw<WeightKind::kInt4, false>(g2, a.num_sms, s);
+    timing_mark(2, true, s);
+    if (e != cudaSuccess) return e;
+  }
   dim3 cgrid((a.H / 4 + 127) / 128, a.T);
   timing_mark(3, false, s);
   e = launch_kernel(combine_kernel, cgrid, dim3(128), 0, s, true, (const float*)a.ybuf, a.topk_ids, a.topk_w, a.E,

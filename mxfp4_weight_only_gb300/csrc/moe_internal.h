@@ -38,8 +38,14 @@ constexpr int kTcRowsDown = 128; // sorted rows per down work item (MMA N, at mo
 enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
 
 // Byte offsets of the workspace regions for one problem.
+// Words between the CTAs of the fused decode kernel: an epoch (word 0) and
+// one publication flag per CTA from word kSyncFlagsOffset on.
+constexpr int kSyncFlagsOffset = 32;
+constexpr int kMaxSyncCtas = 1024;
+constexpr int kSyncWords = kSyncFlagsOffset + kMaxSyncCtas;
+
 struct Workspace {
-  size_t status, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles, mtiles_dn,
+  size_t status, sync, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles, mtiles_dn,
       n_mtiles_dn;
   size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
   size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 hi/lo [P][2I], f32 [T][H]
@@ -112,6 +118,7 @@ struct DecodeArgs {
   float* abuf;            // [P][I], rows by sorted position
   float* ybuf;            // [P][H], rows by flat pair index
   uint32_t* status;
+  uint32_t* sync;         // [kSyncWords] epoch and per-CTA flags of the fused kernel
   int num_sms;
 };
 

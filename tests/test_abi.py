@@ -56,6 +56,10 @@ def test_workspace_bytes_host_logic(lib):
     assert 0 < lib.moe_workspace_bytes(ctypes.byref(d1)) < lib.moe_workspace_bytes(ctypes.byref(d32))
     assert lib.moe_workspace_bytes(ctypes.byref(dims(112, 3584 + 32, 3072, 15, 1))) == 0  # H % 64
     assert lib.moe_workspace_bytes(ctypes.byref(dims(0, 256, 128, 2, 4))) == 0
+    # H and I at most 4096 (two pipeline slots of 32 weight rows x K in shared memory)
+    assert lib.moe_workspace_bytes(ctypes.byref(dims(8, 4096, 4096, 2, 4))) > 0
+    assert lib.moe_workspace_bytes(ctypes.byref(dims(8, 4160, 128, 2, 4))) == 0
+    assert lib.moe_workspace_bytes(ctypes.byref(dims(8, 256, 4160, 2, 4))) == 0
 
 
 def _call(lib, d, ptr=16, ws_bytes=1 << 30):

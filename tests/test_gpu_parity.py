@@ -135,6 +135,46 @@ def test_moe_decode_grouping_limit(mw, T, topk):
     assert_moe_close(run_gpu(mw, prob, path=1), ref)
 
 
+@pytest.mark.parametrize("E,H,I,T,topk", [(4, 4096, 256, 3, 2), (3, 256, 3840, 5, 2), (2, 4096, 4096, 2, 3)])
+def test_moe_decode_two_launch_path(mw, E, H, I, T, topk):
+    # H or I above 3584: the gate_up and down GEMMs run as two launches
+    # (wider per-warp activation fragments) instead of the single fused one
+    prob = gaussian_problem(E * 7 + H + I, E, H, I, T, topk)
+    ref = moe.moe_forward(*prob)
+    assert_moe_close(run_gpu(mw, prob, path=1), ref)
+
+
+@pytest.mark.parametrize("fill", ["ones", "ramp", "zeros"])
+def test_fused_decode_workspace_contents_irrelevant(mw, fill):
+    # the fused decode kernel synchronises its CTAs through words in the
+    # workspace; whatever the workspace held before, repeated calls on it must
+    # all match the oracle and each other, also after moe_read_status clears it
+    S = synth.TINY
+    x, ids, w, w13, s13, w2, s2 = gaussian_problem(11, S.E, S.H, S.I, S.T, S.topk)
+    ref = moe.moe_forward(x, ids, w, w13, s13, w2, s2)
+    d = mw.dims(S.E, S.H, S.I, S.topk, S.T, 1)
+    n = mw.moe_workspace_bytes(d)
+    if fill == "ones":
+        ws = torch.full((n,), 255, dtype=torch.uint8, device="cuda")
+    elif fill == "ramp":
+        ws = (torch.arange(n, device="cuda") % 251).to(torch.uint8)
+    else:
+        ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    ws[:4] = 0  # the status word reads what the memory held until first cleared
+    args = (x_dev(x), dev(ids), dev(w), dev(w13), dev(s13), dev(w2), dev(s2))
+    outs = []
+    for i in range(6):
+        if i == 3:
+            assert mw.moe_read_status(d, ws) == 0
+        out = mw.moe_a16w4_mxfp4(*args, workspace=ws, path=1)
+        torch.cuda.synchronize()
+        outs.append(out_host(out).copy())
+    assert mw.moe_read_status(d, ws) == 0
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    assert_moe_close(formats.bf16_to_f64(outs[0]), ref)
+
+
 def test_moe_invalid_and_duplicate_ids(mw):
     prob = list(gaussian_problem(5, 8, 256, 128, 6, 3))
     ids = prob[1]
