@@ -6,8 +6,9 @@
 //   scale = fl32(amax / 7),  q = round_half_even(fl32(w / scale)), q in [-8, 7],
 // an all-zero group giving scale 0 and q 0.
 //
-// One thread per 32-group: 16 bytes in, one scale byte in, 16 bytes and one
-// float out, all coalesced.  HBM-bound.  Division-free fast path: inside the
+// One thread per 32-group and iteration (four per thread in flight): 16 bytes
+// in, one scale byte in, 16 bytes and one float out, all coalesced; one wave
+// of resident CTAs.  HBM-bound.  Division-free fast path: inside the
 // normal float32 range every element is c * 2^(s-127) and the group maximum is
 // cmax * 2^(s-127), so fl32(w / fl32(amax / 7)) equals
 // fl32(c / fl32(cmax / 7)) -- the power of two cancels exactly.  The quotient
@@ -23,6 +24,7 @@ namespace moe {
 namespace {
 
 constexpr int kRequantThreads = 256;
+constexpr int kGroupsPerIter = 4;  // 32-groups per thread and loop iteration
 // Scale bytes inside which the table path is exact (values, amax/7 and the
 // quotients are normal float32 numbers and nothing overflows).
 constexpr uint32_t kFastLo = 8, kFastHi = 250;
@@ -133,30 +135,33 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
   }
   __syncthreads();
 
-  // two groups per thread and iteration: both loads are in flight together
+  // kGroupsPerIter groups per thread and iteration, all loads issued before
+  // any arithmetic, so that many 16-byte loads per thread are in flight
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups; g += 2 * stride) {
-    const long long g2 = g + stride;
-    const bool two = g2 < n_groups;
-    const uint4 v0 = __ldcs(reinterpret_cast<const uint4*>(w) + g);
-    const uint32_t s0 = scale[g];
-    uint4 v1 = make_uint4(0, 0, 0, 0);
-    uint32_t s1 = 0;
-    if (two) {
-      v1 = __ldcs(reinterpret_cast<const uint4*>(w) + g2);
-      s1 = scale[g2];
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups;
+       g += kGroupsPerIter * stride) {
+    uint4 v[kGroupsPerIter];
+    uint32_t sb[kGroupsPerIter];
+#pragma unroll
+    for (int i = 0; i < kGroupsPerIter; ++i) {
+      const long long gi = g + i * stride;
+      v[i] = make_uint4(0, 0, 0, 0);
+      sb[i] = 0;
+      if (gi < n_groups) {
+        v[i] = __ldcs(reinterpret_cast<const uint4*>(w) + gi);
+        sb[i] = scale[gi];
+      }
     }
-    uint4 q0;
-    float o0;
-    requant_group(v0, s0, lut, lut_s, q0, o0);
-    __stcs(reinterpret_cast<uint4*>(out_q) + g, q0);
-    __stcs(out_s + g, o0);
-    if (two) {
-      uint4 q1;
-      float o1;
-      requant_group(v1, s1, lut, lut_s, q1, o1);
-      __stcs(reinterpret_cast<uint4*>(out_q) + g2, q1);
-      __stcs(out_s + g2, o1);
+#pragma unroll
+    for (int i = 0; i < kGroupsPerIter; ++i) {
+      const long long gi = g + i * stride;
+      if (gi < n_groups) {
+        uint4 q;
+        float o;
+        requant_group(v[i], sb[i], lut, lut_s, q, o);
+        __stcs(reinterpret_cast<uint4*>(out_q) + gi, q);
+        __stcs(out_s + gi, o);
+      }
     }
   }
 }
@@ -171,8 +176,15 @@ cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  // one wave: as many CTAs as are resident at once (a second, partial wave
+  // would leave most SMs idle at the end)
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel, kRequantThreads, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
   const long long want = (n_groups + kRequantThreads - 1) / kRequantThreads;
-  const int grid = (int)(want < (long long)sms * 8 ? want : (long long)sms * 8);
+  const long long resident = (long long)sms * per_sm;
+  const int grid = (int)(want < resident ? want : resident);
   requant_kernel<<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
   return cudaGetLastError();
 }
