@@ -19,6 +19,17 @@ For each pair (t, k) with e = topk_ids[t, k] in [0, E):
     y = W2[e] @ a                    (H values)
     out[t] += topk_weights[t, k] * y  (k ascending)
 All in float64 from exact inputs.  Pairs with invalid ids add nothing.
+
+Optional variants (not on the benchmarked path; the kernels do not take them
+yet):
+* biases: ``create_weights`` registers ``w13_bias`` bf16[E, 2I] and
+  ``w2_bias`` bf16[E, H] when the layer has biases, and
+  ``get_fused_moe_quant_config`` hands them to the kernel as ``w1_bias`` /
+  ``w2_bias``.  The pages print no formula; read as the bias of each linear
+  map: h = W13[e] @ x[t] + b13[e], y = W2[e] @ a + b2[e].
+* ``apply_router_weight_on_input`` (``apply``): read as x[t] scaled by the
+  pair's router weight before stage 1, and the combine summing the pairs'
+  outputs unweighted.
 """
 
 from __future__ import annotations
@@ -33,11 +44,20 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
-def _expert_mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray) -> np.ndarray:
+def _expert_mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray, b13=None, b2=None) -> np.ndarray:
     I = W13.shape[0] // 2
     h = X @ W13.T
+    if b13 is not None:
+        h = h + b13
     a = silu(h[:, :I]) * h[:, I:]
-    return a @ W2.T
+    y = a @ W2.T
+    if b2 is not None:
+        y = y + b2
+    return y
+
+
+def _bias_rows(b_bits, e):
+    return None if b_bits is None else formats.bf16_to_f64(np.asarray(b_bits)[e])
 
 
 def dequant_int4(q_packed: np.ndarray, scales_f32: np.ndarray) -> np.ndarray:
@@ -58,8 +78,11 @@ def _deq(kind: str, w: np.ndarray, s: np.ndarray) -> np.ndarray:
     raise ValueError(kind)
 
 
-def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4") -> np.ndarray:
-    """Full MoE output, float64[T, H].  ``x_bits`` are bfloat16 bit patterns uint16[T, H]."""
+def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4", b13=None, b2=None,
+                router_weight_on_input: bool = False) -> np.ndarray:
+    """Full MoE output, float64[T, H].  ``x_bits`` are bfloat16 bit patterns
+    uint16[T, H]; ``b13`` / ``b2`` optional bias bit patterns uint16[E, 2I] /
+    uint16[E, H]."""
     X = formats.bf16_to_f64(x_bits)
     T, H = X.shape
     ids = np.asarray(topk_ids)
@@ -74,10 +97,13 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4")
             continue
         W13 = _deq(kind, w13[e], s13[e])
         W2 = _deq(kind, w2[e], s2[e])
-        y[pairs] = _expert_mlp(X[pairs // topk], W13, W2)
+        Xp = X[pairs // topk]
+        if router_weight_on_input:
+            Xp = Xp * w.reshape(-1)[pairs][:, None]
+        y[pairs] = _expert_mlp(Xp, W13, W2, _bias_rows(b13, e), _bias_rows(b2, e))
     out = np.zeros((T, H), dtype=np.float64)
     for k in range(topk):
-        out += w[:, k:k + 1] * y[k::topk]
+        out += y[k::topk] if router_weight_on_input else w[:, k:k + 1] * y[k::topk]
     return out
 
 

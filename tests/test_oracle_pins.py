@@ -254,6 +254,70 @@ def test_moe_invariants():
     assert np.all(moe.moe_forward(np.zeros_like(x), ids, w, w13, s13, w2, s2) == 0)
 
 
+def _bias_bits(g, shape, std=0.5):
+    return synth.bf16_bits_from_f32(synth.gaussian(g, shape, std))
+
+
+def _dense_torch_variants(x, ids, w, w13, s13, w2, s2, b13, b2, on_input):
+    """Every expert on every token through torch's linear-with-bias, then the
+    top-k selection (router weight on the input or on the output)."""
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double()
+    W13 = torch.from_numpy(formats.dequant_mxfp4(w13, s13))
+    W2 = torch.from_numpy(formats.dequant_mxfp4(w2, s2))
+    B13 = torch.from_numpy(b13.view(np.int16)).view(torch.bfloat16).double()
+    B2 = torch.from_numpy(b2.view(np.int16)).view(torch.bfloat16).double()
+    E, I = W13.shape[0], W13.shape[1] // 2
+    out = torch.zeros(X.shape, dtype=torch.float64)
+    for t in range(ids.shape[0]):
+        for k in range(ids.shape[1]):
+            e = int(ids[t, k])
+            if not 0 <= e < E:
+                continue
+            xt = X[t] * float(w[t, k]) if on_input else X[t]
+            h = torch.nn.functional.linear(xt, W13[e], B13[e])
+            a = torch.nn.functional.silu(h[:I]) * h[I:]
+            y = torch.nn.functional.linear(a, W2[e], B2[e])
+            out[t] += y if on_input else float(w[t, k]) * y
+    return out.numpy()
+
+
+@pytest.mark.parametrize("on_input", [False, True])
+def test_moe_bias_and_router_weight_on_input_match_torch_linear(on_input):
+    x, ids, w, w13, s13, w2, s2 = _tiny_problem(21, T=6, topk=3)
+    ids[1, 2] = -1
+    g = synth.rng(22)
+    E, I2, H = w13.shape[0], w13.shape[1], w2.shape[1]
+    b13, b2 = _bias_bits(g, (E, I2)), _bias_bits(g, (E, H))
+    ours = moe.moe_forward(x, ids, w, w13, s13, w2, s2, b13=b13, b2=b2, router_weight_on_input=on_input)
+    ref = _dense_torch_variants(x, ids, w, w13, s13, w2, s2, b13, b2, on_input)
+    assert np.allclose(ours, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_bias_closed_form_with_zero_weights():
+    # all-zero E2M1 codes: h = b13, y = b2, so out[t] = sum_k w[t,k] * b2[e]
+    # (router weight on the output) or sum_k b2[e] (router weight on the input)
+    x, ids, w, w13, s13, w2, s2 = _tiny_problem(23, T=5, topk=2)
+    ids[3, 1] = 8  # invalid
+    g = synth.rng(24)
+    E, I2, H = w13.shape[0], w13.shape[1], w2.shape[1]
+    b13, b2 = _bias_bits(g, (E, I2)), _bias_bits(g, (E, H))
+    z13, z2 = np.zeros_like(w13), np.zeros_like(w2)
+    B2 = formats.bf16_to_f64(b2)
+    want_w = np.zeros((ids.shape[0], H))
+    want_1 = np.zeros((ids.shape[0], H))
+    for t in range(ids.shape[0]):
+        for k in range(ids.shape[1]):
+            if 0 <= ids[t, k] < E:
+                want_w[t] += float(w[t, k]) * B2[ids[t, k]]
+                want_1[t] += B2[ids[t, k]]
+    got_w = moe.moe_forward(x, ids, w, z13, s13, z2, s2, b13=b13, b2=b2)
+    got_1 = moe.moe_forward(x, ids, w, z13, s13, z2, s2, b13=b13, b2=b2, router_weight_on_input=True)
+    assert np.array_equal(got_w, want_w)
+    assert np.array_equal(got_1, want_1)
+    # without biases the same weights give zero
+    assert np.all(moe.moe_forward(x, ids, w, z13, s13, z2, s2) == 0)
+
+
 def test_moe_sampled_matches_full():
     x, ids, w, w13, s13, w2, s2 = _tiny_problem(11, T=9, topk=3)
     full = moe.moe_forward(x, ids, w, w13, s13, w2, s2)
