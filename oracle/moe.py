@@ -30,6 +30,8 @@ yet):
 * ``apply_router_weight_on_input`` (``apply``): read as x[t] scaled by the
   pair's router weight before stage 1, and the combine summing the pairs'
   outputs unweighted.
+* ``expert_map`` (``apply``, expert parallelism): global ids mapped to local
+  ids (or -1) before the grouping, as in ``route.route``.
 """
 
 from __future__ import annotations
@@ -37,7 +39,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import formats
-from .route import route
+from .route import local_ids, route
 
 
 def silu(z: np.ndarray) -> np.ndarray:
@@ -79,17 +81,18 @@ def _deq(kind: str, w: np.ndarray, s: np.ndarray) -> np.ndarray:
 
 
 def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4", b13=None, b2=None,
-                router_weight_on_input: bool = False) -> np.ndarray:
+                router_weight_on_input: bool = False, expert_map=None) -> np.ndarray:
     """Full MoE output, float64[T, H].  ``x_bits`` are bfloat16 bit patterns
     uint16[T, H]; ``b13`` / ``b2`` optional bias bit patterns uint16[E, 2I] /
-    uint16[E, H]."""
+    uint16[E, H]; ``expert_map`` optional int32[global experts] (global id ->
+    local id or -1)."""
     X = formats.bf16_to_f64(x_bits)
     T, H = X.shape
     ids = np.asarray(topk_ids)
     topk = ids.shape[1]
     E = w13.shape[0]
     w = np.asarray(topk_w, dtype=np.float32).astype(np.float64)
-    counts, offsets, sorted_pair, _ = route(ids, E)
+    counts, offsets, sorted_pair, _ = route(ids, E, expert_map)
     y = np.zeros((T * topk, H), dtype=np.float64)
     for e in range(E):
         pairs = sorted_pair[offsets[e]:offsets[e + 1]]
@@ -108,14 +111,14 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4",
 
 
 def moe_forward_sampled(x_bits, topk_ids, topk_w, w13, s13, w2, s2, tokens, cols,
-                        kind: str = "mxfp4") -> np.ndarray:
+                        kind: str = "mxfp4", expert_map=None) -> np.ndarray:
     """out[tokens][:, cols] only, float64[len(tokens), len(cols)].
 
     Each selected token's pairs need their full stage-1 output, but only the
     selected rows of W2; used to check full-size problems element by element.
     """
     X = formats.bf16_to_f64(x_bits)
-    ids = np.asarray(topk_ids)
+    ids = local_ids(topk_ids, expert_map)
     topk = ids.shape[1]
     E = w13.shape[0]
     I = w13.shape[1] // 2

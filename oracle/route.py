@@ -7,6 +7,13 @@ pages give no algorithm for this step; the reading used here is a stable
 counting sort of the flat pair index p = t*topk + k by expert id.  Ids outside
 [0, E) (the ``expert_map`` -1 convention for non-local experts) join no group.
 Duplicate ids in one row are separate pairs.
+
+Expert parallelism (``apply`` passes ``global_num_experts`` and
+``expert_map``): with a map, the ids in ``topk_ids`` are global expert ids in
+[0, global_num_experts); ``expert_map[g]`` is the local id of global expert g
+on this GPU, or -1 when another GPU holds it.  The pages print no formula for
+the lookup; the plain reading is used: a global id outside the map, or one the
+map sends to -1, joins no group, exactly like an invalid local id.
 """
 
 from __future__ import annotations
@@ -14,7 +21,21 @@ from __future__ import annotations
 import numpy as np
 
 
-def route(topk_ids: np.ndarray, E: int):
+def local_ids(topk_ids: np.ndarray, expert_map=None) -> np.ndarray:
+    """Global expert ids -> local ids through ``expert_map`` (int64 array; -1
+    for non-local or out-of-range ids).  Without a map the ids are returned as
+    they are (already local)."""
+    ids = np.asarray(topk_ids).astype(np.int64)
+    if expert_map is None:
+        return ids
+    emap = np.asarray(expert_map).astype(np.int64)
+    inside = (ids >= 0) & (ids < emap.size)
+    out = np.full(ids.shape, -1, dtype=np.int64)
+    out[inside] = emap[ids[inside]]
+    return out
+
+
+def route(topk_ids: np.ndarray, E: int, expert_map=None):
     """Group pairs by expert.
 
     Returns ``(counts int32[E], offsets int32[E+1], sorted_pair int32[P],
@@ -22,7 +43,7 @@ def route(topk_ids: np.ndarray, E: int):
     e's pairs in ascending flat index; entries past ``offsets[E]`` are -1.
     ``pair_pos[p]`` is the position of pair p in ``sorted_pair`` (-1 if invalid).
     """
-    ids = np.asarray(topk_ids).reshape(-1).astype(np.int64)
+    ids = local_ids(topk_ids, expert_map).reshape(-1)
     P = ids.size
     valid = (ids >= 0) & (ids < E)
     counts = np.bincount(ids[valid], minlength=E).astype(np.int32)

@@ -165,6 +165,21 @@ def test_route_matches_bruteforce_with_invalid_and_duplicate_ids(T, topk, E):
     assert list(c) == bc and list(o) == bo and list(sp) == bsp and list(pos) == bpos
 
 
+@pytest.mark.parametrize("G,E", [(16, 8), (9, 3)])
+def test_route_with_expert_map_matches_bruteforce(G, E):
+    # global ids (some out of range) through a map that sends some experts to
+    # other GPUs (-1): the brute force maps each id by hand, then groups
+    g = np.random.default_rng(G * 10 + E)
+    ids = g.integers(-2, G + 2, size=(11, 4)).astype(np.int32)
+    emap = np.full(G, -1, np.int32)
+    owned = g.choice(G, E, replace=False)
+    emap[owned] = g.permutation(E)
+    local = [[int(emap[i]) if 0 <= i < G else -1 for i in row] for row in ids]
+    c, o, sp, pos = route.route(ids, E, expert_map=emap)
+    bc, bo, bsp, bpos = _route_bruteforce(np.array(local, np.int32), E)
+    assert list(c) == bc and list(o) == bo and list(sp) == bsp and list(pos) == bpos
+
+
 def test_route_empty():
     c, o, sp, pos = route.route(np.zeros((0, 4), np.int32), 8)
     assert c.sum() == 0 and o[-1] == 0 and sp.size == 0 and pos.size == 0
@@ -316,6 +331,27 @@ def test_moe_bias_closed_form_with_zero_weights():
     assert np.array_equal(got_1, want_1)
     # without biases the same weights give zero
     assert np.all(moe.moe_forward(x, ids, w, z13, s13, z2, s2) == 0)
+
+
+def test_moe_expert_map_partition_sums_to_the_whole_layer():
+    # expert parallelism: 8 global experts split over two GPUs by parity (local
+    # id = global // 2); each GPU maps the ids it does not hold to -1, and the
+    # two partial outputs add up to the layer computed with every expert local
+    x, ids, w, w13, s13, w2, s2 = _tiny_problem(31, T=7, topk=3)
+    G = w13.shape[0]
+    whole = moe.moe_forward(x, ids, w, w13, s13, w2, s2)
+    parts = []
+    for r in range(2):
+        held = np.arange(r, G, 2)
+        emap = np.full(G, -1, np.int32)
+        emap[held] = np.arange(held.size)
+        parts.append(moe.moe_forward(x, ids, w, w13[held], s13[held], w2[held], s2[held], expert_map=emap))
+    assert np.allclose(parts[0] + parts[1], whole, rtol=1e-12, atol=1e-14)
+    # a map that holds nothing gives zero; the identity map changes nothing
+    none = np.full(G, -1, np.int32)
+    assert np.all(moe.moe_forward(x, ids, w, w13, s13, w2, s2, expert_map=none) == 0)
+    ident = np.arange(G, dtype=np.int32)
+    assert np.array_equal(moe.moe_forward(x, ids, w, w13, s13, w2, s2, expert_map=ident), whole)
 
 
 def test_moe_sampled_matches_full():
