@@ -13,8 +13,10 @@ int4_per_group_32 requantiser over all 112 experts, the int4 MoE at T = 1, 7,
 32, and the tensor-core prefill path at T = 4096 when built.  ``e2e`` is the
 headline measured through the Python binding of the C ABI with inputs copied
 from pinned host memory and the output copied back every step.  ``roofline``
-is the gate_up GEMM kernel against measured HBM bandwidth.  ``cpu_baseline``
-is the CPU oracle on a bounded sample, extrapolated.
+is the dominant decode kernel (both GEMMs of a T=1 call) against measured HBM
+bandwidth, its duration taken with CUDA events in a separate 8-step graph (the
+timed graph carries no events).  ``cpu_baseline`` is the CPU oracle on a
+bounded sample, extrapolated.
 
 --impl reference times the CPU oracle alone on the same workload.
 Multi-GPU (torchrun): independent replicas, one per GPU (the layer has no
@@ -24,10 +26,6 @@ cross-GPU step at this shape); ``value`` is the aggregate time per call.
 from __future__ import annotations
 
 import os
-
-# the CPU oracle runs single-threaded: pin every BLAS pool before numpy loads
-for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-    os.environ.setdefault(_v, "1")
 
 import argparse  # noqa: E402
 import ctypes  # noqa: E402
@@ -164,30 +162,43 @@ def committed_traffic():
 # ----------------------------------------------------------------------------- CPU oracle
 
 
-def oracle_sample_us_per_call(x, ids, w, w13, s13, w2, s2, n_pairs: int, part: int = 1):
-    """Oracle time for ``n_pairs`` of the token's (token, expert) pairs, each on
-    1/``part`` of the expert's weights (the first I/part gate and up rows and the
-    matching H/part x I/part block of w2), extrapolated by weight count to a
-    whole T=1 call (all topk pairs, all weights)."""
-    from oracle import formats, moe
+def blas_threads():
+    """Threads of numpy's BLAS pool (None when threadpoolctl is not installed)."""
+    try:
+        from threadpoolctl import threadpool_info
+    except ImportError:
+        return None
+    n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+    return max(n) if n else None
 
-    X = formats.bf16_to_f64(x)[0]
-    I, H = SHAPE.I, SHAPE.H
-    i_n, h_n = I // part, H // part
+
+def oracle_sample(x, ids, w, weights, n_pairs: int):
+    """Time the oracle's ``moe_forward`` on one T=1 call restricted to its first
+    ``n_pairs`` (token, expert) pairs (the other ids set to -1, which the layer
+    skips).  Returns (seconds measured, microseconds extrapolated to all of the
+    call's pairs by pair count: every pair dequantises and multiplies one whole
+    expert)."""
+    from oracle import moe
+
+    w13, s13, w2, s2 = weights
+    sub = np.array(ids, copy=True)
+    sub[:, n_pairs:] = -1
     t0 = time.perf_counter()
-    acc = np.zeros(h_n)
-    for k in range(n_pairs):
-        e = int(ids[0, k])
-        rows = np.r_[0:i_n, I:I + i_n]
-        W13 = formats.dequant_mxfp4(w13[e][rows], s13[e][rows])
-        W2 = formats.dequant_mxfp4(w2[e][:h_n, :i_n // 2], s2[e][:h_n, :i_n // 32])
-        h = W13 @ X
-        a = moe.silu(h[:i_n]) * h[i_n:]
-        acc += float(w[0, k]) * (W2 @ a)
+    moe.moe_forward(x, sub, w, w13, s13, w2, s2)
     dt = time.perf_counter() - t0
-    done = n_pairs * (2 * i_n * H + h_n * i_n)
-    total = ids.shape[1] * (2 * I * H + H * I)
-    return dt * total / done * 1e6
+    n_valid = int(((ids >= 0) & (ids < w13.shape[0])).sum())
+    return dt, dt * 1e6 * n_valid / n_pairs
+
+
+def cpu_baseline_entry(us_per_call, n_pairs):
+    cores = os.cpu_count()
+    bt = blas_threads()
+    return {"value": round(us_per_call, 1), "unit": UNIT, "cores": bt if bt else cores, "kind": "oracle",
+            "host_cpu_count": cores, "blas_threads": bt,
+            "sample": (f"{n_pairs} of the {SHAPE.topk} (token, expert) pairs of one T=1 call (the other ids set to "
+                       f"-1) through the float64 numpy oracle's moe_forward (whole experts: dequantise, GEMV, SiLU "
+                       f"gate, GEMV, weighted sum), extrapolated by pair count to the whole call; BLAS on the host's "
+                       f"default thread pool, dequantisation single-threaded numpy")}
 
 
 def host_weights(seed: int = 100):
@@ -204,31 +215,34 @@ def host_batch(seed: int, T: int, bias_std=None):
     return x, ids, w
 
 
+REF_PAIRS = 1  # pairs of the 15 per reference-arm step (about half a second of oracle work each)
+
+
 def run_reference(args, rank: int):
     if rank != 0:
         return
-    w13, s13, w2, s2 = host_weights()
+    weights = host_weights()
     batches = [host_batch(1000 + i, 1) for i in range(ROTATE)]
-    n_pairs, part = 1, 8
     for i in range(args.warmup):
         x, ids, w = batches[i % ROTATE]
-        oracle_sample_us_per_call(x, ids, w, w13, s13, w2, s2, n_pairs, part)
-    vals = []
+        oracle_sample(x, ids, w, weights, REF_PAIRS)
+    secs, vals = [], []
     t0 = time.perf_counter()
     for i in range(args.steps):
         x, ids, w = batches[i % ROTATE]
-        vals.append(oracle_sample_us_per_call(x, ids, w, w13, s13, w2, s2, n_pairs, part))
+        s, v = oracle_sample(x, ids, w, weights, REF_PAIRS)
+        secs.append(s)
+        vals.append(v)
     wall = time.perf_counter() - t0
     v = statistics.mean(vals)
-    sample = (f"each step: 1/{part} of the weights of {n_pairs} of the {SHAPE.topk} (token, expert) pairs of one "
-              f"T=1 call through the float64 numpy oracle (dequantise, GEMV, SiLU gate, GEMV), single thread, "
-              f"extrapolated by weight count to the whole call")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1000, 3),
+        "steps": args.steps, "warmup": args.warmup,
+        # the time each step actually took (a sample of one call), not the extrapolated call
+        "ms_per_step": round(1000.0 * statistics.mean(secs), 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(),
-        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": cpu_baseline_entry(v, REF_PAIRS),
         "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 2),
     }
@@ -312,14 +326,11 @@ def run_ours(args, rank: int, world: int):
         with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
             for i in range(n_steps):
                 x, ids, w, ids_h = batches[i % ROTATE]
-                # per-kernel events on timing_steps steps spread evenly over the
-                # graph; an event between two kernels stops the programmatic
-                # overlap of that step, so only a few steps carry them
-                j = -1
-                if timing_steps and i % (n_steps // timing_steps) == 0 and i // (n_steps // timing_steps) < timing_steps:
-                    j = i // (n_steps // timing_steps)
-                if j >= 0:
-                    evs = pre[j]
+                # per-kernel events on the first timing_steps steps (only in the
+                # graphs built for them: an event between two kernels stops
+                # their programmatic overlap)
+                if i < timing_steps:
+                    evs = pre[i]
                     arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in evs])
                     _native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 4))
                     ev.append((evs, distinct(ids_h)))
@@ -342,10 +353,13 @@ def run_ours(args, rank: int, world: int):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    # ---- headline: K steps in one graph, per-kernel events on 8 of them
+    # ---- headline: K steps in one graph that carries no timing events (an
+    # event between two kernels stops their programmatic overlap); the
+    # per-kernel durations come from a separate 8-step graph with events on
+    # every step, replayed after the timed region
     K, W = args.steps, args.warmup
-    timing = min(K, 8)
-    g_main, kev, bytes_main, (d1, ws1) = capture(1, K, timing_steps=timing)
+    g_main, _, bytes_main, (d1, ws1) = capture(1, K)
+    g_ev, kev, _, _ = capture(1, 8, timing_steps=8, seed0=3000)
     g_warm, _, _, _ = capture(1, max(W, 1))
     for _ in range(max(W, 3)):
         time_graph(g_warm)
@@ -363,7 +377,9 @@ def run_ours(args, rank: int, world: int):
     status = m.moe_read_status(d1, ws1)
     ms = max_over_ranks(ms, world, dev)
     us_per_call = ms * 1000.0 / (K * world)
-    # per-kernel durations from the last ``timing`` steps of the timed replay
+    # per-kernel durations: the event graph, replayed twice, read after the second
+    time_graph(g_ev)
+    time_graph(g_ev)
     fused = fused_decode(SHAPE.H, SHAPE.I)
     names = ["route", "gemm_fused_gate_up_down" if fused else "gemm1_gate_up", None if fused else "gemm2_down",
              "combine"]
@@ -424,12 +440,9 @@ def run_ours(args, rank: int, world: int):
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        x, ids, w = host_batch(1000, 1)
         n = 2
-        v = oracle_sample_us_per_call(x, ids, w, w13_h, s13_h, w2_h, s2_h, n)
-        cpu = {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} of the {SHAPE.topk} (token, expert) pairs of one T=1 call (full H outputs), "
-                         f"float64 numpy, single thread, extrapolated to the whole call"}
+        vals = [oracle_sample(*host_batch(1000 + i, 1), (w13_h, s13_h, w2_h, s2_h), n)[1] for i in range(2)]
+        cpu = cpu_baseline_entry(statistics.mean(vals), n)
 
     if rank != 0:
         return
@@ -469,15 +482,15 @@ def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="m
     flops = 2.0 * T * SHAPE.topk * 3 * SHAPE.H * SHAPE.I
     ms_list = []
     s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    kev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(12)]
     for ev in kev:
         ev.record()
     lib = m._native.load()
     for i in range(6):
         x, ids, w, _ = pb[i % 2]
         if i == 5:  # per-kernel times of the last call
-            arr = (ctypes.c_void_p * 10)(*[ev.cuda_event for ev in kev])
-            m._native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 5))
+            arr = (ctypes.c_void_p * 12)(*[ev.cuda_event for ev in kev])
+            m._native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 6))
         s_ev.record()
         fn = m.moe_a16w4_mxfp4 if kind == "mxfp4" else m.moe_a16w4_int4g32
         fn(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws, path=m.MOE_PATH_PREFILL)
@@ -487,7 +500,7 @@ def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="m
             ms_list.append(s_ev.elapsed_time(e_ev))
     ms = statistics.median(ms_list)
     tf = flops / (ms * 1e-3) / 1e12
-    names = ["route", "gather", "gemm1_gate_up_tc", "gemm2_down_tc", "cast"]
+    names = ["route", "gather", "gemm1_gate_up_tc", "convert_f16", "gemm2_down_tc", "cast"]
     kms = {n: round(kev[2 * q].elapsed_time(kev[2 * q + 1]), 3) for q, n in enumerate(names)}
     rows[f"{'mxfp4' if kind == 'mxfp4' else 'int4g32'}_prefill_T{T}_skewed"] = {
         "ms_per_call": round(ms, 3), "TFLOPs_useful": round(tf, 1), "kernels_ms": kms,

@@ -73,13 +73,16 @@ typedef struct moe_dims {
 } moe_dims_t;
 
 /* Bytes of scratch that moe_a16w4_mxfp4 / moe_a16w4_int4g32 need for ``d``
- * (0 if ``d`` is invalid).  The caller allocates it (256-byte aligned) and may
- * reuse it across calls that are ordered on one stream; calls that can run
- * concurrently need separate workspaces.  The outputs do not depend on what the
- * workspace held before: the words the kernels synchronise through carry a
- * per-call value that leftovers do not match.  Only the status word (its
- * first 4 bytes) reads back what the memory held until it is first cleared:
- * zero those bytes, or call moe_read_status once, after allocating. */
+ * (0 if ``d`` is invalid).  Source: vLLM PR #51274, Validation -- the layer
+ * runs under full and piecewise CUDA graph capture, so a call may not
+ * allocate; the caller allocates this scratch once (256-byte aligned) and
+ * passes it to every call.  It may be reused across calls that are ordered on
+ * one stream; calls that can run concurrently need separate workspaces.  The
+ * outputs do not depend on what the workspace held before: the words the
+ * kernels synchronise through carry a per-call value that leftovers do not
+ * match.  Only the status word (its first 4 bytes) reads back what the memory
+ * held until it is first cleared: zero those bytes, or call moe_read_status
+ * once, after allocating. */
 size_t moe_workspace_bytes(const moe_dims_t* d);
 
 /*
@@ -103,18 +106,64 @@ int moe_a16w4_mxfp4(const moe_dims_t* d, const void* x, const int32_t* topk_ids,
                     void* stream);
 
 /*
- * Same layer on int4_per_group_32 weights (the requantiser's output format):
+ * Same layer on int4_per_group_32 weights (the requantiser's output format).
+ * Source: vLLM PR #51274, Summary -- the opt-in int4_per_group_32 MoE path
+ * serves the requantised experts through a BF16 x packed-int4 kernel; the
+ * Mxfp4MoEMethod page's _setup_kernel_k3_situ_gfx942 hands that kernel the
+ * converted w13/w2 and their per-32-group scales in place of the MXFP4 ones.
  *   w13_q  uint8 [E, 2I, H/2]  two's-complement int4, element 2j low    16-byte aligned
  *   w13_s  float32 [E, 2I, H/32] one scale per 32-group                  16-byte aligned
  *   w2_q   uint8 [E, H, I/2],  w2_s float32 [E, H, I/32]                 16-byte aligned
  * Weight value = q * s.  The weight-streaming kernels apply s to each group's
  * partial sum in fp32; the tensor-core kernels (large batches, same rules as
- * moe_a16w4_mxfp4 for ``d->path``) multiply with bf16(fl32(q * s)).
+ * moe_a16w4_mxfp4 for ``d->path``) multiply with bf16(fl32(q * s)) in the
+ * gate_up GEMM and f16(q * f16(s * 2^ew)) in the down GEMM (ew a power of
+ * two per weight row that puts the row's largest weight just below 2^15).
  */
 int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_ids,
                       const float* topk_w, const uint8_t* w13_q, const float* w13_s,
                       const uint8_t* w2_q, const float* w2_s, void* out, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/*
+ * Optional inputs of the layer call.  Source: the Mxfp4MoEMethod page --
+ * ``create_weights`` registers ``w13_bias`` bf16 [E, 2I] and ``w2_bias``
+ * bf16 [E, H] when the layer has biases and ``get_fused_moe_quant_config``
+ * hands them to the kernel (``w1_bias``, ``w2_bias``); ``apply`` passes
+ * ``global_num_experts``, ``expert_map`` and ``apply_router_weight_on_input``.
+ * The pages print no formula for any of them; the readings used:
+ *   w13_bias               added to the gate_up GEMM's outputs before the
+ *                          activation: h = W13[e] x + b13[e]
+ *   w2_bias                added to each expert's output: y = W2[e] a + b2[e]
+ *   router_weight_on_input each pair's input is scaled by its router weight
+ *                          (h = W13[e] (w x) + b13[e]) and the combine sums the
+ *                          pairs' outputs unweighted
+ *   expert_map             topk_ids hold global expert ids in
+ *                          [0, global_num_experts); expert_map[g] is the local
+ *                          id (0..E-1) of global expert g, or -1 if another GPU
+ *                          holds it; ids outside the map or mapped to -1
+ *                          contribute nothing
+ * A zero-initialised struct (all NULL / 0) is the plain layer.
+ */
+typedef struct moe_options {
+  const void* w13_bias;            /* bf16 [E, 2I] or NULL (2-byte aligned) */
+  const void* w2_bias;             /* bf16 [E, H] or NULL (2-byte aligned)  */
+  const int32_t* expert_map;       /* int32 [global_num_experts] or NULL    */
+  int32_t global_num_experts;      /* 1 .. 2^20 when expert_map is set      */
+  int32_t router_weight_on_input;  /* 0 or 1                                */
+} moe_options_t;
+
+/* moe_a16w4_mxfp4 / moe_a16w4_int4g32 with optional inputs (``opt`` may be
+ * NULL: the plain call).  Returns MOE_ERR_BAD_DIMS for global_num_experts
+ * outside [1, 2^20] with a map, or router_weight_on_input not 0 or 1. */
+int moe_a16w4_mxfp4_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                       const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
+                       const uint8_t* w2_scale, const moe_options_t* opt, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream);
+int moe_a16w4_int4g32_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                         const uint8_t* w13_q, const float* w13_s, const uint8_t* w2_q, const float* w2_s,
+                         const moe_options_t* opt, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /*
  * Load-time, lossy MXFP4 -> int4_per_group_32 requantisation
@@ -128,14 +177,20 @@ int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_id
  *   out_s  float32 [E, N, K/32]                              16-byte aligned
  * Experts are converted ``experts_per_chunk`` at a time (one launch per
  * chunk; 8 on the pages); the result does not depend on the chunk size.
- * Source and destination must not overlap.  Scale bytes of 255 (NaN) are
- * outside the contract.  K multiple of 32, N >= 1, E >= 1.
+ * Source and destination must not overlap.  Results are bit-exact for scale
+ * bytes 0..252; bytes 253 and 254 are outside the contract (E2M1 codes 4 and 6
+ * times 2^126 or 2^127 overflow float32) and so is 255 (NaN).  K multiple of
+ * 32, N >= 1, E >= 1.
  */
 int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale,
                              uint8_t* out_q, float* out_s, int32_t experts_per_chunk, void* stream);
 
 /*
- * The grouping step alone (stable counting sort of the T*topk pairs by expert):
+ * The grouping step alone.  Source: the Mxfp4MoEMethod page, ``apply`` -- the
+ * fused-MoE kernel receives topk_ids and topk_weights [T, topk] (ids of
+ * non-local experts arrive as -1 through ``expert_map``) and must bring each
+ * expert's (token, slot) pairs together before its grouped GEMMs.  The pages
+ * give no order; this is a stable counting sort of the T*topk pairs by expert:
  *   counts      int32 [E]     pairs per expert
  *   offsets     int32 [E+1]   exclusive prefix sum of counts
  *   sorted_pair int32 [T*topk] flat pair index t*topk+k, ascending within each
@@ -146,14 +201,53 @@ int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, 
 int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
               int32_t* sorted_pair, int32_t* pair_pos, void* stream);
 
+/*
+ * Top-k routing from router logits.  Source: the Mxfp4MoEMethod page,
+ * ``apply_monolithic`` -- the kernel receives ``router_logits`` instead of
+ * top-k ids and weights and chooses the experts itself; the pages print no
+ * scoring formula.  The plain reading implemented: p = softmax over each
+ * token's logits; the ``topk`` largest p are kept (in decreasing order, ties
+ * to the lower expert id); with ``renormalize`` the kept p are divided by
+ * their sum.  Grouped top-k, a score-correction bias and a routed scaling
+ * factor (named on the page) are not modelled.
+ *   logits    float32 [T, G], G = experts seen by the router (global ids when
+ *             the layer then maps them through moe_options_t.expert_map)
+ *   topk_ids  int32 [T, topk]   (bit-exact: selection by logit, which orders
+ *             the experts exactly as their probabilities do)
+ *   topk_w    float32 [T, topk] (float32 exp and one IEEE division each)
+ * 1 <= G <= 1024, 1 <= topk <= min(64, G), renormalize 0 or 1.  NaN logits
+ * are outside the contract.
+ */
+int moe_router_topk(const float* logits, int32_t T, int32_t G, int32_t topk, int32_t renormalize,
+                    int32_t* topk_ids, float* topk_w, void* stream);
+
 /* Copy the device status word of ``workspace`` (MOE_STATUS_* bits, 0 = clean)
  * into *status and clear it, together with the words the decode kernels
  * synchronise through (after a wait that gave up, those may be inconsistent;
- * read the status before reusing such a workspace).  Synchronises ``stream``. */
+ * read the status before reusing such a workspace).  Synchronises ``stream``.
+ * The pages have no counterpart: their kernels do not wait on one another.
+ * The fail-closed principle of the Mxfp4MoEMethod page (an unsupported
+ * activation is an error, never a silent substitute) is why a wait that ran
+ * out is reported here rather than left as silently wrong output. */
 int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream);
 
 /*
- * Allocation-free variant of moe_a16w4_mxfp4.  The pages have no counterpart:
+ * Bounded-wait hook for the next moe_a16w4_mxfp4 / moe_a16w4_int4g32 call made
+ * from this host thread (then cleared).  The pages have no counterpart.
+ *   limit_ns       limit of every wait inside that call's kernels, instead of
+ *                  the default 2 s; a wait that runs out sets
+ *                  MOE_STATUS_WAIT_TIMEOUT, the kernels stop and return, and the
+ *                  call's output is invalid (> 0)
+ *   extra_waiters  for tests of the give-up path: the fused decode kernel's
+ *                  wait for all of its CTAs' gate_up results expects this many
+ *                  CTAs more than it launched, so that wait runs out after
+ *                  limit_ns (0..64; 0 for normal use)
+ * Returns MOE_ERR_BAD_DIMS for limit_ns = 0 or extra_waiters outside [0, 64].
+ */
+int moe_set_wait_limit(uint64_t limit_ns, int32_t extra_waiters);
+
+/*
+ * Allocation-free variant of moe_a16w4_mxfp4.  The paper has no counterpart:
  * this entry point exists for callers that cannot allocate device memory when
  * they run the layer (a serving thread that must not call cudaMalloc or a
  * framework allocator, a plugin that is handed only input and output pointers,
@@ -170,15 +264,25 @@ int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (once per device, with that device current); make
  *     that first call before any stream capture.
- *   - All calls share the one array, which keeps the previous call's contents;
- *     every region is written before it is read within a call, so nothing needs
- *     clearing.  Calls that may overlap on the GPU (different streams, or
- *     different host threads on one device) race on the array: order them.
- *   - Device status bits of this variant are not exposed.
+ *   - All calls share the one array, which keeps the previous call's contents.
+ *     Its data regions are written before they are read within a call; its
+ *     synchronisation words carry a per-call value that leftovers do not
+ *     match, and the one kernel that synchronises through them is launched so
+ *     that all of its CTAs run at once.  Calls that may overlap on the GPU
+ *     (different streams, or different host threads on one device) race on the
+ *     array: order them.
+ *   - A bounded wait that ran out (MOE_STATUS_WAIT_TIMEOUT) is recorded in the
+ *     array's status word: read and clear it with moe_noalloc_read_status.
  */
 int moe_a16w4_mxfp4_noalloc(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
                             const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
                             const uint8_t* w2_scale, void* out, void* stream);
+
+/* Status word of the current device's allocation-free scratch array (as
+ * moe_read_status does for a workspace): copies it to *status and clears it
+ * and the array's synchronisation words.  Synchronises ``stream``; allocates
+ * nothing.  The paper has no counterpart. */
+int moe_noalloc_read_status(uint32_t* status, void* stream);
 
 /*
  * Optional per-kernel timing, for benchmarks.  ``events`` holds 2*n
@@ -189,7 +293,8 @@ int moe_a16w4_mxfp4_noalloc(const moe_dims_t* d, const void* x, const int32_t* t
  * weight-streaming path 0 grouping, 1 gate_up GEMM, 2 down GEMM, 3 combine,
  * where H and I are at most 3584 one launch runs both GEMMs (index 1) and
  * the index-2 events are recorded back to back; tensor-core path 0 grouping,
- * 1 row gather, 2 gate_up GEMM, 3 down GEMM, 4 combine.  Slots without a
+ * 1 row gather, 2 gate_up GEMM, 3 f16 conversion of the intermediate, 4 down
+ * GEMM (with the weighted combine), 5 bf16 cast of the output.  Slots without a
  * launch (grouping of at most 128 pairs, done inside the decode kernels) are
  * recorded back to back too.  n = 0 clears the hook.  Returns
  * MOE_ERR_BAD_DIMS for n outside [0, 8] and MOE_ERR_NULL for a NULL

@@ -15,11 +15,11 @@ import torch
 
 from . import _native
 from ._native import (MOE_ACT_SWIGLU, MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL,  # noqa: F401
-                      MOE_STATUS_WAIT_TIMEOUT, MoeDims, MoeError)
+                      MOE_STATUS_WAIT_TIMEOUT, MoeDims, MoeError, MoeOptions)
 
 __all__ = [
     "moe_workspace_bytes", "moe_a16w4_mxfp4", "moe_a16w4_int4g32", "requant_mxfp4_to_int4g32",
-    "moe_route", "moe_read_status", "dims", "MoeError",
+    "moe_route", "moe_router_topk", "moe_read_status", "dims", "MoeError",
 ]
 
 
@@ -64,7 +64,24 @@ def _workspace(d: MoeDims, workspace, device):
     return workspace
 
 
-def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, stream, scale_dtype):
+def _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input):
+    """The optional inputs as a MoeOptions struct, or None when none is set."""
+    if w13_bias is None and w2_bias is None and expert_map is None and not router_weight_on_input:
+        return None
+    if w13_bias is not None:
+        _need(w13_bias, "w13_bias", torch.bfloat16, (E, 2 * I))
+    if w2_bias is not None:
+        _need(w2_bias, "w2_bias", torch.bfloat16, (E, H))
+    G = 0
+    if expert_map is not None:
+        G = expert_map.shape[0]
+        _need(expert_map, "expert_map", torch.int32, (G,))
+    return MoeOptions(_ptr(w13_bias).value, _ptr(w2_bias).value, _ptr(expert_map).value, G,
+                      1 if router_weight_on_input else 0)
+
+
+def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, stream, scale_dtype,
+         w13_bias=None, w2_bias=None, expert_map=None, router_weight_on_input=False):
     T, H = x.shape
     E, two_i, _ = w13.shape
     I = two_i // 2
@@ -81,24 +98,39 @@ def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, s
     _need(out, "out", torch.bfloat16, (T, H))
     d = dims(E, H, I, topk, T, path)
     workspace = _workspace(d, workspace, x.device)
-    rc = getattr(_lib(), fn_name)(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13),
-                                  _ptr(w2), _ptr(s2), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    opt = _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input)
+    if opt is None:
+        rc = getattr(_lib(), fn_name)(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13),
+                                      _ptr(w2), _ptr(s2), _ptr(out), _ptr(workspace), workspace.numel(),
+                                      _stream(stream))
+    else:
+        fn_name += "_ex"
+        rc = getattr(_lib(), fn_name)(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13),
+                                      _ptr(w2), _ptr(s2), ctypes.byref(opt), _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream(stream))
     _native.check(fn_name, rc)
     return out
 
 
 def moe_a16w4_mxfp4(x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out=None, workspace=None,
-                    path: int = MOE_PATH_AUTO, stream=None):
-    """Fused MoE on MXFP4 weights (uint8 packed E2M1 + uint8 E8M0 scales)."""
+                    path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
+                    router_weight_on_input: bool = False):
+    """Fused MoE on MXFP4 weights (uint8 packed E2M1 + uint8 E8M0 scales).
+
+    Optional: ``w13_bias`` bf16 [E, 2I], ``w2_bias`` bf16 [E, H], ``expert_map``
+    int32 [global experts] (topk_ids then hold global ids), and
+    ``router_weight_on_input``; any of them selects ``moe_a16w4_mxfp4_ex``."""
     return _moe("moe_a16w4_mxfp4", x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, workspace, path,
-                stream, torch.uint8)
+                stream, torch.uint8, w13_bias, w2_bias, expert_map, router_weight_on_input)
 
 
 def moe_a16w4_int4g32(x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out=None, workspace=None,
-                      path: int = MOE_PATH_AUTO, stream=None):
-    """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 scales)."""
+                      path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
+                      router_weight_on_input: bool = False):
+    """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 scales); options as
+    ``moe_a16w4_mxfp4``."""
     return _moe("moe_a16w4_int4g32", x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out, workspace, path,
-                stream, torch.float32)
+                stream, torch.float32, w13_bias, w2_bias, expert_map, router_weight_on_input)
 
 
 def requant_mxfp4_to_int4g32(w, scale, out_q=None, out_s=None, experts_per_chunk: int = 8, stream=None):
@@ -133,6 +165,18 @@ def moe_route(topk_ids, E: int, stream=None):
                           _stream(stream))
     _native.check("moe_route", rc)
     return counts, offsets, sp, pos
+
+
+def moe_router_topk(logits, topk: int, renormalize: bool = True, stream=None):
+    """Top-k routing from float32 router logits [T, G]: ``(ids int32 [T, topk], weights float32 [T, topk])``."""
+    T, G = logits.shape
+    _need(logits, "logits", torch.float32, (T, G))
+    ids = torch.empty((T, topk), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, topk), dtype=torch.float32, device=logits.device)
+    rc = _lib().moe_router_topk(_ptr(logits), T, G, topk, 1 if renormalize else 0, _ptr(ids), _ptr(w),
+                                _stream(stream))
+    _native.check("moe_router_topk", rc)
+    return ids, w
 
 
 def moe_read_status(d: MoeDims, workspace, stream=None) -> int:

@@ -32,14 +32,29 @@ class MoeDims(ctypes.Structure):
 
 _DimsP = ctypes.POINTER(MoeDims)
 
+
+class MoeOptions(ctypes.Structure):
+    _fields_ = [("w13_bias", _vp), ("w2_bias", _vp), ("expert_map", _vp), ("global_num_experts", _i32),
+                ("router_weight_on_input", _i32)]
+
+
+_OptP = ctypes.POINTER(MoeOptions)
+
 SIGNATURES = {
     "moe_workspace_bytes": (ctypes.c_size_t, [_DimsP]),
     "moe_a16w4_mxfp4": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "moe_a16w4_int4g32": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "moe_a16w4_mxfp4_ex": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _OptP, _vp, _vp,
+                                          ctypes.c_size_t, _vp]),
+    "moe_a16w4_int4g32_ex": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _OptP, _vp, _vp,
+                                            ctypes.c_size_t, _vp]),
     "requant_mxfp4_to_int4g32": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
     "moe_route": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_router_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_read_status": (ctypes.c_int, [_DimsP, _vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "moe_set_wait_limit": (ctypes.c_int, [ctypes.c_uint64, _i32]),
     "moe_a16w4_mxfp4_noalloc": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_noalloc_read_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _vp]),
     "moe_set_timing_events": (ctypes.c_int, [ctypes.POINTER(_vp), _i32]),
     "moe_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_abi_version": (ctypes.c_int, []),

@@ -12,6 +12,7 @@ struct TimingHook {
   int n = 0;
 };
 thread_local TimingHook g_timing;
+thread_local WaitSettings g_wait;
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -61,10 +62,29 @@ int common_checks(const moe_dims_t* d, const void* x, const int32_t* ids, const 
   return MOE_OK;
 }
 
+// Options of a call from the public struct (NULL = none), checked.
+int read_options(const moe_options_t* o, LayerOptions* lo) {
+  *lo = LayerOptions{};
+  if (!o) return MOE_OK;
+  if (o->router_weight_on_input != 0 && o->router_weight_on_input != 1) return MOE_ERR_BAD_DIMS;
+  if (o->expert_map && (o->global_num_experts < 1 || o->global_num_experts > (1 << 20))) return MOE_ERR_BAD_DIMS;
+  if (!aligned(o->w13_bias, 2) || !aligned(o->w2_bias, 2) || !aligned(o->expert_map, 4)) return MOE_ERR_ALIGN;
+  lo->b13 = reinterpret_cast<const uint16_t*>(o->w13_bias);
+  lo->b2 = reinterpret_cast<const uint16_t*>(o->w2_bias);
+  lo->emap = o->expert_map;
+  lo->G = o->expert_map ? o->global_num_experts : 0;
+  lo->rwi = o->router_weight_on_input;
+  return MOE_OK;
+}
+
 int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float* tw, const uint8_t* w13,
-            const void* s13, const uint8_t* w2, const void* s2, void* out, void* workspace, size_t ws_bytes,
-            void* stream, WeightKind kind) {
+            const void* s13, const uint8_t* w2, const void* s2, const moe_options_t* options, void* out,
+            void* workspace, size_t ws_bytes, void* stream, WeightKind kind) {
+  const WaitSettings wait = take_wait_settings();  // the hook applies to this call only
   int rc = common_checks(d, x, ids, tw, w13, s13, w2, s2, out, workspace, ws_bytes, kind);
+  if (rc != MOE_OK) return rc;
+  LayerOptions opt;
+  rc = read_options(options, &opt);
   if (rc != MOE_OK || d->T == 0) return rc;
   int sms = 0;
   rc = check_device(&sms);
@@ -78,7 +98,7 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
   // small decode batches are grouped inside the decode kernels
   const bool route_kernel = L.prefill || (long long)d->T * d->topk > kMaxLocalRoutePairs;
   timing_mark(0, false, s);
-  if (route_kernel && launch_route(ids, d->E, d->T, d->topk, r, L.prefill ? 1 : 0, s) != cudaSuccess)
+  if (route_kernel && launch_route(ids, d->E, d->T, d->topk, opt.emap, opt.G, r, L.prefill ? 1 : 0, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   timing_mark(0, true, s);
   cudaError_t e;
@@ -90,9 +110,14 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
     a.w13 = w13; a.w13_s = s13;
     a.w2 = w2; a.w2_s = s2;
     a.out = out; a.route = r;
-    a.xs = ws + L.xs; a.as = ws + L.as;
+    a.xs = ws + L.xs;
+    a.af = reinterpret_cast<float*>(ws + L.af);
+    a.a16 = ws + L.a16;
+    a.aexp = reinterpret_cast<int32_t*>(ws + L.aexp);
     a.outacc = reinterpret_cast<float*>(ws + L.outacc);
     a.status = status; a.num_sms = sms;
+    a.wait_ns = wait.limit_ns;
+    a.opt = opt;
     e = launch_prefill(a, s);
   } else {
     DecodeArgs a{};
@@ -105,6 +130,8 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
     a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
     a.status = status; a.num_sms = sms;
     a.sync = reinterpret_cast<uint32_t*>(ws + L.sync);
+    a.wait = wait;
+    a.opt = opt;
     e = launch_decode(a, s);
   }
   g_timing.n = 0;
@@ -112,6 +139,24 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
 }
 
 }  // namespace
+
+int read_and_clear_status(uint8_t* ws, uint32_t* status, cudaStream_t s) {
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws + kStatusOffset, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the status word, and the fused decode kernel's epoch and flags (a kernel
+  // that gave up a wait may have left them inconsistent)
+  if (cudaMemsetAsync(ws + kStatusOffset, 0, sizeof(v), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws + kSyncOffset, 0, 4 * kSyncWords, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+WaitSettings take_wait_settings() {
+  const WaitSettings w = g_wait;
+  g_wait = WaitSettings{};
+  return w;
+}
 
 void timing_mark(int index, bool end, cudaStream_t s) {
   if (index >= g_timing.n) return;
@@ -155,6 +200,7 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   size_t o = 0;
   L.status = o; o = align256(o + 256);
   L.sync = o; o = align256(o + 4 * kSyncWords);
+  static_assert(kStatusOffset == 0 && kSyncOffset == 256, "status and sync words lead every workspace");
   L.counts = o; o = align256(o + 4 * E);
   L.offsets = o; o = align256(o + 4 * (E + 1));
   L.active = o; o = align256(o + 4 * E);
@@ -168,7 +214,9 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.n_mtiles_dn = o; o = align256(o + 4);
   if (L.prefill) {
     L.xs = o; o = align256(o + 2 * P * H);
-    L.as = o; o = align256(o + 4 * P * I);
+    L.af = o; o = align256(o + 4 * P * I);
+    L.a16 = o; o = align256(o + 2 * P * I);
+    L.aexp = o; o = align256(o + 4 * P);
     L.outacc = o; o = align256(o + 4 * T * H);
   } else {
     L.abuf = o; o = align256(o + 4 * P * I);
@@ -194,14 +242,30 @@ size_t moe_workspace_bytes(const moe_dims_t* d) {
 int moe_a16w4_mxfp4(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
                     const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
                     void* out, void* workspace, size_t workspace_bytes, void* stream) {
-  return run_moe(d, x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, workspace, workspace_bytes, stream,
-                 WeightKind::kMxfp4);
+  return run_moe(d, x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, nullptr, out, workspace, workspace_bytes,
+                 stream, WeightKind::kMxfp4);
 }
 
 int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
                       const uint8_t* w13_q, const float* w13_s, const uint8_t* w2_q, const float* w2_s, void* out,
                       void* workspace, size_t workspace_bytes, void* stream) {
-  return run_moe(d, x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out, workspace, workspace_bytes, stream,
+  return run_moe(d, x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, nullptr, out, workspace, workspace_bytes,
+                 stream, WeightKind::kInt4);
+}
+
+int moe_a16w4_mxfp4_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                       const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                       const moe_options_t* opt, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return run_moe(d, x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, opt, out, workspace, workspace_bytes,
+                 stream, WeightKind::kMxfp4);
+}
+
+int moe_a16w4_int4g32_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                         const uint8_t* w13_q, const float* w13_s, const uint8_t* w2_q, const float* w2_s,
+                         const moe_options_t* opt, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return run_moe(d, x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, opt, out, workspace, workspace_bytes, stream,
                  WeightKind::kInt4);
 }
 
@@ -241,26 +305,32 @@ int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int
   r.offsets = offsets;
   r.sorted_pair = sorted_pair;
   r.pair_pos = pair_pos;
-  if (launch_route(topk_ids, d->E, d->T, d->topk, r, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (launch_route(topk_ids, d->E, d->T, d->topk, nullptr, 0, r, 0, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+int moe_router_topk(const float* logits, int32_t T, int32_t G, int32_t topk, int32_t renormalize,
+                    int32_t* topk_ids, float* topk_w, void* stream) {
+  if (T < 0 || G < 1 || G > 1024 || topk < 1 || topk > 64 || topk > G || (renormalize != 0 && renormalize != 1) ||
+      (long long)T * G > (1ll << 31) - 1)
+    return MOE_ERR_BAD_DIMS;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_NULL;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_ALIGN;
+  const int rc = check_device(nullptr);
+  if (rc != MOE_OK) return rc;
+  return launch_router_topk(logits, T, G, topk, renormalize, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream) {
   if (!d || !workspace || !status) return MOE_ERR_NULL;
   if (!dims_valid(d)) return MOE_ERR_BAD_DIMS;
-  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t v = 0;
-  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
-  // the status word, and the fused decode kernel's epoch and flags (a kernel
-  // that gave up a wait may have left them inconsistent)
-  const Workspace L = workspace_layout(d, WeightKind::kMxfp4);
-  if (cudaMemsetAsync(ws, 0, sizeof(v), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(ws + L.sync, 0, 4 * kSyncWords, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
-  *status = v;
-  return MOE_OK;
+  return read_and_clear_status(reinterpret_cast<uint8_t*>(workspace), status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_set_timing_events(void* const* events, int32_t n) {
@@ -268,6 +338,13 @@ int moe_set_timing_events(void* const* events, int32_t n) {
   if (n > 0 && !events) return MOE_ERR_NULL;
   for (int i = 0; i < 2 * n; ++i) g_timing.ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   g_timing.n = n;
+  return MOE_OK;
+}
+
+int moe_set_wait_limit(uint64_t limit_ns, int32_t extra_waiters) {
+  if (limit_ns == 0 || extra_waiters < 0 || extra_waiters > 64) return MOE_ERR_BAD_DIMS;
+  g_wait.limit_ns = limit_ns;
+  g_wait.extra_waiters = extra_waiters;
   return MOE_OK;
 }
 
@@ -285,6 +362,6 @@ const char* moe_error_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 }  // extern "C"

@@ -71,14 +71,15 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for phase ``parity`` of ``bar`` to complete, giving up after
-// kWaitLimitNs.  On give-up the status word gets MOE_STATUS_WAIT_TIMEOUT and
+// ``limit_ns``.  On give-up the status word gets MOE_STATUS_WAIT_TIMEOUT and
 // the function returns false; callers then stop their pipeline.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 255u && global_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusWaitTimeout);
       return false;
     }
@@ -140,6 +141,16 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// After relaxed loads that observed other threads' release stores: makes
+// their earlier writes visible to this thread's later reads (acquire pattern).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Value that CTA ``slot`` publishes for ``token``: distinct per slot, so no
 // constant fill of the flag array matches, and a bijection of the token
 // (odd multiplier), so flags left by another token never match.
@@ -148,22 +159,39 @@ __device__ __forceinline__ uint32_t published_value(uint32_t token, int slot) {
 }
 
 // One warp waits until every flags[q], q < n, holds published_value(token, q)
-// (acquire), giving up after kWaitLimitNs like mbar_wait.  Every lane returns
+// (acquire), giving up after ``limit_ns`` like mbar_wait.  Every lane returns
 // the same value.
-__device__ __forceinline__ bool wait_all_published(const uint32_t* flags, int n, uint32_t token, uint32_t* status) {
+__device__ __forceinline__ bool wait_all_published(const uint32_t* flags, int n, uint32_t token, uint32_t* status,
+                                                   uint64_t limit_ns) {
   const int lane = threadIdx.x & 31;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0;; ++i) {
+    // every flag of this lane loaded at once (relaxed, independent), one
+    // acquire fence once all have been seen
     bool ok = true;
-    for (int q = lane; q < n && ok; q += 32) ok = ld_acquire_gpu(flags + q) == published_value(token, q);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    const bool late = (i & 15u) == 15u && global_ns() - t0 > kWaitLimitNs;
+    for (int q = lane; q < n; q += 32) ok &= ld_relaxed_gpu(flags + q) == published_value(token, q);
+    if (__all_sync(0xffffffffu, ok)) {
+      fence_acq_rel_gpu();
+      return true;
+    }
+    const bool late = (i & 15u) == 15u && global_ns() - t0 > limit_ns;
     if (__any_sync(0xffffffffu, late)) {
       if (lane == 0) atomicOr(status, kStatusWaitTimeout);
       return false;
     }
     __nanosleep(64);
   }
+}
+
+// ---------------------------------------------------------------- expert ids
+
+// Local expert id of top-k slot ``p``: ids[p], mapped through ``emap`` (G
+// entries, global id -> local id or -1) when one is given; -1 when the slot
+// has no expert of this GPU.
+__device__ __forceinline__ int local_expert(const int32_t* ids, long long p, const int32_t* emap, int G, int E) {
+  int e = ids[p];
+  if (emap) e = (unsigned)e < (unsigned)G ? emap[e] : -1;
+  return (unsigned)e < (unsigned)E ? e : -1;
 }
 
 // ---------------------------------------------------------------- numeric helpers
@@ -196,6 +224,12 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
   return r;
 }
 

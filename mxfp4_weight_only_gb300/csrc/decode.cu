@@ -48,6 +48,16 @@ constexpr int kGroup = 8;             // pair columns per group (one 8-column MM
 constexpr int kRedFloats = kConsumerWarps * kRows * kGroup;  // one reduction buffer
 constexpr int kRedBufs = 3;                                  // reduction ring depth
 static_assert(kGroup == kMoeGroup, "routing and the decode kernels must agree on the group size");
+
+// Index of consumer warp w's partial sum for (weight row, pair column) in a
+// reduction buffer: column-major per warp (a column's 32 rows contiguous, so
+// the epilogue reads only the columns of pairs that exist), rows XOR-swizzled
+// by the column pair so that the consumers' stores (lanes = 8 rows x 4 column
+// pairs) hit 32 different banks.
+__device__ __forceinline__ int red_idx(int w, int row, int col) {
+  return w * (kRows * kGroup) + col * kRows + (row ^ (8 * ((col >> 1) & 3)));
+}
+static_assert(kRows == 32 && kGroup == 8, "reduction buffer swizzle");
 // Batches of at most kLocalRoute pairs are grouped by every CTA itself, in
 // shared memory, at the start of both kernels: no routing kernel runs before
 // them.  Region: active experts, their first sorted position, their group
@@ -81,13 +91,29 @@ struct GemmParams {
   int srow_bytes;          // scale bytes per weight row
   int stage_bytes;
   int n_stages;
+  uint64_t wait_ns;        // limit of every bounded wait
+  int wait_extra;          // fused kernel, tests only: CTAs its cross-CTA wait expects beyond the grid
+  const float* topk_w;     // [T][topk]
+  // optional inputs
+  const uint16_t* bias;    // bf16 [E][N] added to the outputs (gate_up: b13, down: b2), or null
+  const int32_t* emap;     // global -> local expert ids, or null
+  int G;                   // entries of emap
+  int rwi;                 // router weight on the input (gate_up scales h), unweighted combine
 };
 
-// (c0, c1) += s * (x0, x1) as one packed f32x2 FMA (same rounding as two fmaf).
-__device__ __forceinline__ void fma_f32x2_bcast(float& c0, float& c1, float s, float x0, float x1) {
-  asm("{\n .reg .b64 d, a, b, c;\n mov.b64 a, {%2, %2};\n mov.b64 b, {%3, %4};\n mov.b64 c, {%0, %1};\n"
+// (c0, c1) += (s0, s1) * (x0, x1) as one packed f32x2 FMA (same rounding as two fmaf).
+__device__ __forceinline__ void fma_f32x2(float& c0, float& c1, float s0, float s1, float x0, float x1) {
+  asm("{\n .reg .b64 d, a, b, c;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%0, %1};\n"
       " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
       : "+f"(c0), "+f"(c1)
+      : "f"(s0), "f"(s1), "f"(x0), "f"(x1));
+}
+
+// (d0, d1) = s * (x0, x1) as one packed f32x2 multiply.
+__device__ __forceinline__ void mul_f32x2_bcast(float& d0, float& d1, float s, float x0, float x1) {
+  asm("{\n .reg .b64 d, a, b;\n mov.b64 a, {%2, %2};\n mov.b64 b, {%3, %4};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d0), "=f"(d1)
       : "f"(s), "f"(x0), "f"(x1));
 }
 
@@ -325,13 +351,52 @@ __device__ __forceinline__ void init_barriers(const CtaSmem& c, int S) {
 // yet.  Ends with a CTA barrier.
 __device__ void local_grouping(const GemmParams& p, const CtaSmem& c) {
   const int tid = threadIdx.x;
+  if (p.P <= 32) {
+    // one warp holds every pair (lane = pair): ranks among equal experts by
+    // __match_any_sync, sorted positions and active-list fields by one pass of
+    // shuffles over the 32 lanes; no CTA-wide barrier until the end
+    if (tid < 32) {
+      const int lane = tid;
+      const int e = lane < p.P ? local_expert(p.ids, lane, p.emap, p.G, p.E) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int cnt = __popc(peers);
+      const bool first = e >= 0 && rank == 0;
+      const int groups = first ? (cnt + kGroup - 1) / kGroup : 0;
+      int less = 0, dd = 0, gp = 0;  // valid pairs, active experts and their groups with a smaller id
+#pragma unroll 8
+      for (int q = 0; q < 32; ++q) {
+        const int f = __shfl_sync(0xffffffffu, e, q);
+        const int fg = __shfl_sync(0xffffffffu, groups, q);
+        const bool smaller = f >= 0 && f < e;
+        less += smaller ? 1 : 0;
+        dd += (smaller && fg > 0) ? 1 : 0;
+        gp += smaller ? fg : 0;
+      }
+      if (e >= 0) c.r_pair[less + rank] = lane;
+      if (first) {
+        c.r_act[dd] = e;
+        c.r_base[dd] = less;
+        c.r_gpre[dd] = gp;
+      }
+      const int n = __popc(__ballot_sync(0xffffffffu, first));
+      const int tot = __popc(__ballot_sync(0xffffffffu, e >= 0));
+      int gt = groups;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      if (lane == 0) {
+        c.r_base[n] = tot;
+        c.r_gpre[n] = gt;
+        *c.r_n = n;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   int32_t* ids_s = reinterpret_cast<int32_t*>(c.stages);  // [P] expert or -1
   int32_t* first_g = ids_s + kLocalRoute;                 // [P] groups of its expert at its first pair, else 0
   const int P = p.P;
-  if (tid < P) {
-    const int e = p.ids[tid];
-    ids_s[tid] = (unsigned)e < (unsigned)p.E ? e : -1;
-  }
+  if (tid < P) ids_s[tid] = local_expert(p.ids, tid, p.emap, p.G, p.E);
   __syncthreads();
   int e = -1, less = 0, rank = 0, cnt = 0;
   if (tid < P) {
@@ -405,20 +470,33 @@ __device__ __forceinline__ Grouping grouping_view(const GemmParams& p, const Cta
   return g;
 }
 
-// This CTA's contiguous run [u0, u1) of a phase's work units (active expert d,
-// 8-pair group, weight tile j; group-major within an expert, so a run reloads
-// activations only at group boundaries; experts with more than 8 pairs stream
-// their weights once per group), and the active expert d0 holding unit u0.
+// This CTA's contiguous run [u0, u1) of the work units of active experts
+// [d_lo, d_hi) in one phase (unit = active expert d, 8-pair group, weight
+// tile j; group-major within an expert, so a run reloads activations only at
+// group boundaries; experts with more than 8 pairs stream their weights once
+// per group), and the active expert d0 holding unit u0.  Every CTA gets
+// floor(n / grid) units, and the n % grid remaining ones go to the CTAs of a
+// window that starts at ``rot`` (wrapping); ``rot`` then moves past that
+// window, so over several phases each CTA gets within one unit of its share.
 struct UnitRange {
   int u0, u1, d0;
 };
 
-__device__ __forceinline__ UnitRange cta_units(const Grouping& gr, int tiles) {
+__device__ __forceinline__ UnitRange cta_units(const Grouping& gr, int tiles, int d_lo, int d_hi, int& rot) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int U0 = gr.gpre[d_lo] * tiles;
+  const int n = gr.gpre[d_hi] * tiles - U0;
+  const int base = n / G, rem = n - base * G;
+  // CTAs c < b holding one of the rem extra units: ((c - rot) mod G) < rem
+  int before;
+  if (rot + rem <= G) before = min(max(b - rot, 0), rem);
+  else before = min(b, rot + rem - G) + max(b - rot, 0);
+  const bool extra = ((b - rot + G) % G) < rem;
   UnitRange r;
-  const int n_units = gr.gpre[gr.n_act] * tiles;
-  r.u0 = (int)((long long)n_units * blockIdx.x / gridDim.x);
-  r.u1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x);
-  int lo = 0, hi = gr.n_act;  // largest d with gpre[d] * tiles <= u0
+  r.u0 = U0 + b * base + before;
+  r.u1 = r.u0 + base + (extra ? 1 : 0);
+  rot = (rot + rem) % G;
+  int lo = d_lo, hi = d_hi;  // largest d with gpre[d] * tiles <= u0
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (gr.gpre[mid] * tiles <= r.u0) lo = mid; else hi = mid;
@@ -456,7 +534,7 @@ __device__ void produce_units(const GemmParams& p, const Grouping& gr, const Uni
     if (*c.abort_flag) return;
     if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
     const int j = cur.j;
-    if (ring.n >= S && !mbar_wait(&c.empty[ring.slot], ring.parity ^ 1u, p.status)) {
+    if (ring.n >= S && !mbar_wait(&c.empty[ring.slot], ring.parity ^ 1u, p.status, p.wait_ns)) {
       *c.abort_flag = 1;
       return;
     }
@@ -482,7 +560,7 @@ __device__ void produce_units(const GemmParams& p, const Grouping& gr, const Uni
 
 // Before the CTA may exit: wait for the last min(fills, S) fills, walking the
 // ring backwards (earlier ones were consumed).
-__device__ void producer_drain(const CtaSmem& c, int S, RingPos ring, uint32_t* status) {
+__device__ void producer_drain(const CtaSmem& c, int S, RingPos ring, uint32_t* status, uint64_t limit_ns) {
   for (int v = 0; v < (ring.n < S ? ring.n : S); ++v) {
     if (ring.slot == 0) {
       ring.slot = S - 1;
@@ -490,57 +568,62 @@ __device__ void producer_drain(const CtaSmem& c, int S, RingPos ring, uint32_t* 
     } else {
       --ring.slot;
     }
-    mbar_wait(&c.full[ring.slot], ring.parity, status);
+    mbar_wait(&c.full[ring.slot], ring.parity, status, limit_ns);
   }
 }
 
-// Epilogue warp: sums the consumer warps' partials of each unit and writes
-// the results while the consumers go on with the next units.
+// Epilogue warp: sums the consumer warps' partials of each unit over the
+// pair columns that exist and writes the results (gate_up: SiLU(h_gate) *
+// h_up into abuf; down: per-pair rows into ybuf) while the consumers go on
+// with the next units.
 template <bool GATE_UP>
 __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
                              RingPos& rr) {
   const int lane = threadIdx.x & 31;
   UnitCursor cur;
   if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
+  int cur_e = -1, cur_grp = -1;
+  // lane < nv: its pair column's pair and router weight
+  int my_pair = -1;
+  float my_w = 0.f;
   for (int u = r.u0; u < r.u1; ++u) {
     if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
     const int d = cur.d, grp = cur.grp, j = cur.j;
     const int e = gr.act[d];
     const int base = gr.base(d, e);
     const int npairs = gr.end(d, e) - base;
-    if (!mbar_wait(&c.red_full[rr.slot], rr.parity, p.status)) {
+    const int nv = min(kGroup, npairs - grp * kGroup);  // pair columns that exist
+    if (e != cur_e || grp != cur_grp) {
+      cur_e = e;
+      cur_grp = grp;
+      my_pair = lane < nv ? gr.spair[base + grp * kGroup + lane] : -1;
+      my_w = (GATE_UP && p.rwi && my_pair >= 0) ? p.topk_w[my_pair] : 0.f;
+    }
+    // this lane's output row of the unit: gate_up lanes 0-15 gate rows, 16-31 up rows
+    const int orow = GATE_UP ? (lane < kRows / 2 ? (kRows / 2) * j + lane : p.I + (kRows / 2) * j + lane - kRows / 2)
+                             : kRows * j + lane;
+    const float bias = p.bias ? bf16_lo(p.bias[(size_t)e * p.N + orow]) : 0.f;
+    if (!mbar_wait(&c.red_full[rr.slot], rr.parity, p.status, p.wait_ns)) {
       *c.abort_flag = 1;
       return;
     }
     const float* rb = c.red + rr.slot * kRedFloats;
-    if (GATE_UP) {
-      constexpr int kOut = kRows / 2;  // activated outputs per unit
+    for (int cc = 0; cc < nv; ++cc) {
+      float v = 0.f;
 #pragma unroll
-      for (int q = 0; q < kOut * kGroup / 32; ++q) {
-        const int idx = lane + 32 * q;
-        const int row = idx / kGroup, col = idx % kGroup;
-        float hg = 0.f, hu = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          hg += rb[w * kRows * kGroup + row * kGroup + col];
-          hu += rb[w * kRows * kGroup + (row + kOut) * kGroup + col];
-        }
-        const int slot = grp * kGroup + col;
-        if (slot < npairs) p.dst[(size_t)(base + slot) * p.I + kOut * j + row] = silu(hg) * hu;
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < kRows * kGroup / 32; ++q) {
-        const int idx = lane + 32 * q;
-        const int row = idx / kGroup, col = idx % kGroup;
-        float y = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + row * kGroup + col];
-        const int slot = grp * kGroup + col;
-        if (slot < npairs) {
-          const int pair = gr.spair[base + slot];
-          p.dst[(size_t)pair * p.N + kRows * j + row] = y;
-        }
+      for (int w = 0; w < kConsumerWarps; ++w) v += rb[red_idx(w, lane, cc)];
+      if (GATE_UP) {
+        // h = (router weight) * W13 x + b13: the router weight on the input
+        // scales the GEMM's output exactly as it would scale x
+        if (p.rwi) v *= __shfl_sync(0xffffffffu, my_w, cc);
+        v += bias;
+        // lanes 0-15 hold the gate rows of the unit's 16 outputs, lanes 16-31 the up rows
+        const float hu = __shfl_down_sync(0xffffffffu, v, 16);
+        if (lane < kRows / 2)
+          p.dst[(size_t)(base + grp * kGroup + cc) * p.I + (kRows / 2) * j + lane] = silu(v) * hu;
+      } else {
+        const int pair = __shfl_sync(0xffffffffu, my_pair, cc);
+        p.dst[(size_t)pair * p.N + kRows * j + lane] = v + bias;
       }
     }
     __syncwarp();
@@ -565,7 +648,7 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
   const int cnt = min(nbw, nb - wb0);
 
   uint32_t xf[NBW][4];
-  float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1
+  float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1 (folded into the block scales)
   int cur_e = -1, cur_grp = -1;
   UnitCursor cur;
   if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
@@ -581,7 +664,7 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
       cur_e = e;
       cur_grp = grp;
     }
-    if (!mbar_wait(&c.full[wr.slot], wr.parity, p.status)) {
+    if (!mbar_wait(&c.full[wr.slot], wr.parity, p.status, p.wait_ns)) {
       *c.abort_flag = 1;
       return;
     }
@@ -602,6 +685,14 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
           const int row = 16 * tl + g;
           float sc[2][2];  // [row / row+8][block b / b+1]
           load_scales2<KIND>(ss, p.srow_bytes, row, b, sc);
+          // block scale times each pair column's power-of-two undo: the partial
+          // sums stay at the magnitude of the result (no float32 overflow for
+          // large block scales with tiny, up-scaled activations)
+          float m[2][2][2];  // [row / row+8][block][column 2t / 2t+1]
+#pragma unroll
+          for (int r2 = 0; r2 < 2; ++r2)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) mul_f32x2_bcast(m[r2][h][0], m[r2][h][1], sc[r2][h], inv[0], inv[1]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint8_t* rg = sw + row * p.row_stride + (b + h) * 16 + 4 * t;
@@ -611,8 +702,8 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
             float dd[4];
             mma_f16_16816(dd, a0, c0, a1, c1, xf[bb + h][0], xf[bb + h][1], zero);
             mma_f16_16816(dd, a2, c2, a3, c3, xf[bb + h][2], xf[bb + h][3], dd);
-            fma_f32x2_bcast(acc[tl][0], acc[tl][1], sc[0][h], dd[0], dd[1]);
-            fma_f32x2_bcast(acc[tl][2], acc[tl][3], sc[1][h], dd[2], dd[3]);
+            fma_f32x2(acc[tl][0], acc[tl][1], m[0][h][0], m[0][h][1], dd[0], dd[1]);
+            fma_f32x2(acc[tl][2], acc[tl][3], m[1][h][0], m[1][h][1], dd[2], dd[3]);
           }
         }
       }
@@ -622,17 +713,18 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
     wr.advance(S);
 
     // ---- hand the partial sums to the epilogue warp
-    if (rr.n >= kRedBufs && !mbar_wait(&c.red_empty[rr.slot], rr.parity ^ 1u, p.status)) {
+    if (rr.n >= kRedBufs && !mbar_wait(&c.red_empty[rr.slot], rr.parity ^ 1u, p.status, p.wait_ns)) {
       *c.abort_flag = 1;
       return;
     }
-    float* rw = c.red + rr.slot * kRedFloats + warp * (kRows * kGroup);
+    float* rw = c.red + rr.slot * kRedFloats;
 #pragma unroll
     for (int tl = 0; tl < kTiles; ++tl) {
       const int row = 16 * tl + g;
-      *reinterpret_cast<float2*>(rw + row * kGroup + 2 * t) = make_float2(acc[tl][0] * inv[0], acc[tl][1] * inv[1]);
-      *reinterpret_cast<float2*>(rw + (row + 8) * kGroup + 2 * t) =
-          make_float2(acc[tl][2] * inv[0], acc[tl][3] * inv[1]);
+      rw[red_idx(warp, row, 2 * t)] = acc[tl][0];
+      rw[red_idx(warp, row, 2 * t + 1)] = acc[tl][1];
+      rw[red_idx(warp, row + 8, 2 * t)] = acc[tl][2];
+      rw[red_idx(warp, row + 8, 2 * t + 1)] = acc[tl][3];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.red_full[rr.slot]);
@@ -655,11 +747,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   grid_dep_launch_dependents();
   if (p.local) local_grouping(p, c);
   const Grouping gr = grouping_view(p, c);
-  const UnitRange r = cta_units(gr, p.tiles);
+  int rot = 0;
+  const UnitRange r = cta_units(gr, p.tiles, 0, gr.n_act, rot);
   RingPos wr{0, 0, 0u}, rr{0, 0, 0u};
   if (warp == kProducerWarp) {
     produce_units<GATE_UP>(p, gr, r, c, l2_policy_evict_first(), wr);
-    producer_drain(c, p.n_stages, wr, p.status);
+    producer_drain(c, p.n_stages, wr, p.status, p.wait_ns);
     return;
   }
   if (warp == kEpilogueWarp) {
@@ -670,17 +763,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
   consume_units<KIND, GATE_UP, NBW>(p, gr, r, c, wr, rr);
 }
 
-// Both GEMM stages in one persistent launch (grid = one CTA per SM, all
-// resident).  The weight stream runs on from the gate_up units into the down
-// units without a gap; the down units' activations come from every CTA, so
-// before its first down unit a CTA waits until all CTAs have published their
-// gate_up results.  Publication: each CTA's epilogue warp writes the call's
-// token into its own flag (release) after its last activation store; the
-// waiting warp reads all flags (acquire).  The token is epoch + 1, the epoch
-// word being advanced by CTA 0 once every CTA has published (so every CTA
-// read it before); the published values differ per CTA and per token, so
-// flags left by earlier calls (or any constant fill) never match: the flags
-// and the epoch need no clearing between calls.
+// Both GEMM stages in one persistent, cooperative launch (grid = the CTAs
+// that can be resident at once).  The weight stream runs on from the gate_up
+// units into the down units without a gap; the down units' activations come
+// from every CTA, so before its first down unit a CTA waits until all CTAs
+// have published their gate_up results.  Publication: each CTA's epilogue
+// warp writes the call's token into its own flag (release) after its last
+// activation store; the waiting warp reads all flags (relaxed, then one
+// acquire fence).  The token is epoch + 1, the epoch word being advanced by
+// CTA 0 once every CTA has published (so every CTA read it before); the
+// published values differ per CTA and per token, so flags left by earlier
+// calls (or any constant fill) never match: the flags and the epoch need no
+// clearing between calls.  (Splitting each phase into two halves of the
+// experts, so the wait for the first half hides behind the second half's
+// units, measured slower: every CTA then reloads its activation fragments in
+// twice as many places, and each reload is a global-memory round trip of
+// about 2 us under the full weight stream.)
 template <WeightKind KIND, int NBW>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const GemmParams p1, const GemmParams p2) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -694,14 +792,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const Gemm
   __syncthreads();
   const uint32_t token = *c.token;
   const Grouping gr = grouping_view(p1, c);
-  const UnitRange r1 = cta_units(gr, p1.tiles);
-  const UnitRange r2 = cta_units(gr, p2.tiles);
+  int rot = 0;
+  const UnitRange r1 = cta_units(gr, p1.tiles, 0, gr.n_act, rot);
+  const UnitRange r2 = cta_units(gr, p2.tiles, 0, gr.n_act, rot);
   RingPos wr{0, 0, 0u}, rr{0, 0, 0u};
   if (warp == kProducerWarp) {
     const uint64_t policy = l2_policy_evict_first();
     produce_units<true>(p1, gr, r1, c, policy, wr);
     produce_units<false>(p2, gr, r2, c, policy, wr);
-    producer_drain(c, p1.n_stages, wr, p1.status);
+    producer_drain(c, p1.n_stages, wr, p1.status, p1.wait_ns);
     return;
   }
   if (warp == kEpilogueWarp) {
@@ -717,7 +816,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const Gemm
   // CTA 0 always waits: it advances the epoch
   if (r2.u0 < r2.u1 || blockIdx.x == 0) {
     if (warp == 0) {
-      if (!wait_all_published(p1.flags, gridDim.x, token, p1.status) && lane == 0) *c.abort_flag = 1;
+      if (!wait_all_published(p1.flags, gridDim.x + p1.wait_extra, token, p1.status, p1.wait_ns) && lane == 0)
+        *c.abort_flag = 1;
       if (blockIdx.x == 0 && lane == 0) *p1.epoch = token;
     }
     named_bar_sync(1, kConsumerWarps * 32);
@@ -728,33 +828,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const Gemm
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ ybuf,
                                                       const int32_t* __restrict__ ids,
                                                       const float* __restrict__ topk_w, int E, int topk,
-                                                      int H, uint16_t* __restrict__ out) {
+                                                      int H, uint16_t* __restrict__ out,
+                                                      const int32_t* __restrict__ emap, int G, int rwi) {
   __shared__ int s_ids[64];
   __shared__ float s_w[64];
   // the next kernel on the stream may start its prologue now; it waits
   // (griddepcontrol.wait) for this grid to complete before using anything
   grid_dep_launch_dependents();
-  grid_dep_wait();  // ybuf comes from the down kernel
+  // ids and router weights are read before the wait for the GEMM kernel: they
+  // are inputs of the call, written before the call's first kernel, which
+  // waited for all earlier work before it let this grid launch
   const int t = blockIdx.y;
   if (threadIdx.x < topk) {
-    s_ids[threadIdx.x] = ids[t * topk + threadIdx.x];
-    s_w[threadIdx.x] = topk_w[t * topk + threadIdx.x];
+    s_ids[threadIdx.x] = local_expert(ids, t * topk + threadIdx.x, emap, G, E);
+    s_w[threadIdx.x] = rwi ? 1.f : topk_w[t * topk + threadIdx.x];
   }
+  grid_dep_wait();  // ybuf comes from the down kernel
   __syncthreads();
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c4 * 4 >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* yb = reinterpret_cast<const float4*>(ybuf + (size_t)t * topk * H) + c4;
   const int h4 = H / 4;
-  for (int k0 = 0; k0 < topk; k0 += 8) {
-    float4 y[8];
+  // all of a round's loads are issued before any use (one memory latency per
+  // 16 slots: a whole top-15 token in one round)
+  for (int k0 = 0; k0 < topk; k0 += 16) {
+    float4 y[16];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 16; ++k) {
       const bool valid = k0 + k < topk && (unsigned)s_ids[k0 + k] < (unsigned)E;
       y[k] = valid ? __ldcg(yb + (size_t)(k0 + k) * h4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 16; ++k) {
       if (k0 + k < topk && (unsigned)s_ids[k0 + k] < (unsigned)E) {
         const float wk = s_w[k0 + k];
         acc.x = fmaf(wk, y[k].x, acc.x);
@@ -776,7 +882,7 @@ cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, gp);
+  return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, false, gp);
 }
 
 // activation blocks of 32 per consumer warp (even), which sizes the register fragments
@@ -794,13 +900,29 @@ cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
 // both GEMMs).
 constexpr int kFusedNbw = 8;
 
+// CTAs of the fused kernel that can be resident at once on this device (0 if
+// the device cannot launch cooperative grids or a query fails).  Its CTAs
+// wait on one another, so it is launched as a cooperative grid of this size:
+// the launch then either places every CTA at once or fails, instead of
+// leaving CTAs waiting for others that cannot be scheduled.
+template <WeightKind KIND>
+int fused_resident_ctas(size_t smem, int sms) {
+  auto kern = decode_fused_kernel<KIND, kFusedNbw>;
+  int dev = 0, coop = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem) != cudaSuccess) return 0;
+  return per_sm * sms;
+}
+
 template <WeightKind KIND>
 cudaError_t launch_fused(const GemmParams& g1, const GemmParams& g2, int grid, cudaStream_t s) {
   const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
   auto kern = decode_fused_kernel<KIND, kFusedNbw>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, g1, g2);
+  return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, true, g1, g2);
 }
 
 int stage_bytes_for(int K, WeightKind kind, int* row_stride, int* srow_bytes) {
@@ -848,6 +970,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g1.status = a.status;
   g1.epoch = a.sync;
   g1.flags = a.sync ? a.sync + kSyncFlagsOffset : nullptr;
+  g1.wait_ns = a.wait.limit_ns;
+  g1.wait_extra = 0;
+  g1.topk_w = a.topk_w;
+  g1.bias = a.opt.b13;
+  g1.emap = a.opt.emap;
+  g1.G = a.opt.G;
+  g1.rwi = a.opt.rwi;
 
   GemmParams g2 = g1;
   g2.w = a.w2;
@@ -857,26 +986,52 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g2.tiles = a.H / kRows;
   g2.src = a.abuf;
   g2.dst = a.ybuf;
+  g2.bias = a.opt.b2;
 
-  // one launch for both GEMMs when both fit the fused kernel's fragments and
-  // its grid fits the flag array
-  const bool fused = a.sync != nullptr && blocks_per_warp(a.H) <= kFusedNbw && blocks_per_warp(a.I) <= kFusedNbw &&
-                     a.num_sms <= kMaxSyncCtas;
-  fill_stage_geometry(g1, a.kind, fused ? &g2 : nullptr);
-  fill_stage_geometry(g2, a.kind, fused ? &g1 : nullptr);
+  const bool fp4 = a.kind == WeightKind::kMxfp4;
+  // one launch for both GEMMs when both fit the fused kernel's fragments and a
+  // resident grid fits the flag array
+  bool fused = a.sync != nullptr && blocks_per_warp(a.H) <= kFusedNbw && blocks_per_warp(a.I) <= kFusedNbw;
+  int fused_grid = 0;
+  if (fused) {
+    fill_stage_geometry(g1, a.kind, &g2);
+    fill_stage_geometry(g2, a.kind, &g1);
+    const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
+    fused_grid = fp4 ? fused_resident_ctas<WeightKind::kMxfp4>(smem, a.num_sms)
+                     : fused_resident_ctas<WeightKind::kInt4>(smem, a.num_sms);
+    g1.wait_extra = a.wait.extra_waiters;
+    fused = fused_grid >= 1 && g1.n_stages >= 2 && fused_grid + a.wait.extra_waiters <= kMaxSyncCtas;
+  }
+  if (!fused) {
+    fill_stage_geometry(g1, a.kind, nullptr);
+    fill_stage_geometry(g2, a.kind, nullptr);
+    g1.wait_extra = 0;
+  }
   if (g1.n_stages < 2 || g2.n_stages < 2) return cudaErrorInvalidValue;
 
   cudaError_t e;
-  const bool fp4 = a.kind == WeightKind::kMxfp4;
   if (fused) {
     timing_mark(1, false, s);
-    e = fp4 ? launch_fused<WeightKind::kMxfp4>(g1, g2, a.num_sms, s)
-            : launch_fused<WeightKind::kInt4>(g1, g2, a.num_sms, s);
+    e = fp4 ? launch_fused<WeightKind::kMxfp4>(g1, g2, fused_grid, s)
+            : launch_fused<WeightKind::kInt4>(g1, g2, fused_grid, s);
     timing_mark(1, true, s);
-    if (e != cudaSuccess) return e;
-    timing_mark(2, false, s);
-    timing_mark(2, true, s);
-  } else {
+    if (e != cudaSuccess) {
+      // a cooperative grid that cannot be placed (for example under an SM
+      // limit) fails at launch: outside stream capture the call goes on with
+      // the two-launch path, under capture the error is returned
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return e;
+      (void)cudaGetLastError();
+      fused = false;
+      fill_stage_geometry(g1, a.kind, nullptr);
+      fill_stage_geometry(g2, a.kind, nullptr);
+      g1.wait_extra = 0;
+    } else {
+      timing_mark(2, false, s);
+      timing_mark(2, true, s);
+    }
+  }
+  if (!fused) {
     timing_mark(1, false, s);
     e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, true>(g1, a.num_sms, s)
             : dispatch_nbw<WeightKind::kInt4, true>(g1, a.num_sms, s);
@@ -890,8 +1045,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   }
   dim3 cgrid((a.H / 4 + 127) / 128, a.T);
   timing_mark(3, false, s);
-  e = launch_kernel(combine_kernel, cgrid, dim3(128), 0, s, true, (const float*)a.ybuf, a.topk_ids, a.topk_w, a.E,
-                    a.topk, a.H, reinterpret_cast<uint16_t*>(a.out));
+  e = launch_kernel(combine_kernel, cgrid, dim3(128), 0, s, true, false, (const float*)a.ybuf, a.topk_ids, a.topk_w, a.E,
+                    a.topk, a.H, reinterpret_cast<uint16_t*>(a.out), a.opt.emap, a.opt.G, a.opt.rwi);
   timing_mark(3, true, s);
   return e;
 }

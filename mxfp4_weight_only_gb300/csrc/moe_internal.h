@@ -37,18 +37,31 @@ constexpr int kTcRowsDown = 128; // sorted rows per down work item (MMA N, at mo
 
 enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
 
+// Optional inputs of a call (moe_options_t), as the kernels read them.
+struct LayerOptions {
+  const uint16_t* b13 = nullptr;   // bf16 [E][2I], added to the gate_up outputs
+  const uint16_t* b2 = nullptr;    // bf16 [E][H], added to each expert's output
+  const int32_t* emap = nullptr;   // [G] global expert id -> local id or -1
+  int G = 0;
+  int rwi = 0;                     // router weight on the input, unweighted combine
+};
+
 // Byte offsets of the workspace regions for one problem.
 // Words between the CTAs of the fused decode kernel: an epoch (word 0) and
 // one publication flag per CTA from word kSyncFlagsOffset on.
 constexpr int kSyncFlagsOffset = 32;
 constexpr int kMaxSyncCtas = 1024;
 constexpr int kSyncWords = kSyncFlagsOffset + kMaxSyncCtas;
+// Every workspace starts with the status word (a 256-byte region) and then
+// the synchronisation words, whatever the problem.
+constexpr size_t kStatusOffset = 0;
+constexpr size_t kSyncOffset = 256;
 
 struct Workspace {
   size_t status, sync, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles, mtiles_dn,
       n_mtiles_dn;
   size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
-  size_t xs, as, outacc;    // prefill: bf16 [P][H], bf16 hi/lo [P][2I], f32 [T][H]
+  size_t xs, af, a16, aexp, outacc;  // prefill: bf16 [P][H], f32 [P][I], f16 [P][I], i32 [P], f32 [T][H]
   size_t total;
   bool prefill;
 };
@@ -76,29 +89,58 @@ struct RouteOut {
 
 // Launch ``kern`` on ``s``; with ``pdl`` the launch may begin before the previous
 // kernel on the stream finishes (the kernel must call grid_dep_wait() before
-// reading that kernel's results).
+// reading that kernel's results); with ``cooperative`` every CTA of the grid is
+// resident at once, or the launch fails (for kernels whose CTAs wait on one
+// another).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                          Args... args) {
+                          bool cooperative, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
+
+// Bounded-wait settings of one call: the limit of every wait in its kernels
+// and, for tests of the give-up path only, extra CTAs the fused decode
+// kernel's cross-CTA wait expects beyond its grid (so that wait runs out).
+struct WaitSettings {
+  uint64_t limit_ns = kWaitLimitNs;
+  int extra_waiters = 0;
+};
+// Settings for the next call made from this host thread (moe_set_wait_limit);
+// taking them resets the hook to the defaults.
+WaitSettings take_wait_settings();
+
+// Copy the status word of workspace ``ws`` to *status, then clear it and the
+// synchronisation words (synchronises ``s``).
+int read_and_clear_status(uint8_t* ws, uint32_t* status, cudaStream_t s);
 
 // Benchmark timing hook (moe_set_timing_events): record the caller's event
 // before (end = false) or after (end = true) kernel ``index`` of this call.
 void timing_mark(int index, bool end, cudaStream_t s);
 
-cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const RouteOut& r, int make_mtiles,
-                         cudaStream_t s);
+cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const int32_t* emap, int G,
+                         const RouteOut& r, int make_mtiles, cudaStream_t s);
+
+cudaError_t launch_router_topk(const float* logits, int T, int G, int topk, int renorm, int32_t* ids, float* w,
+                               cudaStream_t s);
 
 cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, float* out_s,
                            long long n_groups, cudaStream_t s);
@@ -120,6 +162,8 @@ struct DecodeArgs {
   uint32_t* status;
   uint32_t* sync;         // [kSyncWords] epoch and per-CTA flags of the fused kernel
   int num_sms;
+  WaitSettings wait;
+  LayerOptions opt;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
@@ -137,10 +181,14 @@ struct PrefillArgs {
   void* out;
   RouteOut route;
   void* xs;       // bf16 [P][H]
-  void* as;       // bf16 [P][2I]: hi and lo parts of the activated intermediate
+  float* af;      // f32 [P][I]: the activated intermediate
+  void* a16;      // f16 [P][I]: the same, row i scaled by 2^aexp[i]
+  int32_t* aexp;  // [P]
   float* outacc;  // f32 [T][H]
   uint32_t* status;
   int num_sms;
+  uint64_t wait_ns;
+  LayerOptions opt;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);

@@ -67,3 +67,12 @@ extern "C" int moe_a16w4_mxfp4_noalloc(const moe_dims_t* d, const void* x, const
   return moe_a16w4_mxfp4(&dd, x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, scratch,
                          moe::kNoAllocScratchBytes, stream);
 }
+
+extern "C" int moe_noalloc_read_status(uint32_t* status, void* stream) {
+  if (!status) return MOE_ERR_NULL;
+  void* scratch = nullptr;
+  const int rc = moe::scratch_for_current_device(&scratch);
+  if (rc != MOE_OK) return rc;
+  return moe::read_and_clear_status(reinterpret_cast<uint8_t*>(scratch), status,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}

@@ -6,10 +6,11 @@
 // vLLM quantization/mxfp4 API page, gate_up ``w13`` then down ``w2``), laid
 // out for a dense contraction:
 //   gather:  xs[i] = x[token of sorted pair i]                 (bf16 rows)
-//   gemm1:   h = W13[e] xs^T, a = SiLU(h_gate) * h_up -> as    (a as bf16
-//            hi + lo parts, interleaved per 64 columns: 16 significant bits)
-//   gemm2:   y = W2[e] [a_hi + a_lo]^T, outacc[t] += topk_w * y
-//                                                              (fp32, red.add)
+//   gemm1:   h = W13[e] xs^T, a = SiLU(h_gate) * h_up -> af    (f32)
+//   convert: a16[i] = f16(af[i] * 2^aexp[i]), aexp[i] putting row i's largest
+//            |a| in [2^14, 2^15)                               (f16 rows)
+//   gemm2:   y = W2[e] a^T on f16 operands (weight row m scaled by 2^ew[m]),
+//            outacc[t] += topk_w * y * 2^-(ew + aexp)          (fp32, red.add)
 //   cast:    out = bf16(outacc)
 //
 // Work item = (expert, up to 192 (gate_up) or 128 (down) of its sorted rows,
@@ -28,29 +29,35 @@
 // the SM's tensor memory and shared memory.  Items go round-robin over all
 // CTAs.  Gate_up items are wider (192 rows) than down items (128) because
 // every item converts its 128 x K weight tile once: more rows per item means
-// fewer conversions per MMA; the down GEMM's two activation parts per step
-// leave shared memory for only 128.
+// fewer conversions per MMA.
 //
-// The pipeline runs in steps of 64 of K: gate_up issues 4 MMAs per step (one
-// 64-column tile of x), down issues 8 (the hi and the lo part of the
-// activated intermediate).  Shared memory holds only the activation ring
-// (four gate_up or three down steps deep, enough to cover the L2 latency of
-// the TMA loads); the converters read the packed weights and scales straight
-// from global memory, one group of four steps ahead, into registers.
+// The pipeline runs in steps of 64 of K, 4 MMAs per step (one 64-column
+// activation tile).  Shared memory holds only the activation ring (four
+// gate_up or six down steps deep, enough to cover the L2 latency of the TMA
+// loads); the converters read the packed weights and scales straight from
+// global memory, one group of four steps ahead, into registers.
+// Gate_up multiplies bf16 operands (weights exact in bf16, x bf16); down
+// multiplies f16 operands: the intermediate a has 11 significant bits there
+// (a bf16 a alone, 8 bits, is too coarse for the layer's tolerance) and the
+// weights are exact in f16 when their block scale lies within 2^36 of the
+// row's largest block scale (smaller blocks lose low bits, at 2^-37 of the
+// row's largest weights).
 // Warp roles per CTA:
-//   warp 0      lane 0: TMA of the step's rows x 64 bf16 activation tile(s)
+//   warp 0      lane 0: TMA of the step's rows x 64 activation tile
 //               (SWIZZLE_128B, the canonical K-major layout tcgen05 reads)
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-9   weight converters: thread = one weight row (its TMEM lane)
 //               and one of the step's two 32-element blocks; loads its 16
-//               packed bytes and its scale, converts them exactly to bf16
-//               (cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias, multiply by the
-//               block scale) and stores them into the step's tensor-memory
-//               weight stage with tcgen05.st
+//               packed bytes and its scale, converts them exactly (gate_up:
+//               bf16 by cvt.rn.f16x2.e2m1x2, f16 -> bf16 re-bias and the block
+//               scale; down: f16 times 2^(s - 127 + ew[row])) and stores them
+//               into the step's tensor-memory weight stage with tcgen05.st
 //               int4_per_group_32 weights: q exact to f16 by a mantissa
-//               trick, then bf16(fl32(q * s)) with the group's fp32 scale
+//               trick, then bf16(fl32(q * s)) (gate_up) or
+//               f16(q * f16(s * 2^ew[row])) (down)
 //   warps 10-13 epilogue: tcgen05.ld of the accumulator, SiLU gating (gemm1)
-//               or router-weighted scatter-add (gemm2), global stores
+//               or the exponent undo and router-weighted scatter-add (gemm2),
+//               global stores
 // Tensor memory per CTA (256 columns): two (gate_up) or four (down) 32-column
 // weight stages, then one accumulator of 192 (gate_up) or 128 (down) columns.
 #include <cuda.h>
@@ -69,13 +76,13 @@ constexpr int kGroupSteps = 4;                // steps per converter load group 
 constexpr uint32_t kTmemCols = 256;
 
 // Tile rows, pipeline depths, tensor-memory and shared-memory layout of one
-// CTA; gate_up activation stages hold one tile, down stages two (hi and lo).
+// CTA; an activation stage holds one tile.
 template <bool GATE_UP>
 struct TcLayout {
   static constexpr int kRows = GATE_UP ? kTcRowsUp : kTcRowsDown;  // MMA N, at most
-  static constexpr int kBoxBytes = kRows * 128;                   // one tile: kRows rows x 64 bf16
-  static constexpr int kActStages = GATE_UP ? 4 : 3;
-  static constexpr int kStageBytes = (GATE_UP ? 1 : 2) * kBoxBytes;
+  static constexpr int kBoxBytes = kRows * 128;                   // one tile: kRows rows x 64 16-bit values
+  static constexpr int kActStages = GATE_UP ? 4 : 6;
+  static constexpr int kStageBytes = kBoxBytes;
   static constexpr int kWStages = GATE_UP ? 2 : 4;
   static constexpr uint32_t kAccCol0 = kWStages * kWCols;         // accumulator columns [kAccCol0, +kRows)
   static_assert(kAccCol0 + kRows <= kTmemCols, "tensor memory budget");
@@ -83,7 +90,8 @@ struct TcLayout {
   // activation ring | mbarriers; + 1024 for aligning the base: two CTAs per
   // SM need at most 113 KB each
   static constexpr int kBarOff = kActStages * kStageBytes;
-  static constexpr int kSmemBytes = 1024 + kBarOff + 256;
+  static constexpr int kEwOff = kBarOff + 256;                    // down: [2][128] weight-row exponents
+  static constexpr int kSmemBytes = 1024 + kEwOff + 2 * kTcW * 4;
   static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -99,9 +107,13 @@ struct TcParams {
   const int32_t* sorted_pair;
   int topk;
   const float* topk_w;
-  uint16_t* act_out;  // gemm1: [P][2I] bf16, hi and lo parts per 64 columns
+  float* act_out;     // gemm1: [P][I] f32, the activated intermediate
+  const int32_t* aexp;  // gemm2: [P] power-of-two exponent of each f16 intermediate row
   float* outacc;      // gemm2: [T][H]
   uint32_t* status;
+  uint64_t wait_ns;   // limit of every bounded wait
+  const uint16_t* bias;  // bf16 [E][N] added to the outputs (gate_up: b13, down: b2), or null
+  int rwi;            // router weight on the input: gate_up scales h by it, down adds unweighted
 };
 
 // ------------------------------------------------------------------ tcgen05 / TMA helpers
@@ -131,12 +143,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A and B both bf16 (or both f16),
+// both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool bf16) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
-// D (tensor memory) (+)= A (tensor memory) * B (shared memory descriptor)^T.
+// D (tensor memory) (+)= A (tensor memory) * B (shared memory descriptor)^T,
+// kind::f16 (bf16 or f16 operands, as the instruction descriptor says).
 __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -194,12 +209,6 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ void red_add(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
-  uint16_t r;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
-  return r;
 }
 
 // Two exact E2M1 values as f16 (one packed byte) -> the same values times
@@ -269,6 +278,82 @@ __device__ __forceinline__ void dequant_block_int4(const uint4& q, float s, uint
   }
 }
 
+// 2^d as two f16 (both halves), d <= 15; d below -24 (smaller than every f16)
+// gives zero.
+__device__ __forceinline__ uint32_t f16x2_pow2(int d) {
+  uint32_t f = 0;
+  if (d >= -14) f = (uint32_t)(d + 15) << 10;
+  else if (d >= -24) f = 1u << (d + 24);
+  return f | (f << 16);
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 32 E2M1 values of one block with E8M0 scale s -> 16 words of two f16, the
+// values times 2^(s - 127 + ew): exact for s - 127 + ew >= -23 (the product of
+// a 2-significant-bit E2M1 value and a power of two stays on the f16 grid down
+// to its subnormals); below, rounded to the f16 grid (or zero).
+__device__ __forceinline__ void dequant_block_f16(const uint4& q, uint32_t s, int ew, uint4 (&out)[4]) {
+  const uint32_t f = f16x2_pow2((int)s - 127 + ew);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h0, h1, h2, h3;
+    e2m1x8_to_f16x8(w[i], h0, h1, h2, h3);
+    out[i] = make_uint4(f16x2_mul(h0, f), f16x2_mul(h1, f), f16x2_mul(h2, f), f16x2_mul(h3, f));
+  }
+}
+
+// 32 int4 values of one group with fp32 scale s -> 16 words of two f16:
+// f16(q * f16(s * 2^ew)): q is exact in f16, the scale is rounded to f16 once
+// (s * 2^ew itself is exact: a power-of-two scaling inside the float32 range)
+// and the product once more.
+__device__ __forceinline__ void dequant_block_int4_f16(const uint4& q, float s, int ew, uint4 (&out)[4]) {
+  const uint32_t sc = f32x2_to_f16x2(s * exp2_int(ew), s * exp2_int(ew));
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] ^ 0x88888888u;  // offset binary: q + 8
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = prmt(u, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
+      o[j] = f16x2_mul(f16x2_fma((v & 0x00F0000Fu) | 0x64006400u, 0x2C003C00u, 0xD480E408u), sc);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Exponent ew of one weight row for the f16 down GEMM: its largest weight
+// times 2^ew lies below 2^15 (6 * 2^13 for E2M1, 7 * 2^(floor(log2 smax) + 12)
+// for int4), clamped to [-126, 126].  ``sr`` is the row's Kb scales.
+template <WeightKind KIND>
+__device__ __forceinline__ int weight_row_exponent(const uint8_t* sr, int Kb) {
+  if (KIND == WeightKind::kMxfp4) {
+    uint32_t m = 0;
+    for (int i = 0; i < Kb; i += 16) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(sr + i));
+      m = __vmaxu4(m, __vmaxu4(__vmaxu4(u.x, u.y), __vmaxu4(u.z, u.w)));
+    }
+    m = __vmaxu4(m, m >> 16);
+    m = __vmaxu4(m, m >> 8);
+    return min(140 - (int)(m & 0xFFu), 126);
+  } else {
+    float m = 0.f;
+    for (int i = 0; i < Kb; i += 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(sr) + i / 4);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+    }
+    if (m == 0.f) return 0;
+    const int em = max((int)((__float_as_uint(m) >> 23) & 0xFFu), 1) - 127;  // floor(log2 m), subnormals as -126
+    return max(min(11 - em, 126), -126);
+  }
+}
+
 struct ItemInfo {
   int e, nt, row0, rows;
 };
@@ -306,7 +391,9 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
   uint64_t* acc_full = w_empty + kWStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ew_full = drain + 1;              // [2] down: an item's weight-row exponents written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ew_full + 2);
+  int32_t* ew_s = reinterpret_cast<int32_t*>(smem + Lay::kEwOff);  // [2][kTcW]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -322,6 +409,8 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
     mbar_init(drain, 1);
+    mbar_init(&ew_full[0], 4);
+    mbar_init(&ew_full[1], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -332,8 +421,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
   const uint32_t tmem_base = *tmem_slot;
 
   const int n_items = *p.n_mtiles * p.n_tiles;
-  // a step is 64 of K: gate_up one 64-column tile of x; down the 64-column hi
-  // and lo tiles of the activated intermediate (interleaved per 64 columns)
+  // a step is 64 of K: one 64-column tile of x (gate_up) or of the f16 intermediate (down)
   const int n_steps = p.K / 64;
 
   if (warp == 0) {
@@ -347,19 +435,14 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
         const ItemInfo it = nxt;  // this item's routing fields were loaded an item ahead
         if (item + (int)gridDim.x < n_items) nxt = decode_item<kRows>(p, item + gridDim.x);
         for (int step = 0; step < n_steps; ++step) {
-          if (used >= (uint32_t)kActStages && !mbar_wait(&act_empty[stage], phase ^ 1u, p.status)) {
+          if (used >= (uint32_t)kActStages && !mbar_wait(&act_empty[stage], phase ^ 1u, p.status, p.wait_ns)) {
             *abort_flag = 1;
             stop = true;
             break;
           }
           uint8_t* st = act_ring + stage * Lay::kStageBytes;
           mbar_arrive_expect_tx(&act_full[stage], Lay::kStageBytes);
-          if (GATE_UP) {
-            tma_load_2d(st, &tmap_a, 64 * step, it.row0, &act_full[stage]);
-          } else {
-            tma_load_2d(st, &tmap_a, 128 * step, it.row0, &act_full[stage]);
-            tma_load_2d(st + kBoxBytes, &tmap_a, 128 * step + 64, it.row0, &act_full[stage]);
-          }
+          tma_load_2d(st, &tmap_a, 64 * step, it.row0, &act_full[stage]);
           ++used;
           if (++stage == (uint32_t)kActStages) {
             stage = 0;
@@ -372,7 +455,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       for (uint32_t v = 0; v < (used < (uint32_t)kActStages ? used : (uint32_t)kActStages); ++v) {
         stage = stage == 0 ? kActStages - 1 : stage - 1;
         if (stage == (uint32_t)kActStages - 1) phase ^= 1u;
-        mbar_wait(&act_full[stage], phase, p.status);
+        mbar_wait(&act_full[stage], phase, p.status, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -387,9 +470,9 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       for (; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
         // the next item's routing fields, loaded a whole item ahead
         const ItemInfo nxt = item + (int)gridDim.x < n_items ? decode_item<kRows>(p, item + gridDim.x) : it;
-        const uint32_t idesc = idesc_bf16(kTcW, (it.rows + 15) & ~15);  // N: the rows rounded up to 16
+        const uint32_t idesc = idesc_f16kind(kTcW, (it.rows + 15) & ~15, GATE_UP);  // N: the rows rounded up to 16
         // the epilogue must have read the previous item's accumulator
-        if (j >= 1 && !mbar_wait(acc_empty, (j - 1) & 1u, p.status)) {
+        if (j >= 1 && !mbar_wait(acc_empty, (j - 1) & 1u, p.status, p.wait_ns)) {
           *abort_flag = 1;
           break;
         }
@@ -397,7 +480,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
         bool ok = true;
         for (int step = 0; step < n_steps; ++step) {
           if (!mbar_try_wait2(&w_full[ws], wph, &act_full[as], aph) &&
-              (!mbar_wait(&w_full[ws], wph, p.status) || !mbar_wait(&act_full[as], aph, p.status))) {
+              (!mbar_wait(&w_full[ws], wph, p.status, p.wait_ns) || !mbar_wait(&act_full[as], aph, p.status, p.wait_ns))) {
             ok = false;
             break;
           }
@@ -406,11 +489,6 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           const uint64_t b0 = sw128_desc(act0 + as * Lay::kStageBytes);
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_bf16_ta(d, a + 8 * k, b0 + 2 * k, idesc, (step > 0 || k > 0) ? 1u : 0u);
-          if (!GATE_UP) {
-            const uint64_t b1 = b0 + (kBoxBytes >> 4);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mma_bf16_ta(d, a + 8 * k, b1 + 2 * k, idesc, 1u);
-          }
           mma_commit(&act_empty[as]);
           mma_commit(&w_empty[ws]);
           if (++as == (uint32_t)kActStages) {
@@ -431,7 +509,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       }
       // all issued MMAs complete before TMEM is released
       mma_commit(drain);
-      mbar_wait(drain, 0, p.status);
+      mbar_wait(drain, 0, p.status, p.wait_ns);
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------------ weight converters
@@ -479,7 +557,18 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
       for (int i = 0; i < kGroupSteps; ++i) qb[i] = __ldg(reinterpret_cast<const uint4*>(wrow + 32 * i));
       load_scales(srow, 0, ns, nf);
     }
-    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x) {
+    uint32_t jj = 0;  // items of this CTA so far
+    for (int item = blockIdx.x; item < n_items && !*abort_flag && !stop; item += gridDim.x, ++jj) {
+      // down: this row's f16 exponent, handed to the epilogue thread of the
+      // same row (slot jj & 1: by the time an item two later is converted, the
+      // epilogue has finished this one, whose accumulator the MMAs of the item
+      // in between had to wait for)
+      const int ew = GATE_UP ? 0 : weight_row_exponent<KIND>(srow, Kb);
+      if (!GATE_UP && hk == 0) {
+        ew_s[(jj & 1u) * kTcW + L] = ew;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ew_full[jj & 1u]);
+      }
       // the following item's rows, for the loads issued during our last group
       const bool has_next = item + (int)gridDim.x < n_items;
       const uint8_t *wrow_n = wrow, *srow_n = srow;
@@ -499,12 +588,14 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           uint4 cv[4];
           if (KIND == WeightKind::kMxfp4) {
             const uint32_t s = ((i < 2 ? cs.x >> (8 * c) : cs.y >> (8 * (c - 4))) & 0xFFu);
-            dequant_block(qb[i], s, cv);
+            if (GATE_UP) dequant_block(qb[i], s, cv);
+            else dequant_block_f16(qb[i], s, ew, cv);
           } else {
-            dequant_block_int4(qb[i], cf[i], cv);
+            if (GATE_UP) dequant_block_int4(qb[i], cf[i], cv);
+            else dequant_block_int4_f16(qb[i], cf[i], ew, cv);
           }
           if (more) qb[i] = __ldg(reinterpret_cast<const uint4*>(wnext + 32 * i));
-          if (used >= (uint32_t)kWStages && !mbar_wait(&w_empty[ws], wph ^ 1u, p.status)) {
+          if (used >= (uint32_t)kWStages && !mbar_wait(&w_empty[ws], wph ^ 1u, p.status, p.wait_ns)) {
             *abort_flag = 1;
             stop = true;
             break;
@@ -531,23 +622,48 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     uint32_t j = 0;
     for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++j) {
       const ItemInfo it = decode_item<Lay::kRows>(p, item);
-      // down: token and router weight of rows lane, lane + 32, ... (loaded
-      // before the accumulator wait, handed out with shuffles below)
-      int tok[kRows / 32];
+      // token, router weight and (down) intermediate exponent of rows lane,
+      // lane + 32, ... (loaded before the accumulator wait, handed out with
+      // shuffles below): down always, gate_up for the router weight on the input
+      int tok[kRows / 32], aex[kRows / 32];
       float wgt[kRows / 32];
-      if (!GATE_UP) {
+      if (!GATE_UP || p.rwi) {
 #pragma unroll
         for (int c = 0; c < kRows / 32; ++c) {
           tok[c] = 0;
+          aex[c] = 0;
           wgt[c] = 0.f;
           if (32 * c + lane < it.rows) {
             const int pair = p.sorted_pair[it.row0 + 32 * c + lane];
             tok[c] = pair / p.topk;
-            wgt[c] = p.topk_w[pair];
+            wgt[c] = (GATE_UP || !p.rwi) ? p.topk_w[pair] : 1.f;
+            if (!GATE_UP) aex[c] = p.aexp[it.row0 + 32 * c + lane];
           }
         }
       }
-      if (!mbar_wait(acc_full, j & 1u, p.status)) {
+      // down: the f16 exponent of this thread's weight row, from its converter
+      int ewr = 0;
+      if (!GATE_UP) {
+        if (!mbar_wait(&ew_full[j & 1u], (j >> 1) & 1u, p.status, p.wait_ns)) {
+          *abort_flag = 1;
+          break;
+        }
+        ewr = ew_s[(j & 1u) * kTcW + 32 * q + lane];
+      }
+      // this lane's bias: gate_up the gate and up bias of its activation
+      // column, down the bias of its output row
+      float bias0 = 0.f, bias1 = 0.f;
+      if (p.bias) {
+        const uint16_t* b = p.bias + (size_t)it.e * p.N;
+        if (GATE_UP) {
+          const int j1 = 64 * it.nt + 16 * q + (lane & 15);
+          bias0 = bf16_lo(b[j1]);
+          bias1 = bf16_lo(b[p.I + j1]);
+        } else {
+          bias0 = bf16_lo(b[kTcW * it.nt + 32 * q + lane]);
+        }
+      }
+      if (!mbar_wait(acc_full, j & 1u, p.status, p.wait_ns)) {
         *abort_flag = 1;
         break;
       }
@@ -564,8 +680,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           // lanes 0-15: gate rows of activations 16q + lane, tokens c0..c0+15;
           // lanes 16-31: the matching up rows, tokens c0+16..c0+31
           const bool lo_half = lane < 16;
-          uint16_t* dst = p.act_out + (size_t)(it.row0 + c0 + (lo_half ? 0 : 16)) * (2 * p.I) + 128 * it.nt +
-                          16 * q + (lane & 15);
+          float* dst = p.act_out + (size_t)(it.row0 + c0 + (lo_half ? 0 : 16)) * p.I + 64 * it.nt + 16 * q + (lane & 15);
           const int nvalid = it.rows - c0 - (lo_half ? 0 : 16);
           // exchange in place: afterwards v[i] is the gate and v[16 + i] the up
           // value of this lane's token i (all shuffles first, then independent math)
@@ -575,48 +690,51 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
             if (lo_half) v[16 + i] = recv;
             else v[i] = recv;
           }
-          const size_t rs = 2 * (size_t)p.I;
-          // a = hi + lo with hi = bf16(a), lo = bf16(a - hi): 16 significant
-          // bits; all 16 values first, then the stores (predicated only in a
-          // partial chunk)
-          uint32_t hl[16];
+          const size_t rs = (size_t)p.I;
+          // all 16 values first, then the stores (predicated only in a partial chunk)
+          float av[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a = silu(__uint_as_float(v[i])) * __uint_as_float(v[16 + i]);
-            const uint32_t hi = f32_to_bf16_bits(a);
-            hl[i] = hi | ((uint32_t)f32_to_bf16_bits(a - __uint_as_float(hi << 16)) << 16);
+            float hg = __uint_as_float(v[i]), hu = __uint_as_float(v[16 + i]);
+            if (p.rwi) {
+              const float wt = __shfl_sync(0xffffffffu, wgt[c], (lo_half ? 0 : 16) + i);
+              hg *= wt;
+              hu *= wt;
+            }
+            av[i] = silu(hg + bias0) * (hu + bias1);
           }
           if (nvalid >= 16) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              dst[i * rs] = (uint16_t)hl[i];
-              dst[i * rs + 64] = (uint16_t)(hl[i] >> 16);
-            }
+            for (int i = 0; i < 16; ++i) dst[i * rs] = av[i];
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              if (i < nvalid) {
-                dst[i * rs] = (uint16_t)hl[i];
-                dst[i * rs + 64] = (uint16_t)(hl[i] >> 16);
-              }
-            }
+            for (int i = 0; i < 16; ++i)
+              if (i < nvalid) dst[i * rs] = av[i];
           }
         } else {
           float* dst = p.outacc + kTcW * it.nt + 32 * q + lane;
           const int nvalid = min(32, it.rows - c0);
+          // y = acc * 2^-(ew + aexp) in two power-of-two steps (each exponent
+          // within [-126, 126], the intermediate between acc and y)
+          auto undo = [&](float acc, int ea) {
+            const int k = ewr + ea, k1 = k >> 1;
+            return acc * exp2_int(-k1) * exp2_int(k1 - k);
+          };
           if (nvalid == 32) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int t = __shfl_sync(0xffffffffu, tok[c], i);
               const float wk = __shfl_sync(0xffffffffu, wgt[c], i);
-              red_add(dst + (size_t)t * p.H, wk * __uint_as_float(v[i]));
+              const int ea = __shfl_sync(0xffffffffu, aex[c], i);
+              red_add(dst + (size_t)t * p.H, wk * (undo(__uint_as_float(v[i]), ea) + bias0));
             }
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int t = __shfl_sync(0xffffffffu, tok[c], i);
               const float wk = __shfl_sync(0xffffffffu, wgt[c], i);
-              if (i < nvalid) red_add(dst + (size_t)t * p.H, wk * __uint_as_float(v[i]));
+              const int ea = __shfl_sync(0xffffffffu, aex[c], i);
+              if (i < nvalid) red_add(dst + (size_t)t * p.H, wk * (undo(__uint_as_float(v[i]), ea) + bias0));
             }
           }
         }
@@ -645,6 +763,47 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)i * H);
   for (int c = threadIdx.x; c < H / 8; c += blockDim.x) dst[c] = __ldg(src + c);
+}
+
+// Row i of the activated intermediate (f32) -> f16, scaled by 2^aexp[i] so
+// that the row's largest magnitude lies in [2^14, 2^15): every value within
+// 2^28 of it keeps 11 significant bits.  aexp is clamped to [-126, 126]; an
+// all-zero row gets 0.  One CTA of 256 threads per row, I <= 4096.
+__global__ void __launch_bounds__(256) act_to_f16_kernel(const float* __restrict__ af,
+                                                         const int32_t* __restrict__ n_valid, int I,
+                                                         uint16_t* __restrict__ a16, int32_t* __restrict__ aexp) {
+  __shared__ float s_max[8];
+  const int row = blockIdx.x;
+  if (row >= *n_valid) return;
+  const float4* src = reinterpret_cast<const float4*>(af + (size_t)row * I);
+  const int n4 = I / 4;
+  float4 v[4];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = threadIdx.x + 256 * i;
+    v[i] = c < n4 ? __ldcs(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = s_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, s_max[w]);
+  // floor(log2 m) from the exponent field (subnormal m counts as 2^-127)
+  const int lg = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+  const int ea = m > 0.f ? max(min(14 - lg, 126), -126) : 0;
+  const float sc = exp2_int(ea);
+  uint2* dst = reinterpret_cast<uint2*>(a16 + (size_t)row * I);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = threadIdx.x + 256 * i;
+    if (c < n4)
+      dst[c] = make_uint2(f32x2_to_f16x2(v[i].x * sc, v[i].y * sc), f32x2_to_f16x2(v[i].z * sc, v[i].w * sc));
+  }
+  if (threadIdx.x == 0) aexp[row] = ea;
 }
 
 __global__ void __launch_bounds__(256) cast_out_kernel(const float* __restrict__ acc, long long n4,
@@ -677,8 +836,8 @@ cudaError_t get_encoder(EncodeTiledFn* fn) {
   return cudaSuccess;
 }
 
-// bf16 [rows][K] row-major, box_rows x 64 boxes with 128-byte swizzle.
-cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+// 16-bit [rows][K] row-major (bf16 or f16), box_rows x 64 boxes with 128-byte swizzle.
+cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows, bool f16) {
   EncodeTiledFn enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
@@ -686,7 +845,8 @@ cudaError_t make_act_map(CUtensorMap* m, const void* base, long long rows, int K
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -707,9 +867,9 @@ cudaError_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaS
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   const long long P = (long long)a.T * a.topk;
   CUtensorMap map_x, map_a;
-  cudaError_t e = make_act_map(&map_x, a.xs, P, a.H, kTcRowsUp);
+  cudaError_t e = make_act_map(&map_x, a.xs, P, a.H, kTcRowsUp, false);
   if (e != cudaSuccess) return e;
-  e = make_act_map(&map_a, a.as, P, 2 * a.I, kTcRowsDown);
+  e = make_act_map(&map_a, a.a16, P, a.I, kTcRowsDown, true);
   if (e != cudaSuccess) return e;
 
   timing_mark(1, false, s);
@@ -734,14 +894,24 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.sorted_pair = a.route.sorted_pair;
   p.topk = a.topk;
   p.topk_w = a.topk_w;
-  p.act_out = reinterpret_cast<uint16_t*>(a.as);
+  p.act_out = a.af;
+  p.aexp = a.aexp;
   p.outacc = a.outacc;
   p.status = a.status;
+  p.wait_ns = a.wait_ns;
+  p.bias = a.opt.b13;
+  p.rwi = a.opt.rwi;
   timing_mark(2, false, s);
   e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, true>(map_x, p, 2 * a.num_sms, s)
                                    : launch_tc<WeightKind::kInt4, true>(map_x, p, 2 * a.num_sms, s);
   timing_mark(2, true, s);
   if (e != cudaSuccess) return e;
+
+  timing_mark(3, false, s);
+  act_to_f16_kernel<<<(unsigned)P, 256, 0, s>>>(a.af, a.route.offsets + a.E, a.I, reinterpret_cast<uint16_t*>(a.a16),
+                                                 a.aexp);
+  timing_mark(3, true, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if ((e = cudaMemsetAsync(a.outacc, 0, (size_t)a.T * a.H * sizeof(float), s)) != cudaSuccess) return e;
   TcParams p2 = p;
@@ -752,17 +922,18 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.n_tiles = a.H / kTcW;
   p2.mtiles = a.route.mtiles_dn;
   p2.n_mtiles = a.route.n_mtiles_dn;
-  timing_mark(3, false, s);
+  p2.bias = a.opt.b2;
+  timing_mark(4, false, s);
   e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, false>(map_a, p2, 2 * a.num_sms, s)
                                    : launch_tc<WeightKind::kInt4, false>(map_a, p2, 2 * a.num_sms, s);
-  timing_mark(3, true, s);
+  timing_mark(4, true, s);
   if (e != cudaSuccess) return e;
 
   const long long n4 = (long long)a.T * a.H / 4;
   const int grid = (int)((n4 + 255) / 256 < (long long)a.num_sms * 8 ? (n4 + 255) / 256 : (long long)a.num_sms * 8);
-  timing_mark(4, false, s);
+  timing_mark(5, false, s);
   cast_out_kernel<<<grid, 256, 0, s>>>(a.outacc, n4, reinterpret_cast<uint16_t*>(a.out));
-  timing_mark(4, true, s);
+  timing_mark(5, true, s);
   return cudaGetLastError();
 }
 

@@ -4,7 +4,8 @@
 // The fused MoE call of Mxfp4MoEMethod.apply (vLLM quantization/mxfp4 API page)
 // receives topk_ids[T, topk]; the grouped GEMMs need each expert's pairs
 // contiguous.  Pairs keep ascending flat index p = t*topk + k inside each
-// expert, ids outside [0, E) are dropped.  Besides counts/offsets/order this
+// expert, ids outside [0, E) are dropped (with an expert map, global ids are
+// first mapped to local ids, -1 for experts of other GPUs).  Besides counts/offsets/order this
 // kernel emits the list of active experts with their 8-pair group counts
 // (the weight-streaming kernels iterate over it) and, on request, the list of
 // 256-row M tiles per expert for the tensor-core kernels.
@@ -45,7 +46,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const int32_t* __restrict__ ids, int E, int T, int topk, RouteOut r, int make_mtiles) {
+    route_kernel(const int32_t* __restrict__ ids, int E, int T, int topk, const int32_t* __restrict__ emap, int G,
+                 RouteOut r, int make_mtiles) {
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;           // [E]
   int32_t* base = sm + E;      // [E]
@@ -56,14 +58,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
   for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
   // one pair per thread stays in a register when P fits one pass
-  const int my_e = tid < P ? ids[tid] : -1;
+  const int my_e = tid < P ? local_expert(ids, tid, emap, G, E) : -1;
   __syncthreads();
   if (P <= kRouteThreads) {
-    if ((unsigned)my_e < (unsigned)E) atomicAdd(&cnt[my_e], 1);
+    if (my_e >= 0) atomicAdd(&cnt[my_e], 1);
   } else {
     for (int p = tid; p < P; p += kRouteThreads) {
-      const int e = ids[p];
-      if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+      const int e = local_expert(ids, p, emap, G, E);
+      if (e >= 0) atomicAdd(&cnt[e], 1);
     }
   }
   __syncthreads();
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (int c0 = 0; c0 < P; c0 += kRouteThreads) {
       for (int i = tid; i < 32 * E; i += kRouteThreads) wcnt[i] = 0;
       const int p = c0 + tid;
-      const int e = p < P ? (c0 == 0 ? my_e : ids[p]) : -1;
+      const int e = p < P ? (c0 == 0 ? my_e : local_expert(ids, p, emap, G, E)) : -1;
       const bool valid = p < P && (unsigned)e < (unsigned)E;
       __syncthreads();
       const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
@@ -178,14 +180,87 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   for (int i = n_valid + tid; i < P; i += kRouteThreads) r.sorted_pair[i] = -1;
 }
 
+// Top-k routing from router logits, one warp per token (G <= 1024: each
+// lane holds up to 32 logits in registers).  Experts are selected by logit,
+// which orders them exactly as their softmax probabilities do; among equal
+// logits the lower id comes first.  Weights: exp(l - max) over the sum of
+// the selected ones (renormalised) or of all (softmax).
+constexpr int kRouterMaxExperts = 1024;
+constexpr int kRouterMaxTopk = 64;
+
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int G, int topk,
+                                                          int renorm, int32_t* __restrict__ ids,
+                                                          float* __restrict__ w) {
+  const int t = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = logits + (size_t)t * G;
+  float v[kRouterMaxExperts / 32];
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kRouterMaxExperts / 32; ++j) {
+    const int i = lane + 32 * j;
+    v[j] = i < G ? row[i] : -INFINITY;
+    m = fmaxf(m, v[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float all = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRouterMaxExperts / 32; ++j)
+    if (lane + 32 * j < G) all += expf(v[j] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) all += __shfl_xor_sync(0xffffffffu, all, o);
+  uint32_t taken = 0;           // bit j: logit j of this lane already selected
+  float ek[kRouterMaxTopk / 32] = {0.f, 0.f};  // exp(l - max) of selection k, kept by lane k % 32
+  for (int k = 0; k < topk; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < kRouterMaxExperts / 32; ++j) {
+      const int i = lane + 32 * j;
+      if (i < G && !((taken >> j) & 1u) && (v[j] > bv || bi == 0x7FFFFFFF)) {
+        bv = v[j];
+        bi = i;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == (k & 31)) ek[k >> 5] = expf(bv - m);
+    if (lane == 0) ids[(size_t)t * topk + k] = bi;
+  }
+  float sel = ek[0] + ek[1];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
+  const float den = renorm ? sel : all;
+  for (int k = lane; k < topk; k += 32) w[(size_t)t * topk + k] = __fdiv_rn(ek[k >> 5], den);
+}
+
 }  // namespace
 
-cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const RouteOut& r, int make_mtiles,
-                         cudaStream_t s) {
+cudaError_t launch_router_topk(const float* logits, int T, int G, int topk, int renorm, int32_t* ids, float* w,
+                               cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const int blocks = (T + warps_per_block - 1) / warps_per_block;
+  router_topk_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(logits, T, G, topk, renorm, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const int32_t* emap, int G,
+                         const RouteOut& r, int make_mtiles, cudaStream_t s) {
   const size_t smem = (size_t)34 * E * sizeof(int32_t);
   cudaError_t err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  route_kernel<<<1, kRouteThreads, smem, s>>>(topk_ids, E, T, topk, r, make_mtiles);
+  route_kernel<<<1, kRouteThreads, smem, s>>>(topk_ids, E, T, topk, emap, G, r, make_mtiles);
   return cudaGetLastError();
 }
 

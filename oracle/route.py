@@ -59,6 +59,35 @@ def route(topk_ids: np.ndarray, E: int, expert_map=None):
     return counts, offsets, sorted_pair, pair_pos
 
 
+def router_topk(logits: np.ndarray, topk: int, renormalize: bool = True):
+    """Top-k routing from router logits, float64.
+
+    The Mxfp4MoEMethod page's ``apply_monolithic`` hands the kernel
+    ``router_logits`` and lets it choose each token's experts; the pages print
+    no scoring formula.  The plain reading used here (the one that turns the
+    logits into the top-k ids and weights ``apply`` takes): p = softmax over
+    the experts of each token's logits; keep the ``topk`` largest p, ties to
+    the lower expert id; with ``renormalize`` the kept p are divided by their
+    sum.  Grouped top-k, a score-correction bias and a routed scaling factor
+    are not modelled.
+
+    Returns ``ids int32[T, topk]`` (in decreasing p) and ``w float32[T, topk]``
+    (the float64 result rounded to float32 once).
+    """
+    L = np.asarray(logits, dtype=np.float64)
+    T, G = L.shape
+    ids = np.zeros((T, topk), dtype=np.int32)
+    w = np.zeros((T, topk), dtype=np.float64)
+    for t in range(T):
+        e = np.exp(L[t] - L[t].max())
+        p = e / e.sum()
+        # decreasing p; among equal p the lower id first
+        order = sorted(range(G), key=lambda i: (-p[i], i))[:topk]
+        ids[t] = order
+        w[t] = p[order] / p[order].sum() if renormalize else p[order]
+    return ids, w.astype(np.float32)
+
+
 def active_experts(counts: np.ndarray) -> np.ndarray:
     """Ids of experts that received at least one pair, ascending."""
     return np.nonzero(np.asarray(counts) > 0)[0].astype(np.int32)

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_error_strings(lib):
-    assert lib.moe_abi_version() == 100
+    assert lib.moe_abi_version() == 101
     assert lib.moe_error_string(0) == b"ok"
     assert b"SwiGLU" in lib.moe_error_string(-4)
 
@@ -81,3 +81,36 @@ def test_argument_errors_are_host_side(lib):
     n = lib.requant_mxfp4_to_int4g32(2, 4, 48, None, None, None, None, 8, None)
     assert n == -2  # K % 32
     assert lib.requant_mxfp4_to_int4g32(2, 4, 64, None, None, None, None, 8, None) == -1
+    # the bounded-wait hook rejects a zero limit and out-of-range extra waiters
+    assert lib.moe_set_wait_limit(0, 0) == -2
+    assert lib.moe_set_wait_limit(1000, -1) == -2
+    assert lib.moe_set_wait_limit(1000, 65) == -2
+    assert lib.moe_noalloc_read_status(None, None) == -1
+
+
+def test_router_errors_are_host_side(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.moe_router_topk(p, 4, 1025, 8, 1, p, p, None) == -2  # more than 1024 experts
+    assert lib.moe_router_topk(p, 4, 32, 65, 1, p, p, None) == -2  # top-k above 64
+    assert lib.moe_router_topk(p, 4, 8, 9, 1, p, p, None) == -2  # top-k above the experts
+    assert lib.moe_router_topk(p, 4, 32, 4, 2, p, p, None) == -2  # renormalize not 0 / 1
+    assert lib.moe_router_topk(None, 4, 32, 4, 1, p, p, None) == -1
+    assert lib.moe_router_topk(ctypes.c_void_p(18), 4, 32, 4, 1, p, p, None) == -3
+    assert lib.moe_router_topk(None, 0, 32, 4, 1, None, None, None) == 0  # T = 0: nothing to do
+
+
+def test_option_errors_are_host_side(lib):
+    from mxfp4_weight_only_gb300 import MoeOptions, dims
+
+    d = dims(8, 256, 128, 2, 4)
+    p = ctypes.c_void_p(16)
+
+    def call(opt):
+        return lib.moe_a16w4_mxfp4_ex(ctypes.byref(d), p, p, p, p, p, p, p, ctypes.byref(opt), p,
+                                      ctypes.c_void_p(256), 1 << 30, None)
+
+    assert call(MoeOptions(None, None, None, 0, 2)) == -2  # router_weight_on_input not 0 / 1
+    assert call(MoeOptions(None, None, 64, 0, 0)) == -2  # a map with no entries
+    assert call(MoeOptions(None, None, 64, (1 << 20) + 1, 0)) == -2
+    assert call(MoeOptions(17, None, None, 0, 0)) == -3  # bias not 2-byte aligned
+    assert call(MoeOptions(None, None, 66, 8, 0)) == -3  # map not 4-byte aligned

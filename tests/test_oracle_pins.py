@@ -180,6 +180,46 @@ def test_route_with_expert_map_matches_bruteforce(G, E):
     assert list(c) == bc and list(o) == bo and list(sp) == bsp and list(pos) == bpos
 
 
+def test_router_topk_against_scipy_softmax_and_bruteforce():
+    # scipy's softmax, then a brute-force selection: k passes, each taking the
+    # largest remaining probability (the first such id on ties)
+    from scipy.special import softmax
+
+    g = np.random.default_rng(41)
+    logits = g.standard_normal((6, 40)).astype(np.float32)
+    logits[2, [3, 9, 17]] = 2.5  # a three-way tie at the top
+    for renorm in (True, False):
+        ids, w = route.router_topk(logits, 5, renormalize=renorm)
+        for t in range(logits.shape[0]):
+            p = softmax(logits[t].astype(np.float64))
+            left = list(range(logits.shape[1]))
+            want = []
+            for _ in range(5):
+                best = max(left, key=lambda i: (p[i], -i))
+                want.append(best)
+                left.remove(best)
+            assert list(ids[t]) == want
+            pw = p[want] / (p[want].sum() if renorm else 1.0)
+            assert np.allclose(w[t], pw.astype(np.float32), rtol=1e-6, atol=0)
+    assert list(route.router_topk(logits, 5)[0][2][:3]) == [3, 9, 17]
+
+
+def test_router_topk_invariants():
+    g = np.random.default_rng(42)
+    logits = g.standard_normal((5, 16))
+    ids, w = route.router_topk(logits, 4)
+    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-6)
+    assert np.all(np.diff(w, axis=1) <= 0)  # decreasing weights
+    ids2, w2 = route.router_topk(logits + 7.25, 4)  # softmax is shift invariant
+    assert np.array_equal(ids, ids2) and np.allclose(w, w2, rtol=1e-6)
+    ids_all, _ = route.router_topk(logits, 16)  # k = all experts: a permutation
+    assert all(sorted(r) == list(range(16)) for r in ids_all)
+    one_hot = np.full((2, 8), -30.0)
+    one_hot[0, 5] = one_hot[1, 2] = 30.0
+    ids1, w1 = route.router_topk(one_hot, 1, renormalize=False)
+    assert list(ids1[:, 0]) == [5, 2] and np.allclose(w1, 1.0)
+
+
 def test_route_empty():
     c, o, sp, pos = route.route(np.zeros((0, 4), np.int32), 8)
     assert c.sum() == 0 and o[-1] == 0 and sp.size == 0 and pos.size == 0

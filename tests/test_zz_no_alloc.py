@@ -80,6 +80,13 @@ def _noalloc(lib, shape, t):
     return out
 
 
+def _noalloc_status(lib):
+    v = ctypes.c_uint32(0xFFFFFFFF)
+    rc = lib.moe_noalloc_read_status(ctypes.byref(v), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    return v.value
+
+
 def _f64(t):
     return formats.bf16_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))
 
@@ -97,6 +104,22 @@ def test_noalloc_matches_regular_entry_point_twice(lib, shape_seed):
     torch.cuda.synchronize()
     assert_moe_close(got, ref)
     assert_moe_close(got2, ref2)
+    assert _noalloc_status(lib) == 0
+
+
+def test_noalloc_wait_give_up_is_reported_and_cleared(lib):
+    # a bounded wait that runs out (1 ms limit, one CTA expected beyond the
+    # grid) is recorded in the array's status word; reading it clears the word
+    # and the synchronisation words, and the next call is correct again
+    shape, a = _problem(2, 8, 256, 128, 4, 2)
+    ref = _f64(_regular(lib, shape, a))
+    assert lib.moe_set_wait_limit(ctypes.c_uint64(1_000_000), 1) == 0
+    _noalloc(lib, shape, a)
+    torch.cuda.synchronize()
+    assert _noalloc_status(lib) == 1  # MOE_STATUS_WAIT_TIMEOUT
+    got = _f64(_noalloc(lib, shape, a))
+    assert_moe_close(got, ref)
+    assert _noalloc_status(lib) == 0
 
 
 def test_noalloc_rejects_oversized_problem(lib):
