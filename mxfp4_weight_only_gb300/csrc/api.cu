@@ -98,7 +98,9 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
   // small decode batches are grouped inside the decode kernels
   const bool route_kernel = L.prefill || (long long)d->T * d->topk > kMaxLocalRoutePairs;
   timing_mark(0, false, s);
-  if (route_kernel && launch_route(ids, d->E, d->T, d->topk, opt.emap, opt.G, r, L.prefill ? 1 : 0, s) != cudaSuccess)
+  if (route_kernel && launch_route(ids, d->E, d->T, d->topk, opt.emap, opt.G, r, L.prefill ? 1 : 0, s,
+                                   reinterpret_cast<int32_t*>(ws + L.rhist),
+                                   reinterpret_cast<int32_t*>(ws + L.rrank)) != cudaSuccess)
     return MOE_ERR_CUDA;
   timing_mark(0, true, s);
   cudaError_t e;
@@ -212,6 +214,9 @@ Workspace workspace_layout(const moe_dims_t* d, WeightKind kind) {
   L.n_mtiles = o; o = align256(o + 4);
   L.mtiles_dn = o; o = align256(o + 4 * (P / kTcRowsDown + E + 1));
   L.n_mtiles_dn = o; o = align256(o + 4);
+  // scratch of the two-kernel grouping of large batches
+  L.rhist = o; o = align256(o + (route_two_pass((long long)P) ? 4 * ((P + 1023) / 1024) * E : 0));
+  L.rrank = o; o = align256(o + (route_two_pass((long long)P) ? 4 * P : 0));
   if (L.prefill) {
     L.xs = o; o = align256(o + 2 * P * H);
     L.af = o; o = align256(o + 4 * P * I);

@@ -49,15 +49,7 @@ constexpr int kRedFloats = kConsumerWarps * kRows * kGroup;  // one reduction bu
 constexpr int kRedBufs = 3;                                  // reduction ring depth
 static_assert(kGroup == kMoeGroup, "routing and the decode kernels must agree on the group size");
 
-// Index of consumer warp w's partial sum for (weight row, pair column) in a
-// reduction buffer: column-major per warp (a column's 32 rows contiguous, so
-// the epilogue reads only the columns of pairs that exist), rows XOR-swizzled
-// by the column pair so that the consumers' stores (lanes = 8 rows x 4 column
-// pairs) hit 32 different banks.
-__device__ __forceinline__ int red_idx(int w, int row, int col) {
-  return w * (kRows * kGroup) + col * kRows + (row ^ (8 * ((col >> 1) & 3)));
-}
-static_assert(kRows == 32 && kGroup == 8, "reduction buffer swizzle");
+
 // Batches of at most kLocalRoute pairs are grouped by every CTA itself, in
 // shared memory, at the start of both kernels: no routing kernel runs before
 // them.  Region: active experts, their first sorted position, their group
@@ -205,10 +197,16 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   }
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  // power of two taking the range's largest magnitude into [2^14, 2^15) --
+  // or 1 when it already lies in [2^-4, 2^15), and the kernel skips the undo
+  // multiplies.  Unscaled, values of 2^-14 and more keep f16's 11 bits (bf16
+  // inputs from 2^-17 on are exact) and smaller ones are rounded to the f16
+  // subnormal grid, an error of at most 2^-25 each: summed over a K of 4096,
+  // 2^-9 of the range's largest value.
   int ex = 0;
   if (mx > 0.f) {
     const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
-    ex = min(max(14 - lg, -126), 126);
+    ex = (lg >= -4 && lg <= 14) ? 0 : min(max(14 - lg, -126), 126);
   }
   const float sc = exp2_int(ex);
 #pragma unroll
@@ -572,63 +570,129 @@ __device__ void producer_drain(const CtaSmem& c, int S, RingPos ring, uint32_t* 
   }
 }
 
-// Epilogue warp: sums the consumer warps' partials of each unit over the
-// pair columns that exist and writes the results (gate_up: SiLU(h_gate) *
-// h_up into abuf; down: per-pair rows into ybuf) while the consumers go on
-// with the next units.
+// Epilogue warp: sums the consumer warps' partials of each unit (lane = one
+// of 8 pair columns x 4 of the unit's rows per pass) and writes the results
+// (gate_up: SiLU(h_gate) * h_up into abuf; down: per-pair rows into ybuf)
+// while the consumers go on with the next units.  (Reducing only the columns
+// of pairs that exist, from a column-major buffer, measured slower from 16
+// tokens on: its per-column add chains run one after another.)
 template <bool GATE_UP>
 __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
                              RingPos& rr) {
   const int lane = threadIdx.x & 31;
+  const int col = lane % kGroup;  // this lane's pair column in every pass
   UnitCursor cur;
   if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
   int cur_e = -1, cur_grp = -1;
-  // lane < nv: its pair column's pair and router weight
-  int my_pair = -1;
-  float my_w = 0.f;
+  int my_pair = -1;   // the pair of this lane's column (-1: none)
+  float my_w = 0.f;   // its router weight (gate_up with the weight on the input)
   for (int u = r.u0; u < r.u1; ++u) {
     if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
     const int d = cur.d, grp = cur.grp, j = cur.j;
     const int e = gr.act[d];
     const int base = gr.base(d, e);
     const int npairs = gr.end(d, e) - base;
-    const int nv = min(kGroup, npairs - grp * kGroup);  // pair columns that exist
     if (e != cur_e || grp != cur_grp) {
       cur_e = e;
       cur_grp = grp;
-      my_pair = lane < nv ? gr.spair[base + grp * kGroup + lane] : -1;
+      const int slot = grp * kGroup + col;
+      my_pair = slot < npairs ? gr.spair[base + slot] : -1;
       my_w = (GATE_UP && p.rwi && my_pair >= 0) ? p.topk_w[my_pair] : 0.f;
     }
-    // this lane's output row of the unit: gate_up lanes 0-15 gate rows, 16-31 up rows
-    const int orow = GATE_UP ? (lane < kRows / 2 ? (kRows / 2) * j + lane : p.I + (kRows / 2) * j + lane - kRows / 2)
-                             : kRows * j + lane;
-    const float bias = p.bias ? bf16_lo(p.bias[(size_t)e * p.N + orow]) : 0.f;
     if (!mbar_wait(&c.red_full[rr.slot], rr.parity, p.status, p.wait_ns)) {
       *c.abort_flag = 1;
       return;
     }
     const float* rb = c.red + rr.slot * kRedFloats;
-    for (int cc = 0; cc < nv; ++cc) {
-      float v = 0.f;
+    const uint16_t* bias = p.bias ? p.bias + (size_t)e * p.N : nullptr;
+    if (GATE_UP) {
+      constexpr int kOut = kRows / 2;  // activated outputs per unit
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) v += rb[red_idx(w, lane, cc)];
-      if (GATE_UP) {
-        // h = (router weight) * W13 x + b13: the router weight on the input
-        // scales the GEMM's output exactly as it would scale x
-        if (p.rwi) v *= __shfl_sync(0xffffffffu, my_w, cc);
-        v += bias;
-        // lanes 0-15 hold the gate rows of the unit's 16 outputs, lanes 16-31 the up rows
-        const float hu = __shfl_down_sync(0xffffffffu, v, 16);
-        if (lane < kRows / 2)
-          p.dst[(size_t)(base + grp * kGroup + cc) * p.I + (kRows / 2) * j + lane] = silu(v) * hu;
-      } else {
-        const int pair = __shfl_sync(0xffffffffu, my_pair, cc);
-        p.dst[(size_t)pair * p.N + kRows * j + lane] = v + bias;
+      for (int q = 0; q < kOut * kGroup / 32; ++q) {
+        const int row = (lane + 32 * q) / kGroup;
+        float hg = 0.f, hu = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          hg += rb[w * kRows * kGroup + row * kGroup + col];
+          hu += rb[w * kRows * kGroup + (row + kOut) * kGroup + col];
+        }
+        if (my_pair >= 0) {
+          // h = (router weight) * W13 x + b13: the weight on the input scales
+          // the GEMM's output exactly as it would scale x
+          if (p.rwi) {
+            hg *= my_w;
+            hu *= my_w;
+          }
+          if (bias) {
+            hg += bf16_lo(bias[kOut * j + row]);
+            hu += bf16_lo(bias[p.I + kOut * j + row]);
+          }
+          p.dst[(size_t)(base + grp * kGroup + col) * p.I + kOut * j + row] = silu(hg) * hu;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kRows * kGroup / 32; ++q) {
+        const int row = (lane + 32 * q) / kGroup;
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + row * kGroup + col];
+        if (my_pair >= 0) {
+          if (bias) y += bf16_lo(bias[kRows * j + row]);
+          p.dst[(size_t)my_pair * p.N + kRows * j + row] = y;
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.red_empty[rr.slot]);
     rr.advance(kRedBufs);
+  }
+}
+
+// One consumer warp's part of one unit: its blocks [wb0, wb0 + cnt) of the
+// unit's 32 weight rows (two m16n8k16 tiles) times the activation fragments,
+// two blocks at a time, block scale applied to each block's fp32 partial sum.
+// With FOLD the scale is multiplied by each pair column's power-of-two undo
+// first, so the partial sums stay at the magnitude of the result (no float32
+// overflow for large block scales with tiny, up-scaled activations).
+template <WeightKind KIND, int NBW, bool FOLD>
+__device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t* sw, const uint8_t* ss, int wb0,
+                                              int cnt, int g, int t, const uint32_t (&xf)[NBW][4],
+                                              const float (&inv)[2], float (&acc)[kTiles][4]) {
+#pragma unroll
+  for (int tl = 0; tl < kTiles; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int bb = 0; bb < NBW; bb += 2) {
+    if (bb < cnt) {
+      const int b = wb0 + bb;
+#pragma unroll
+      for (int tl = 0; tl < kTiles; ++tl) {
+        const int row = 16 * tl + g;
+        float sc[2][2];  // [row / row+8][block b / b+1]
+        load_scales2<KIND>(ss, p.srow_bytes, row, b, sc);
+        float m[2][2][2];  // [row / row+8][block][column 2t / 2t+1]
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (FOLD) mul_f32x2_bcast(m[r2][h][0], m[r2][h][1], sc[r2][h], inv[0], inv[1]);
+            else m[r2][h][0] = m[r2][h][1] = sc[r2][h];
+          }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint8_t* rg = sw + row * p.row_stride + (b + h) * 16 + 4 * t;
+          uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+          weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg), a0, a1, a2, a3);
+          weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg + 8 * p.row_stride), c0, c1, c2, c3);
+          float dd[4];
+          mma_f16_16816(dd, a0, c0, a1, c1, xf[bb + h][0], xf[bb + h][1], zero);
+          mma_f16_16816(dd, a2, c2, a3, c3, xf[bb + h][2], xf[bb + h][3], dd);
+          fma_f32x2(acc[tl][0], acc[tl][1], m[0][h][0], m[0][h][1], dd[0], dd[1]);
+          fma_f32x2(acc[tl][2], acc[tl][3], m[1][h][0], m[1][h][1], dd[2], dd[3]);
+        }
+      }
+    }
   }
 }
 
@@ -648,7 +712,8 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
   const int cnt = min(nbw, nb - wb0);
 
   uint32_t xf[NBW][4];
-  float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1 (folded into the block scales)
+  float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1
+  bool fold = false;  // some column of this warp scaled: undo folded into the block scales
   int cur_e = -1, cur_grp = -1;
   UnitCursor cur;
   if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
@@ -661,6 +726,7 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
     const int npairs = gr.end(d, e) - base;
     if (e != cur_e || grp != cur_grp) {
       load_frags<KIND, GATE_UP, NBW>(p, gr.spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
+      fold = __any_sync(0xffffffffu, inv[0] != 1.f || inv[1] != 1.f);
       cur_e = e;
       cur_grp = grp;
     }
@@ -671,43 +737,11 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
     const uint8_t* sw = c.stages + (size_t)wr.slot * p.stage_bytes;
     const uint8_t* ss = sw + kRows * p.row_stride;
 
-    // ---- main loop over this warp's 32-element blocks, two at a time
+    // ---- main loop over this warp's 32-element blocks (fold: the
+    // activations were scaled, so their undo joins the block scales)
     float acc[kTiles][4];
-#pragma unroll
-    for (int tl = 0; tl < kTiles; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
-    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int bb = 0; bb < NBW; bb += 2) {
-      if (bb < cnt) {
-        const int b = wb0 + bb;
-#pragma unroll
-        for (int tl = 0; tl < kTiles; ++tl) {
-          const int row = 16 * tl + g;
-          float sc[2][2];  // [row / row+8][block b / b+1]
-          load_scales2<KIND>(ss, p.srow_bytes, row, b, sc);
-          // block scale times each pair column's power-of-two undo: the partial
-          // sums stay at the magnitude of the result (no float32 overflow for
-          // large block scales with tiny, up-scaled activations)
-          float m[2][2][2];  // [row / row+8][block][column 2t / 2t+1]
-#pragma unroll
-          for (int r2 = 0; r2 < 2; ++r2)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) mul_f32x2_bcast(m[r2][h][0], m[r2][h][1], sc[r2][h], inv[0], inv[1]);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint8_t* rg = sw + row * p.row_stride + (b + h) * 16 + 4 * t;
-            uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-            weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg), a0, a1, a2, a3);
-            weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg + 8 * p.row_stride), c0, c1, c2, c3);
-            float dd[4];
-            mma_f16_16816(dd, a0, c0, a1, c1, xf[bb + h][0], xf[bb + h][1], zero);
-            mma_f16_16816(dd, a2, c2, a3, c3, xf[bb + h][2], xf[bb + h][3], dd);
-            fma_f32x2(acc[tl][0], acc[tl][1], m[0][h][0], m[0][h][1], dd[0], dd[1]);
-            fma_f32x2(acc[tl][2], acc[tl][3], m[1][h][0], m[1][h][1], dd[2], dd[3]);
-          }
-        }
-      }
-    }
+    if (fold) unit_mainloop<KIND, NBW, true>(p, sw, ss, wb0, cnt, g, t, xf, inv, acc);
+    else unit_mainloop<KIND, NBW, false>(p, sw, ss, wb0, cnt, g, t, xf, inv, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.empty[wr.slot]);
     wr.advance(S);
@@ -717,14 +751,14 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
       *c.abort_flag = 1;
       return;
     }
-    float* rw = c.red + rr.slot * kRedFloats;
+    // (the activations' undo is in the partial sums already: folded into the
+    // block scales, or 1 when no column was scaled)
+    float* rw = c.red + rr.slot * kRedFloats + warp * (kRows * kGroup);
 #pragma unroll
     for (int tl = 0; tl < kTiles; ++tl) {
       const int row = 16 * tl + g;
-      rw[red_idx(warp, row, 2 * t)] = acc[tl][0];
-      rw[red_idx(warp, row, 2 * t + 1)] = acc[tl][1];
-      rw[red_idx(warp, row + 8, 2 * t)] = acc[tl][2];
-      rw[red_idx(warp, row + 8, 2 * t + 1)] = acc[tl][3];
+      *reinterpret_cast<float2*>(rw + row * kGroup + 2 * t) = make_float2(acc[tl][0], acc[tl][1]);
+      *reinterpret_cast<float2*>(rw + (row + 8) * kGroup + 2 * t) = make_float2(acc[tl][2], acc[tl][3]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.red_full[rr.slot]);

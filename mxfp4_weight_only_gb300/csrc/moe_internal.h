@@ -59,7 +59,7 @@ constexpr size_t kSyncOffset = 256;
 
 struct Workspace {
   size_t status, sync, counts, offsets, active, n_active, gprefix, sorted_pair, pair_pos, mtiles, n_mtiles, mtiles_dn,
-      n_mtiles_dn;
+      n_mtiles_dn, rhist, rrank;
   size_t abuf, ybuf;        // decode: f32 [P][I], f32 [P][H]
   size_t xs, af, a16, aexp, outacc;  // prefill: bf16 [P][H], f32 [P][I], f16 [P][I], i32 [P], f32 [T][H]
   size_t total;
@@ -136,8 +136,15 @@ int read_and_clear_status(uint8_t* ws, uint32_t* status, cudaStream_t s);
 // before (end = false) or after (end = true) kernel ``index`` of this call.
 void timing_mark(int index, bool end, cudaStream_t s);
 
+// Pairs above which (up to kRouteTwoPassMax) the grouping runs as two kernels
+// over chunks of 1024 pairs (per-chunk counts and ranks, then placement);
+// ``hist`` [ceil(P / 1024)][E] and ``rank`` [P] are their scratch (null: one
+// CTA sorts everything).
+constexpr long long kRouteTwoPassMax = 1ll << 20;
+bool route_two_pass(long long P);
 cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const int32_t* emap, int G,
-                         const RouteOut& r, int make_mtiles, cudaStream_t s);
+                         const RouteOut& r, int make_mtiles, cudaStream_t s, int32_t* hist = nullptr,
+                         int32_t* rank = nullptr);
 
 cudaError_t launch_router_topk(const float* logits, int T, int G, int topk, int renorm, int32_t* ids, float* w,
                                cudaStream_t s);

@@ -12,9 +12,13 @@
 // normal float32 range every element is c * 2^(s-127) and the group maximum is
 // cmax * 2^(s-127), so fl32(w / fl32(amax / 7)) equals
 // fl32(c / fl32(cmax / 7)) -- the power of two cancels exactly.  The quotient
-// therefore depends only on the two codes, and a 8x8 table of q, built with
-// the same IEEE round-to-nearest divisions at kernel start, replaces the 32
-// divisions; likewise fl32(amax / 7) = fl32(cmax / 7) * 2^(s-127).  Groups whose scale byte puts values near the subnormal range or
+// therefore depends only on the two codes: tables built at kernel start with
+// the same IEEE round-to-nearest divisions give, per cmax, the output byte of
+// every packed input byte (two signed codes), so a group costs sixteen
+// shared-memory byte loads instead of 32 divisions (an earlier version
+// applied an 8-entry table four nibbles at a time with byte permutes and a
+// separate sign select: 223 instructions per group, ALU-bound); likewise
+// fl32(amax / 7) = fl32(cmax / 7) * 2^(s-127).  Groups whose scale byte puts values near the subnormal range or
 // near overflow take the per-element division path, so results are bit-exact
 // for every scale byte in [0, 252].
 #include "common.cuh"
@@ -37,27 +41,20 @@ __device__ __forceinline__ float e2m1_mag(uint32_t c) {
   return __uint_as_float(c >= 2u ? normal : (c ? 0x3F000000u : 0u));
 }
 
-// 4 output bytes (int4 codes of elements 0..3 of ``sel`` nibbles) via byte permutes.
-// pos/neg: 8-entry tables (two words each) of q and (-q)&15 by magnitude code.
-__device__ __forceinline__ uint32_t lookup4(uint32_t nib4, uint32_t pos0, uint32_t pos1, uint32_t neg0,
-                                            uint32_t neg1) {
-  const uint32_t mags = nib4 & 0x7777u;
-  const uint32_t a = prmt(pos0, pos1, mags);
-  const uint32_t b = prmt(neg0, neg1, mags);
-  // selector (sign bit, index 4): sign 0 copies byte 4 (0x80), sign 1 replicates its
-  // top bit (0xFF): a per-byte select mask for the negated values.
-  const uint32_t ssel = (nib4 & 0x8888u) | 0x4444u;
-  const uint32_t m = prmt(0u, 0x80808080u, ssel);
-  return (a & ~m) | (b & m);
+// One packed word (four bytes, eight E2M1 codes) -> its four output bytes
+// (eight int4 codes) through the byte table of the group's largest code.
+__device__ __forceinline__ uint32_t lookup_word(uint32_t w, const uint8_t* tab) {
+  const uint32_t b0 = tab[w & 0xFFu], b1 = tab[(w >> 8) & 0xFFu];
+  const uint32_t b2 = tab[(w >> 16) & 0xFFu], b3 = tab[w >> 24];
+  return prmt(prmt(b0, b1, 0x0040u), prmt(b2, b3, 0x0040u), 0x5410u);
 }
 
-// bytes [q0 q1 q2 q3] (each < 16) -> 16-bit value q0 | q1<<4 | q2<<8 | q3<<12 (in bytes 0 and 2)
-__device__ __forceinline__ uint32_t squeeze(uint32_t q4) { return q4 | (q4 >> 4); }
-
 // One group: 16 packed bytes v and scale byte s -> 16 bytes of int4 codes and
-// the fp32 scale.  lut[cmax]: q and (-q)&15 by code; lut_s[cmax] = fl32(cmax/7).
-__device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const uint4* lut, const float* lut_s,
-                                              uint4& q_out, float& s_out) {
+// the fp32 scale.  ltab[cmax][byte]: the output byte of a packed byte (two
+// signed codes) in a group whose largest magnitude code is cmax; lut_s[cmax]
+// = fl32(cmax / 7).
+__device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const uint8_t (*ltab)[256],
+                                              const float* lut_s, uint4& q_out, float& s_out) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
   // largest magnitude code in the group
   uint32_t m = 0;
@@ -80,13 +77,9 @@ __device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const 
     // normal float for these scale bytes, so the power of two commutes with
     // the rounding
     oscale = lut_s[cmax] * sc_unit;
-    const uint4 t = lut[cmax];
+    const uint8_t* tab = ltab[cmax];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = squeeze(lookup4(wd[i], t.x, t.y, t.z, t.w));
-      const uint32_t hi = squeeze(lookup4(wd[i] >> 16, t.x, t.y, t.z, t.w));
-      oq[i] = prmt(lo, hi, 0x6420u);
-    }
+    for (int i = 0; i < 4; ++i) oq[i] = lookup_word(wd[i], tab);
   } else {
     // exact per-element path (values near the subnormal range or near overflow)
     const float amax = e2m1_mag(cmax) * sc_unit;
@@ -115,23 +108,28 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
                                                                   uint8_t* __restrict__ out_q,
                                                                   float* __restrict__ out_s,
                                                                   long long n_groups) {
-  __shared__ uint4 lut[8];  // per cmax: q by code (2 words), (-q)&15 by code (2 words)
-  __shared__ float lut_s[8];  // per cmax: fl32(cmax / 7)
-  if (threadIdx.x < 8) {
-    const uint32_t cm = threadIdx.x;
-    uint32_t pos[2] = {0, 0}, neg[2] = {0, 0};
-    float sc = 0.f;
+  // per cmax (largest magnitude code of a group, 1..7): fl32(cmax / 7), the
+  // int4 code of each signed E2M1 code, and from those the output byte of
+  // every packed byte (two codes)
+  __shared__ float lut_s[8];
+  __shared__ uint8_t qcode[8][16];
+  __shared__ uint8_t ltab[8][256];
+  if (threadIdx.x < 8) lut_s[threadIdx.x] = threadIdx.x ? __fdiv_rn(e2m1_mag(threadIdx.x), 7.0f) : 0.f;
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const uint32_t cm = threadIdx.x >> 4, c = threadIdx.x & 15;
+    int q = 0;
     if (cm > 0) {
-      sc = __fdiv_rn(e2m1_mag(cm), 7.0f);
-      for (uint32_t c = 0; c < 8; ++c) {
-        int q = __float2int_rn(__fdiv_rn(e2m1_mag(c), sc));
-        q = min(max(q, -8), 7);
-        pos[c >> 2] |= uint32_t(q & 0xF) << (8 * (c & 3));
-        neg[c >> 2] |= uint32_t((-q) & 0xF) << (8 * (c & 3));
-      }
+      q = __float2int_rn(__fdiv_rn(e2m1_mag(c), lut_s[cm]));
+      q = min(max(q, -8), 7);
+      if (c & 8u) q = -q;
     }
-    lut[cm] = make_uint4(pos[0], pos[1], neg[0], neg[1]);
-    lut_s[cm] = sc;
+    qcode[cm][c] = (uint8_t)(q & 0xF);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) {
+    const int cm = i >> 8, b = i & 255;
+    ltab[cm][b] = (uint8_t)(qcode[cm][b & 15] | (qcode[cm][b >> 4] << 4));
   }
   __syncthreads();
 
@@ -158,7 +156,7 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
       if (gi < n_groups) {
         uint4 q;
         float o;
-        requant_group(v[i], sb[i], lut, lut_s, q, o);
+        requant_group(v[i], sb[i], ltab, lut_s, q, o);
         __stcs(reinterpret_cast<uint4*>(out_q) + gi, q);
         __stcs(out_s + gi, o);
       }

@@ -113,12 +113,17 @@ def test_scale_bands_decode_two_launch(mw):
     assert_per_band(run(mw, prob, PATH_DECODE), ref, prob[1])
 
 
-@pytest.mark.parametrize("path,T,topk", [(PATH_DECODE, 7, 4), (PATH_DECODE, 40, 4), (PATH_PREFILL, 160, 3)])
-def test_wide_activation_range(mw, path, T, topk):
-    # every element of x scaled by its own power of two in [2^-20, 2^20]
+@pytest.mark.parametrize("path,T,topk,lo,hi", [(PATH_DECODE, 7, 4, -20, 20), (PATH_DECODE, 40, 4, -20, 20),
+                                               (PATH_PREFILL, 160, 3, -20, 20), (PATH_DECODE, 7, 4, -26, 0),
+                                               (PATH_DECODE, 40, 4, -26, 0)])
+def test_wide_activation_range(mw, path, T, topk, lo, hi):
+    # every element of x scaled by its own power of two in [2^lo, 2^hi]; with
+    # [-26, 0] each row's largest value lies in [2^-4, 2^15), where the
+    # weight-streaming kernels leave activations unscaled and the smallest
+    # values fall on the f16 subnormal grid
     E, H, I = 8, 1024, 512
-    g = synth.rng(900 + T)
-    xf = synth.gaussian(g, (T, H)) * np.exp2(g.integers(-20, 21, size=(T, H))).astype(np.float32)
+    g = synth.rng(900 + T + lo)
+    xf = synth.gaussian(g, (T, H)) * np.exp2(g.integers(lo, hi + 1, size=(T, H))).astype(np.float32)
     x = synth.bf16_bits_from_f32(xf)
     ids, w = synth.router_topk(g, T, E, topk)
     w13, s13 = formats.quantize_mxfp4(synth.gaussian(g, (E, 2 * I, H), 0.02))
