@@ -158,18 +158,18 @@ __device__ __forceinline__ uint32_t published_value(uint32_t token, int slot) {
   return token * 0x9E3779B1u + (uint32_t)slot;
 }
 
-// One warp waits until every flags[q], q < n, holds published_value(token, q)
-// (acquire), giving up after ``limit_ns`` like mbar_wait.  Every lane returns
-// the same value.
-__device__ __forceinline__ bool wait_all_published(const uint32_t* flags, int n, uint32_t token, uint32_t* status,
-                                                   uint64_t limit_ns) {
+// One warp waits until every flags[q], q in [lo, hi), holds
+// published_value(token, q) (acquire), giving up after ``limit_ns`` like
+// mbar_wait.  Every lane returns the same value.
+__device__ __forceinline__ bool wait_published_range(const uint32_t* flags, int lo, int hi, uint32_t token,
+                                                     uint32_t* status, uint64_t limit_ns) {
   const int lane = threadIdx.x & 31;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0;; ++i) {
     // every flag of this lane loaded at once (relaxed, independent), one
     // acquire fence once all have been seen
     bool ok = true;
-    for (int q = lane; q < n; q += 32) ok &= ld_relaxed_gpu(flags + q) == published_value(token, q);
+    for (int q = lo + lane; q < hi; q += 32) ok &= ld_relaxed_gpu(flags + q) == published_value(token, q);
     if (__all_sync(0xffffffffu, ok)) {
       fence_acq_rel_gpu();
       return true;

@@ -503,6 +503,14 @@ __device__ __forceinline__ UnitRange cta_units(const Grouping& gr, int tiles, in
   return r;
 }
 
+// The CTA whose run of a phase split with rot = 0 holds unit u (n units over
+// the grid: the first n % grid CTAs get one extra).
+__device__ __forceinline__ int cta_of_unit(int u, int n) {
+  const int G = gridDim.x, base = n / G, rem = n - base * G;
+  if (u < (base + 1) * rem) return u / (base + 1);
+  return base ? rem + (u - (base + 1) * rem) / base : G - 1;
+}
+
 // Position in an mbarrier ring, carried from one phase into the next.
 struct RingPos {
   int n;           // slots taken so far
@@ -847,15 +855,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const Gemm
     return;
   }
   consume_units<KIND, true, NBW>(p1, gr, r1, c, wr, rr);
-  // CTA 0 always waits: it advances the epoch
-  if (r2.u0 < r2.u1 || blockIdx.x == 0) {
+  if (r2.u0 < r2.u1) {
+    // the down units' activations come from the gate_up units of the same
+    // experts: wait for the CTAs whose gate_up runs hold those units only
     if (warp == 0) {
-      if (!wait_all_published(p1.flags, gridDim.x + p1.wait_extra, token, p1.status, p1.wait_ns) && lane == 0)
+      int d_last = r2.d0;
+      while (gr.gpre[d_last + 1] * p2.tiles <= r2.u1 - 1) ++d_last;
+      const int n1 = gr.gpre[gr.n_act] * p1.tiles;
+      const int b_lo = cta_of_unit(gr.gpre[r2.d0] * p1.tiles, n1);
+      const int b_hi = cta_of_unit(gr.gpre[d_last + 1] * p1.tiles - 1, n1);
+      if (!wait_published_range(p1.flags, b_lo, b_hi + 1, token, p1.status, p1.wait_ns) && lane == 0)
         *c.abort_flag = 1;
-      if (blockIdx.x == 0 && lane == 0) *p1.epoch = token;
     }
     named_bar_sync(1, kConsumerWarps * 32);
     consume_units<KIND, false, NBW>(p2, gr, r2, c, wr, rr);
+  }
+  // CTA 0 advances the epoch once every CTA has published (so every CTA has
+  // read it); by the end of its own work that has long happened
+  if (blockIdx.x == 0 && warp == 0) {
+    wait_published_range(p1.flags, 0, gridDim.x + p1.wait_extra, token, p1.status, p1.wait_ns);
+    if (lane == 0) *p1.epoch = token;
   }
 }
 

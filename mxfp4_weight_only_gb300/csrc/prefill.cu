@@ -753,16 +753,30 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
   }
 }
 
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
-                                                          const int32_t* __restrict__ sorted_pair,
-                                                          const int32_t* __restrict__ n_valid, int topk, int H,
-                                                          uint16_t* __restrict__ xs) {
-  const int i = blockIdx.x;
+// xs[i] = x[token of sorted pair i]: one warp per row (H <= 4096: at most 16
+// sixteen-byte chunks per lane, all loads issued before the stores), eight
+// rows per CTA.
+constexpr int kGatherRowsPerCta = 8;
+
+__global__ void __launch_bounds__(32 * kGatherRowsPerCta) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                                            const int32_t* __restrict__ sorted_pair,
+                                                                            const int32_t* __restrict__ n_valid,
+                                                                            int topk, int H,
+                                                                            uint16_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * kGatherRowsPerCta + (threadIdx.x >> 5);
   if (i >= *n_valid) return;
   const int tok = sorted_pair[i] / topk;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)i * H);
-  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) dst[c] = __ldg(src + c);
+  const int n16 = H / 8;  // sixteen-byte chunks per row
+  uint4 v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    if (lane + 32 * k < n16) v[k] = __ldg(src + lane + 32 * k);
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    if (lane + 32 * k < n16) dst[lane + 32 * k] = v[k];
 }
 
 // Row i of the activated intermediate (f32) -> f16, scaled by 2^aexp[i] so
@@ -873,9 +887,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
 
   timing_mark(1, false, s);
-  gather_rows_kernel<<<(unsigned)P, 256, 0, s>>>(reinterpret_cast<const uint16_t*>(a.x), a.route.sorted_pair,
-                                                  a.route.offsets + a.E, a.topk, a.H,
-                                                  reinterpret_cast<uint16_t*>(a.xs));
+  gather_rows_kernel<<<(unsigned)((P + kGatherRowsPerCta - 1) / kGatherRowsPerCta), 32 * kGatherRowsPerCta, 0, s>>>(
+      reinterpret_cast<const uint16_t*>(a.x), a.route.sorted_pair, a.route.offsets + a.E, a.topk, a.H,
+      reinterpret_cast<uint16_t*>(a.xs));
   timing_mark(1, true, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
