@@ -20,8 +20,7 @@ For each pair (t, k) with e = topk_ids[t, k] in [0, E):
     out[t] += topk_weights[t, k] * y  (k ascending)
 All in float64 from exact inputs.  Pairs with invalid ids add nothing.
 
-Optional variants (not on the benchmarked path; the kernels do not take them
-yet):
+Optional variants (not on the benchmarked path):
 * biases: ``create_weights`` registers ``w13_bias`` bf16[E, 2I] and
   ``w2_bias`` bf16[E, H] when the layer has biases, and
   ``get_fused_moe_quant_config`` hands them to the kernel as ``w1_bias`` /
@@ -32,13 +31,18 @@ yet):
   outputs unweighted.
 * ``expert_map`` (``apply``, expert parallelism): global ids mapped to local
   ids (or -1) before the grouping, as in ``route.route``.
+* ``act_quant`` (vLLM PR #39136, the ``w_mxfp4_a_mxfp4`` and ``w_mxfp4_a_fp8``
+  schemes): both GEMMs take quantised-dequantised activations,
+  ``actquant.act_qdq``; the stage-1 input is x (bf16, exact in float32), the
+  stage-2 input the intermediate a rounded to float32; W4A8 uses the static
+  input scales ``w13_input_scale`` / ``w2_input_scale``.
 """
 
 from __future__ import annotations
 
 import numpy as np
 
-from . import formats
+from . import actquant, formats
 from .route import local_ids, route
 
 
@@ -46,12 +50,17 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
-def _expert_mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray, b13=None, b2=None) -> np.ndarray:
+def _expert_mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray, b13=None, b2=None,
+                act_quant=None, s13: float = 1.0, s2: float = 1.0) -> np.ndarray:
     I = W13.shape[0] // 2
+    if act_quant:
+        X = actquant.act_qdq(X, act_quant, s13)
     h = X @ W13.T
     if b13 is not None:
         h = h + b13
     a = silu(h[:, :I]) * h[:, I:]
+    if act_quant:
+        a = actquant.act_qdq(a.astype(np.float32), act_quant, s2)
     y = a @ W2.T
     if b2 is not None:
         y = y + b2
@@ -81,11 +90,15 @@ def _deq(kind: str, w: np.ndarray, s: np.ndarray) -> np.ndarray:
 
 
 def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4", b13=None, b2=None,
-                router_weight_on_input: bool = False, expert_map=None) -> np.ndarray:
+                router_weight_on_input: bool = False, expert_map=None, act_quant=None,
+                w13_input_scale: float = 1.0, w2_input_scale: float = 1.0) -> np.ndarray:
     """Full MoE output, float64[T, H].  ``x_bits`` are bfloat16 bit patterns
     uint16[T, H]; ``b13`` / ``b2`` optional bias bit patterns uint16[E, 2I] /
     uint16[E, H]; ``expert_map`` optional int32[global experts] (global id ->
-    local id or -1)."""
+    local id or -1); ``act_quant`` None, "mxfp4" or "fp8" (static scales
+    ``w13_input_scale``, ``w2_input_scale``)."""
+    if act_quant and router_weight_on_input:
+        raise ValueError("router weight on the input with quantised activations is not modelled")
     X = formats.bf16_to_f64(x_bits)
     T, H = X.shape
     ids = np.asarray(topk_ids)
@@ -103,7 +116,8 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4",
         Xp = X[pairs // topk]
         if router_weight_on_input:
             Xp = Xp * w.reshape(-1)[pairs][:, None]
-        y[pairs] = _expert_mlp(Xp, W13, W2, _bias_rows(b13, e), _bias_rows(b2, e))
+        y[pairs] = _expert_mlp(Xp, W13, W2, _bias_rows(b13, e), _bias_rows(b2, e), act_quant,
+                               w13_input_scale, w2_input_scale)
     out = np.zeros((T, H), dtype=np.float64)
     for k in range(topk):
         out += y[k::topk] if router_weight_on_input else w[:, k:k + 1] * y[k::topk]
@@ -111,13 +125,16 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4",
 
 
 def moe_forward_sampled(x_bits, topk_ids, topk_w, w13, s13, w2, s2, tokens, cols,
-                        kind: str = "mxfp4", expert_map=None) -> np.ndarray:
+                        kind: str = "mxfp4", expert_map=None, act_quant=None,
+                        w13_input_scale: float = 1.0, w2_input_scale: float = 1.0) -> np.ndarray:
     """out[tokens][:, cols] only, float64[len(tokens), len(cols)].
 
     Each selected token's pairs need their full stage-1 output, but only the
     selected rows of W2; used to check full-size problems element by element.
     """
     X = formats.bf16_to_f64(x_bits)
+    if act_quant:
+        X = actquant.act_qdq(X, act_quant, w13_input_scale)
     ids = local_ids(topk_ids, expert_map)
     topk = ids.shape[1]
     E = w13.shape[0]
@@ -136,5 +153,7 @@ def moe_forward_sampled(x_bits, topk_ids, topk_w, w13, s13, w2, s2, tokens, cols
                     continue
                 h = W13 @ X[t]
                 a = silu(h[:I]) * h[I:]
+                if act_quant:
+                    a = actquant.act_qdq(a.astype(np.float32), act_quant, w2_input_scale)
                 out[i] += w[t, k] * (W2c @ a)
     return out
