@@ -62,8 +62,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--copies", type=int, default=4, help="rotating weight copies (L2 defeat)")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak before the timed region")
-    ap.add_argument("--rows", default="sweep,requant,int4,prefill",
-                    help="comma list of secondary measurements to run (sweep, requant, int4, prefill)")
+    ap.add_argument("--rows", default="sweep,requant,int4,prefill,actquant",
+                    help="comma list of secondary measurements to run (sweep, requant, int4, prefill, actquant)")
     ap.add_argument("--prefill-tokens", type=int, default=4096, help="tokens of the prefill row")
     return ap.parse_args()
 
@@ -297,8 +297,10 @@ def run_ours(args, rank: int, world: int):
 
     stream = torch.cuda.Stream(device=dev)
 
-    def capture(T, n_steps, kind="mxfp4", timing_steps=0, weights=None, seed0=1000, path=0):
-        """Capture n_steps MoE calls (rotating weight copies and batches) into one graph."""
+    def capture(T, n_steps, kind="mxfp4", timing_steps=0, weights=None, seed0=1000, path=0, opts=None):
+        """Capture n_steps MoE calls (rotating weight copies and batches) into one graph;
+        ``opts``: optional layer inputs (keyword arguments of the binding)."""
+        opts = opts or {}
         weights = weights or copies
         batches = [dev_batch(T, seed0 + i) for i in range(ROTATE)]
         d = m.dims(SHAPE.E, SHAPE.H, SHAPE.I, SHAPE.topk, T, path)
@@ -310,7 +312,7 @@ def run_ours(args, rank: int, world: int):
         with torch.cuda.stream(stream):
             for i in range(2):  # eager warm-up outside capture (kernel attributes, module load)
                 x, ids, w, _ = batches[i % ROTATE]
-                fn(x, ids, w, *weights[i % len(weights)], out=out, workspace=ws, path=path)
+                fn(x, ids, w, *weights[i % len(weights)], out=out, workspace=ws, path=path, **opts)
         stream.synchronize()
         # timing events exist before capture; the library records them as graph nodes
         pre = []
@@ -334,7 +336,7 @@ def run_ours(args, rank: int, world: int):
                     arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in evs])
                     _native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 4))
                     ev.append((evs, distinct(ids_h)))
-                fn(x, ids, w, *weights[i % len(weights)], out=out, workspace=ws, path=path)
+                fn(x, ids, w, *weights[i % len(weights)], out=out, workspace=ws, path=path, **opts)
                 bytes_total += distinct(ids_h) * (W13_BYTES + W2_BYTES)
         return graph, ev, bytes_total, (d, ws)
 
@@ -471,8 +473,9 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
-def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="mxfp4"):
+def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="mxfp4", opts=None, label=None):
     """Tensor-core (prefill) path: skewed routing, median of 4 timed calls."""
+    opts = opts or {}
     rows = {}
     T = prefill_tokens
     pb = [dev_batch(T, 2000 + i, bias=2.0) for i in range(2)]
@@ -493,7 +496,7 @@ def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="m
             m._native.check("moe_set_timing_events", lib.moe_set_timing_events(arr, 6))
         s_ev.record()
         fn = m.moe_a16w4_mxfp4 if kind == "mxfp4" else m.moe_a16w4_int4g32
-        fn(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws, path=m.MOE_PATH_PREFILL)
+        fn(x, ids, w, *copies[i % len(copies)], out=out, workspace=ws, path=m.MOE_PATH_PREFILL, **opts)
         e_ev.record()
         e_ev.synchronize()
         if i >= 2:
@@ -502,7 +505,7 @@ def prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, kind="m
     tf = flops / (ms * 1e-3) / 1e12
     names = ["route", "gather", "gemm1_gate_up_tc", "convert_f16", "gemm2_down_tc", "cast"]
     kms = {n: round(kev[2 * q].elapsed_time(kev[2 * q + 1]), 3) for q, n in enumerate(names)}
-    rows[f"{'mxfp4' if kind == 'mxfp4' else 'int4g32'}_prefill_T{T}_skewed"] = {
+    rows[label or f"{'mxfp4' if kind == 'mxfp4' else 'int4g32'}_prefill_T{T}_skewed"] = {
         "ms_per_call": round(ms, 3), "TFLOPs_useful": round(tf, 1), "kernels_ms": kms,
         "bf16_frac_burst": round(tf / peaks["bf16_tflops"], 3),
         "bf16_frac_sustained": round(tf / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]), 3),
@@ -529,6 +532,24 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
         sweep[f"T{T}"] = {"us_per_call": round(us, 2), "GBps": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
     if sweep:
         rows["mxfp4_decode_sweep"] = sweep
+    if "actquant" in which:
+        # quantised activations (W4A8: static FP8 scales sized for x ~ N(0, 1);
+        # W4A4: MXFP4), same weights and batches as the A16W4 lines
+        schemes = {"w4a8_fp8": {"act_quant": "fp8", "w13_input_scale": 0.02, "w2_input_scale": 0.004},
+                   "w4a4_mxfp4": {"act_quant": "mxfp4"}}
+        aq = {}
+        for name, opts in schemes.items():
+            for T in (1, 32):
+                g, _, nbytes, _ = capture(T, 8, opts=opts)
+                time_graph(g, 2)
+                ms = time_graph(g, reps) / reps
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                aq[f"{name}_T{T}"] = {"us_per_call": round(ms * 1000 / 8, 2), "GBps": round(gbs, 1),
+                                      "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
+            if "prefill" in which:
+                rows.update(prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, opts=opts,
+                                        label=f"mxfp4_{name}_prefill_T{prefill_tokens}_skewed"))
+        rows["mxfp4_act_quant_decode"] = aq
     if not ({"requant", "int4"} & which):
         return rows
     # requantiser over all experts (w13 and w2), then the int4 MoE

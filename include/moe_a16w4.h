@@ -44,10 +44,24 @@ extern "C" {
 
 /* Device status bits (moe_read_status). */
 #define MOE_STATUS_WAIT_TIMEOUT 0x1u /* a pipeline wait in a kernel gave up; outputs invalid */
+/* Set only by the checked build of the library (libmoe_a16w4_check.so, the
+ * same sources compiled with -DMOE_CHECK), whose kernels check every index
+ * they derive (expert, pair, token, row, tile) against its buffer and every
+ * E8M0 weight-scale byte they read -- a stand-in for a memory checker: */
+#define MOE_STATUS_BAD_INDEX 0x2u    /* an index was out of range; it was replaced by 0 (outputs invalid) */
+#define MOE_STATUS_NAN_SCALE 0x4u    /* an E8M0 weight-scale byte was 255 (NaN in the format)          */
 
 /* Activation selector.  Only the SiLU-gated one the pages' stage-1 kernels
  * compute is implemented; SiTUv2 is named on the pages without a formula. */
 #define MOE_ACT_SWIGLU 0
+
+/* Activation quantisation of both GEMM inputs (moe_options_t.act_quant):
+ * the OCP MX schemes of vLLM PR #39136 ("[ROCm][Quantization][2/N] Refactor
+ * quark_moe w4a8 w/ oracle", Summary and review): ``w_mxfp4_a_mxfp4`` (W4A4)
+ * and ``w_mxfp4_a_fp8`` (W4A8, static FP8 activations). */
+#define MOE_AQ_NONE 0  /* bf16 activations (the A16W4 layer)                              */
+#define MOE_AQ_MXFP4 1 /* MXFP4 activations: E2M1 + E8M0 per 32 values along K           */
+#define MOE_AQ_FP8 2   /* e4m3fn activations with one static float32 scale per GEMM input */
 
 /* Kernel family selector (moe_dims_t.path). */
 #define MOE_PATH_AUTO 0    /* weight-streaming kernels for small batches, tensor-core kernels for large */
@@ -143,6 +157,13 @@ int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_id
  *                          id (0..E-1) of global expert g, or -1 if another GPU
  *                          holds it; ids outside the map or mapped to -1
  *                          contribute nothing
+ * Activation quantisation (MOE_AQ_*; MXFP4 weights only, and not together
+ * with router_weight_on_input): each GEMM's input -- x for gate_up, the
+ * SiLU-gated intermediate a (float32 in the kernels) for down -- is replaced
+ * by its quantised-dequantised value, as moe_quantize_act() defines it
+ * (MXFP4 per 32-value block of each row; FP8 with w13_input_scale for x and
+ * w2_input_scale for a).  The GEMMs run on exact codes (FP8: the e4m3 values,
+ * the scale applied to the float32 result).
  * A zero-initialised struct (all NULL / 0) is the plain layer.
  */
 typedef struct moe_options {
@@ -151,11 +172,16 @@ typedef struct moe_options {
   const int32_t* expert_map;       /* int32 [global_num_experts] or NULL    */
   int32_t global_num_experts;      /* 1 .. 2^20 when expert_map is set      */
   int32_t router_weight_on_input;  /* 0 or 1                                */
+  int32_t act_quant;               /* MOE_AQ_*                              */
+  float w13_input_scale;           /* MOE_AQ_FP8: finite, > 0               */
+  float w2_input_scale;            /* MOE_AQ_FP8: finite, > 0               */
 } moe_options_t;
 
 /* moe_a16w4_mxfp4 / moe_a16w4_int4g32 with optional inputs (``opt`` may be
  * NULL: the plain call).  Returns MOE_ERR_BAD_DIMS for global_num_experts
- * outside [1, 2^20] with a map, or router_weight_on_input not 0 or 1. */
+ * outside [1, 2^20] with a map, router_weight_on_input not 0 or 1, act_quant
+ * outside MOE_AQ_*, an FP8 input scale that is not finite and positive, or
+ * act_quant set with int4 weights or with router_weight_on_input. */
 int moe_a16w4_mxfp4_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
                        const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
                        const uint8_t* w2_scale, const moe_options_t* opt, void* out, void* workspace,
@@ -301,6 +327,30 @@ int moe_noalloc_read_status(uint32_t* status, void* stream);
  * ``events`` with n > 0.
  */
 int moe_set_timing_events(void* const* events, int32_t n);
+
+/*
+ * Activation quantiser of the W4A4 / W4A8 schemes (vLLM PR #39136:
+ * ``w_mxfp4_a_mxfp4``, ``w_mxfp4_a_fp8``; the pages name the schemes, the
+ * rules below are the plain readings): the routine the layer kernels apply
+ * to each GEMM input, as a call of its own.
+ *   x          [rows, K] row-major, bf16 (x_is_f32 = 0) or float32 (1);
+ *              16-byte aligned; finite values
+ *   K          multiple of 32, 32 .. 2^20; rows 0 .. 2^31
+ *   MOE_AQ_MXFP4: per 32 consecutive values of a row, the OCP MX v1.0 scale
+ *              byte floor(log2 amax) - 2 + 127 (0 when amax < 2^-125, zero
+ *              included) -> q_scale [rows, K/32]; each value times
+ *              2^(127 - byte) rounded to the nearest E2M1 value, ties to the
+ *              even code, saturating at +-6 -> q [rows, K/2] (value 2j in the
+ *              low nibble of byte j); the sign bit follows the input.
+ *   MOE_AQ_FP8: r = fl32(x / scale) (correctly rounded), rounded to the
+ *              nearest e4m3fn value, ties to even, saturating at +-448 ->
+ *              q [rows, K] (one code per byte); q_scale unused (may be NULL).
+ *   q          16-byte aligned; caller-owned outputs, written on ``stream``.
+ * Returns MOE_ERR_BAD_DIMS for a bad mode, dtype, size or FP8 scale,
+ * MOE_ERR_NULL / MOE_ERR_ALIGN for the pointers.
+ */
+int moe_quantize_act(int32_t act_quant, const void* x, int32_t x_is_f32, int64_t rows, int32_t K, float scale,
+                     uint8_t* q, uint8_t* q_scale, void* stream);
 
 /* Static text for a MOE_ERR_* code. */
 const char* moe_error_string(int code);

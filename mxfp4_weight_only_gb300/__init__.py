@@ -14,13 +14,16 @@ import ctypes
 import torch
 
 from . import _native
-from ._native import (MOE_ACT_SWIGLU, MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL,  # noqa: F401
-                      MOE_STATUS_WAIT_TIMEOUT, MoeDims, MoeError, MoeOptions)
+from ._native import (MOE_ACT_SWIGLU, MOE_AQ_FP8, MOE_AQ_MXFP4, MOE_AQ_NONE,  # noqa: F401
+                      MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL, MOE_STATUS_BAD_INDEX,
+                      MOE_STATUS_NAN_SCALE, MOE_STATUS_WAIT_TIMEOUT, MoeDims, MoeError, MoeOptions, use_checked)
 
 __all__ = [
     "moe_workspace_bytes", "moe_a16w4_mxfp4", "moe_a16w4_int4g32", "requant_mxfp4_to_int4g32",
-    "moe_route", "moe_router_topk", "moe_read_status", "dims", "MoeError",
+    "moe_route", "moe_router_topk", "moe_read_status", "moe_quantize_act", "dims", "MoeError",
 ]
+
+_AQ = {None: MOE_AQ_NONE, "bf16": MOE_AQ_NONE, "mxfp4": MOE_AQ_MXFP4, "fp8": MOE_AQ_FP8}
 
 
 def _lib():
@@ -64,9 +67,11 @@ def _workspace(d: MoeDims, workspace, device):
     return workspace
 
 
-def _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input):
+def _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant=None,
+             w13_input_scale=1.0, w2_input_scale=1.0):
     """The optional inputs as a MoeOptions struct, or None when none is set."""
-    if w13_bias is None and w2_bias is None and expert_map is None and not router_weight_on_input:
+    aq = _AQ[act_quant]
+    if w13_bias is None and w2_bias is None and expert_map is None and not router_weight_on_input and not aq:
         return None
     if w13_bias is not None:
         _need(w13_bias, "w13_bias", torch.bfloat16, (E, 2 * I))
@@ -77,11 +82,12 @@ def _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input):
         G = expert_map.shape[0]
         _need(expert_map, "expert_map", torch.int32, (G,))
     return MoeOptions(_ptr(w13_bias).value, _ptr(w2_bias).value, _ptr(expert_map).value, G,
-                      1 if router_weight_on_input else 0)
+                      1 if router_weight_on_input else 0, aq, float(w13_input_scale), float(w2_input_scale))
 
 
 def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, stream, scale_dtype,
-         w13_bias=None, w2_bias=None, expert_map=None, router_weight_on_input=False):
+         w13_bias=None, w2_bias=None, expert_map=None, router_weight_on_input=False, act_quant=None,
+         w13_input_scale=1.0, w2_input_scale=1.0):
     T, H = x.shape
     E, two_i, _ = w13.shape
     I = two_i // 2
@@ -98,7 +104,8 @@ def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, s
     _need(out, "out", torch.bfloat16, (T, H))
     d = dims(E, H, I, topk, T, path)
     workspace = _workspace(d, workspace, x.device)
-    opt = _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input)
+    opt = _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant, w13_input_scale,
+                   w2_input_scale)
     if opt is None:
         rc = getattr(_lib(), fn_name)(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13),
                                       _ptr(w2), _ptr(s2), _ptr(out), _ptr(workspace), workspace.numel(),
@@ -114,23 +121,29 @@ def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, s
 
 def moe_a16w4_mxfp4(x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out=None, workspace=None,
                     path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
-                    router_weight_on_input: bool = False):
+                    router_weight_on_input: bool = False, act_quant=None, w13_input_scale: float = 1.0,
+                    w2_input_scale: float = 1.0):
     """Fused MoE on MXFP4 weights (uint8 packed E2M1 + uint8 E8M0 scales).
 
     Optional: ``w13_bias`` bf16 [E, 2I], ``w2_bias`` bf16 [E, H], ``expert_map``
-    int32 [global experts] (topk_ids then hold global ids), and
-    ``router_weight_on_input``; any of them selects ``moe_a16w4_mxfp4_ex``."""
+    int32 [global experts] (topk_ids then hold global ids),
+    ``router_weight_on_input``, and ``act_quant`` ("mxfp4": W4A4, "fp8": W4A8
+    with the static ``w13_input_scale`` / ``w2_input_scale``); any of them
+    selects ``moe_a16w4_mxfp4_ex``."""
     return _moe("moe_a16w4_mxfp4", x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, workspace, path,
-                stream, torch.uint8, w13_bias, w2_bias, expert_map, router_weight_on_input)
+                stream, torch.uint8, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant,
+                w13_input_scale, w2_input_scale)
 
 
 def moe_a16w4_int4g32(x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out=None, workspace=None,
                       path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
-                      router_weight_on_input: bool = False):
+                      router_weight_on_input: bool = False, act_quant=None, w13_input_scale: float = 1.0,
+                      w2_input_scale: float = 1.0):
     """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 scales); options as
-    ``moe_a16w4_mxfp4``."""
+    ``moe_a16w4_mxfp4`` (the library rejects ``act_quant`` with int4 weights)."""
     return _moe("moe_a16w4_int4g32", x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out, workspace, path,
-                stream, torch.float32, w13_bias, w2_bias, expert_map, router_weight_on_input)
+                stream, torch.float32, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant,
+                w13_input_scale, w2_input_scale)
 
 
 def requant_mxfp4_to_int4g32(w, scale, out_q=None, out_s=None, experts_per_chunk: int = 8, stream=None):
@@ -177,6 +190,27 @@ def moe_router_topk(logits, topk: int, renormalize: bool = True, stream=None):
                                 _stream(stream))
     _native.check("moe_router_topk", rc)
     return ids, w
+
+
+def moe_quantize_act(x, act_quant: str, scale: float = 1.0, stream=None):
+    """Activation quantiser of the W4A4 / W4A8 schemes on rows x [rows, K]
+    (bf16 or float32, K % 32 == 0).  "mxfp4": ``(packed uint8 [rows, K/2],
+    scale bytes uint8 [rows, K/32])``; "fp8": ``(e4m3 codes uint8 [rows, K], None)``."""
+    rows, K = x.shape
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype, (rows, K))
+    aq = _AQ[act_quant]
+    if aq == MOE_AQ_MXFP4:
+        q = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+        qs = torch.empty((rows, K // 32), dtype=torch.uint8, device=x.device)
+    else:
+        q = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+        qs = None
+    rc = _lib().moe_quantize_act(aq, _ptr(x), 1 if x.dtype == torch.float32 else 0, rows, K, float(scale), _ptr(q),
+                                 _ptr(qs), _stream(stream))
+    _native.check("moe_quantize_act", rc)
+    return q, qs
 
 
 def moe_read_status(d: MoeDims, workspace, stream=None) -> int:

@@ -19,7 +19,8 @@ ERRORS = {
 }
 MOE_ACT_SWIGLU = 0
 MOE_PATH_AUTO, MOE_PATH_DECODE, MOE_PATH_PREFILL = 0, 1, 2
-MOE_STATUS_WAIT_TIMEOUT = 0x1
+MOE_STATUS_WAIT_TIMEOUT, MOE_STATUS_BAD_INDEX, MOE_STATUS_NAN_SCALE = 0x1, 0x2, 0x4
+MOE_AQ_NONE, MOE_AQ_MXFP4, MOE_AQ_FP8 = 0, 1, 2
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp = ctypes.c_void_p
@@ -35,7 +36,8 @@ _DimsP = ctypes.POINTER(MoeDims)
 
 class MoeOptions(ctypes.Structure):
     _fields_ = [("w13_bias", _vp), ("w2_bias", _vp), ("expert_map", _vp), ("global_num_experts", _i32),
-                ("router_weight_on_input", _i32)]
+                ("router_weight_on_input", _i32), ("act_quant", _i32), ("w13_input_scale", ctypes.c_float),
+                ("w2_input_scale", ctypes.c_float)]
 
 
 _OptP = ctypes.POINTER(MoeOptions)
@@ -55,20 +57,28 @@ SIGNATURES = {
     "moe_set_wait_limit": (ctypes.c_int, [ctypes.c_uint64, _i32]),
     "moe_a16w4_mxfp4_noalloc": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_noalloc_read_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "moe_quantize_act": (ctypes.c_int, [_i32, _vp, _i32, ctypes.c_int64, _i32, ctypes.c_float, _vp, _vp, _vp]),
     "moe_set_timing_events": (ctypes.c_int, [ctypes.POINTER(_vp), _i32]),
     "moe_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_abi_version": (ctypes.c_int, []),
 }
 
-_lib = None
+_libs = {}
+_use_checked = False
 
 
-def load(path: str | None = None) -> ctypes.CDLL:
-    """Load the library (built in-tree).  Raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = path or _build.lib_path()
+def load(path: str | None = None, checked: bool | None = None) -> ctypes.CDLL:
+    """Load the library (built in-tree).  Raises if it has not been built.
+
+    ``checked`` selects the bounds-checked build (``libmoe_a16w4_check.so``);
+    by default the one chosen with ``use_checked`` (the regular build unless
+    changed)."""
+    if checked is None:
+        checked = _use_checked
+    key = path or checked
+    if key in _libs:
+        return _libs[key]
+    path = path or _build.lib_path(checked)
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build it with `python -m mxfp4_weight_only_gb300.build` "
@@ -79,8 +89,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    _libs[key] = lib
     return lib
+
+
+def use_checked(on: bool) -> None:
+    """Route the package's calls to the bounds-checked build (True) or the
+    regular one (False)."""
+    global _use_checked
+    _use_checked = bool(on)
 
 
 class MoeError(RuntimeError):

@@ -1,8 +1,11 @@
 """Build ``libmoe_a16w4.so`` in-tree for sm_103a with nvcc.
 
 Each CUDA translation unit is compiled in parallel, then linked into one
-shared library under ``mxfp4_weight_only_gb300/_build``.  Rebuilds only what
-is older than its sources.  Usage: ``python -m mxfp4_weight_only_gb300.build``.
+shared library under ``mxfp4_weight_only_gb300/_build``.  The same sources
+compiled with ``-DMOE_CHECK`` give the checked library
+``libmoe_a16w4_check.so`` (kernels that bounds-check their indices into the
+status word), built alongside.  Rebuilds only what is older than its sources.
+Usage: ``python -m mxfp4_weight_only_gb300.build``.
 """
 
 from __future__ import annotations
@@ -18,7 +21,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libmoe_a16w4.so"
-SOURCES = ["api.cu", "route.cu", "requant.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
+CHECK_LIB_NAME = "libmoe_a16w4_check.so"
+SOURCES = ["api.cu", "route.cu", "requant.cu", "decode.cu", "prefill.cu", "noalloc.cu", "actquant.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "moe_internal.h")] + [
     os.path.join(ROOT, "include", "moe_a16w4.h")
 ]
@@ -33,8 +37,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libmoe_a16w4")
 
 
-def lib_path() -> str:
-    return os.path.join(BUILD, LIB_NAME)
+def lib_path(checked: bool = False) -> str:
+    return os.path.join(BUILD, CHECK_LIB_NAME if checked else LIB_NAME)
 
 
 def _stale(target: str, deps) -> bool:
@@ -45,16 +49,18 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(verbose: bool = False, jobs: int | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+    """Build both libraries; returns the path of the regular one."""
+    os.makedirs(os.path.join(BUILD, "check"), exist_ok=True)
     cc = nvcc()
-    objs = []
+    objs = {False: [], True: []}
     todo = []
-    for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
-        objs.append(o)
-        if _stale(o, [s] + HEADERS):
-            todo.append([cc] + FLAGS + ["-c", s, "-o", o])
+    for checked in (False, True):
+        for src in SOURCES:
+            s = os.path.join(CSRC, src)
+            o = os.path.join(BUILD, "check" if checked else "", src.replace(".cu", ".o"))
+            objs[checked].append(o)
+            if _stale(o, [s] + HEADERS):
+                todo.append([cc] + FLAGS + (["-DMOE_CHECK"] if checked else []) + ["-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,12 +71,13 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
 
     with ThreadPoolExecutor(max_workers=jobs or min(len(todo), os.cpu_count() or 4) or 1) as ex:
         list(ex.map(run, todo))
-    lib = lib_path()
-    if todo or _stale(lib, objs):
-        tmp = lib + ".tmp"
-        run([cc] + ARCH + ["-shared", "-o", tmp] + objs)
-        os.replace(tmp, lib)
-    return lib
+    for checked in (False, True):
+        lib = lib_path(checked)
+        if todo or _stale(lib, objs[checked]):
+            tmp = lib + ".tmp"
+            run([cc] + ARCH + ["-shared", "-o", tmp] + objs[checked])
+            os.replace(tmp, lib)
+    return lib_path()
 
 
 if __name__ == "__main__":

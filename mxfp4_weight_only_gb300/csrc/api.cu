@@ -43,6 +43,7 @@ RouteOut route_view(uint8_t* ws, const Workspace& L) {
   r.n_mtiles = reinterpret_cast<int32_t*>(ws + L.n_mtiles);
   r.mtiles_dn = reinterpret_cast<int32_t*>(ws + L.mtiles_dn);
   r.n_mtiles_dn = reinterpret_cast<int32_t*>(ws + L.n_mtiles_dn);
+  r.status = reinterpret_cast<uint32_t*>(ws + L.status);
   return r;
 }
 
@@ -74,6 +75,18 @@ int read_options(const moe_options_t* o, LayerOptions* lo) {
   lo->emap = o->expert_map;
   lo->G = o->expert_map ? o->global_num_experts : 0;
   lo->rwi = o->router_weight_on_input;
+  if (o->act_quant < MOE_AQ_NONE || o->act_quant > MOE_AQ_FP8) return MOE_ERR_BAD_DIMS;
+  lo->aq = o->act_quant;
+  if (lo->aq == MOE_AQ_FP8) {
+    // static scales: finite and positive (the comparisons are false for NaN)
+    if (!(o->w13_input_scale > 0.f && o->w13_input_scale <= 3.0e38f)) return MOE_ERR_BAD_DIMS;
+    if (!(o->w2_input_scale > 0.f && o->w2_input_scale <= 3.0e38f)) return MOE_ERR_BAD_DIMS;
+    lo->s13 = o->w13_input_scale;
+    lo->s2 = o->w2_input_scale;
+  }
+  // the schemes quantise the activations of MXFP4-weight layers; the router
+  // weight on the input is not modelled together with them
+  if (lo->aq != MOE_AQ_NONE && lo->rwi) return MOE_ERR_BAD_DIMS;
   return MOE_OK;
 }
 
@@ -85,6 +98,7 @@ int run_moe(const moe_dims_t* d, const void* x, const int32_t* ids, const float*
   if (rc != MOE_OK) return rc;
   LayerOptions opt;
   rc = read_options(options, &opt);
+  if (rc == MOE_OK && opt.aq != MOE_AQ_NONE && kind != WeightKind::kMxfp4) rc = MOE_ERR_BAD_DIMS;
   if (rc != MOE_OK || d->T == 0) return rc;
   int sms = 0;
   rc = check_device(&sms);
@@ -332,6 +346,24 @@ int moe_router_topk(const float* logits, int32_t T, int32_t G, int32_t topk, int
              : MOE_ERR_CUDA;
 }
 
+int moe_quantize_act(int32_t act_quant, const void* x, int32_t x_is_f32, int64_t rows, int32_t K, float scale,
+                     uint8_t* q, uint8_t* q_scale, void* stream) {
+  if (act_quant != MOE_AQ_MXFP4 && act_quant != MOE_AQ_FP8) return MOE_ERR_BAD_DIMS;
+  if ((x_is_f32 != 0 && x_is_f32 != 1) || rows < 0 || rows > (1ll << 31) || K < 32 || K % 32 || K > (1 << 20))
+    return MOE_ERR_BAD_DIMS;
+  if (act_quant == MOE_AQ_FP8 && !(scale > 0.f && scale <= 3.0e38f)) return MOE_ERR_BAD_DIMS;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || (act_quant == MOE_AQ_MXFP4 && !q_scale)) return MOE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(q, 16)) return MOE_ERR_ALIGN;
+  int sms = 0;
+  const int rc = check_device(&sms);
+  if (rc != MOE_OK) return rc;
+  return launch_act_quant(act_quant, x, x_is_f32 == 1, rows, K, scale, q, q_scale, sms,
+                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 int moe_read_status(const moe_dims_t* d, void* workspace, uint32_t* status, void* stream) {
   if (!d || !workspace || !status) return MOE_ERR_NULL;
   if (!dims_valid(d)) return MOE_ERR_BAD_DIMS;
@@ -367,6 +399,6 @@ const char* moe_error_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 101; }
+int moe_abi_version(void) { return 102; }
 
 }  // extern "C"

@@ -183,6 +183,37 @@ __device__ __forceinline__ bool wait_published_range(const uint32_t* flags, int 
   }
 }
 
+// ---------------------------------------------------------------- checked build
+//
+// Compiled with -DMOE_CHECK (the checked library), the kernels pass every
+// index they derive from the grouping (expert, pair, token, row, tile)
+// through chk() and every E8M0 weight-scale word they read through
+// chk_e8m0(): an index outside its buffer sets MOE_STATUS_BAD_INDEX and is
+// replaced by 0, so the access stays in bounds; a scale byte 255 (NaN in
+// E8M0) sets MOE_STATUS_NAN_SCALE.  Without the flag both compile to nothing.
+#ifdef MOE_CHECK
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+__device__ __forceinline__ int chk(long long i, long long n, uint32_t* status) {
+  if (kChecked && (i < 0 || i >= n)) {
+    if (status) atomicOr(status, kStatusBadIndex);
+    return 0;
+  }
+  return (int)i;
+}
+
+// ``nbytes`` (1..4) E8M0 bytes in the low bytes of ``w``.
+__device__ __forceinline__ void chk_e8m0(uint32_t w, int nbytes, uint32_t* status) {
+  if (kChecked) {
+    bool nan = false;
+    for (int b = 0; b < nbytes; ++b) nan |= ((w >> (8 * b)) & 0xFFu) == 0xFFu;
+    if (nan && status) atomicOr(status, kStatusNanScale);
+  }
+}
+
 // ---------------------------------------------------------------- expert ids
 
 // Local expert id of top-k slot ``p``: ids[p], mapped through ``emap`` (G
@@ -248,6 +279,123 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       "{%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// ---------------------------------------------------------------- activation quantisation
+//
+// The W4A4 and W4A8 schemes of vLLM PR #39136 (``w_mxfp4_a_mxfp4``,
+// ``w_mxfp4_a_fp8``): each GEMM input is quantised where a kernel loads it.
+// A lane holds 8 consecutive values of a row; the 4 lanes 4m .. 4m+3 hold one
+// 32-value block (the MX block), so block maxima take two shuffles.
+
+enum ActQuant : int { kActNone = 0, kActMxfp4 = 1, kActFp8 = 2 };
+static_assert(kActNone == MOE_AQ_NONE && kActMxfp4 == MOE_AQ_MXFP4 && kActFp8 == MOE_AQ_FP8,
+              "kernel and public activation-quantisation codes");
+
+// OCP MX scale byte of a block with largest magnitude ``amax``:
+// floor(log2 amax) - 2 + 127 (2 = E2M1's largest exponent), 0 for a block
+// whose amax is below 2^-125 (zero and subnormal amax included).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  return eb > 2 ? (uint32_t)(eb - 2) : 0u;
+}
+
+// Eight floats -> eight E2M1 codes (value 2j in the low nibble of byte j),
+// round to nearest even, saturating at +-6; the sign bit follows the input.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Four floats -> four e4m3fn codes (value j in byte j), round to nearest
+// even, saturating at +-448; the sign bit follows the input.
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float v0, float v1, float v2, float v3) {
+  uint32_t r;
+  asm("{\n .reg .b16 h0, h1;\n"
+      " cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n"
+      " mov.b32 %0, {h0, h1};\n}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return r;
+}
+
+// Four e4m3fn codes (byte j = value j) -> two f16x2 (values 0,1 and 2,3), exact.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t c, uint32_t& o0, uint32_t& o1) {
+  asm("{\n .reg .b16 h0, h1;\n mov.b32 {h0, h1}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, h0;\n cvt.rn.f16x2.e4m3x2 %1, h1;\n}"
+      : "=r"(o0), "=r"(o1)
+      : "r"(c));
+}
+
+// The low / high f16 half of a word as float, exact.
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  float f;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(v));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  float f;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(v));
+  return f;
+}
+
+// MXFP4 quantisation of one lane's 8 values of a block (all 32 lanes call it
+// together): codes, the block's scale byte, and v replaced by the dequantised
+// values code * 2^(scale - 127) (exact in float).
+__device__ __forceinline__ void mx_quant8(float (&v)[8], uint32_t& codes, uint32_t& sbyte) {
+  float m = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(v[q]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  sbyte = mx_scale_byte(m);
+  const float rcp = __uint_as_float((254u - sbyte) << 23);  // 2^(127 - scale), scale <= 252
+  float r[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) r[q] = v[q] * rcp;  // exact unless far below 0.25 (rounds to 0 either way)
+  codes = f32x8_to_e2m1x8(r);
+  uint32_t h[4];
+  e2m1x8_to_f16x8(codes, h[0], h[1], h[2], h[3]);
+  const float X = e8m0_to_float(sbyte);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[2 * q] = f16_lo(h[q]) * X;
+    v[2 * q + 1] = f16_hi(h[q]) * X;
+  }
+}
+
+// FP8 quantisation with a static scale: codes of r = fl32(v / s) (correctly
+// rounded division), and v replaced by the e4m3 values (NOT times s: the
+// callers apply s to their float32 results).
+__device__ __forceinline__ void fp8_quant8(float (&v)[8], float s, uint32_t& c0, uint32_t& c1) {
+  float r[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) r[q] = __fdiv_rn(v[q], s);
+  c0 = f32x4_to_e4m3x4(r[0], r[1], r[2], r[3]);
+  c1 = f32x4_to_e4m3x4(r[4], r[5], r[6], r[7]);
+  uint32_t h[4];
+  e4m3x4_to_f16x4(c0, h[0], h[1]);
+  e4m3x4_to_f16x4(c1, h[2], h[3]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[2 * q] = f16_lo(h[q]);
+    v[2 * q + 1] = f16_hi(h[q]);
+  }
+}
+
+// In-place quantise-dequantise of one lane's 8 values under ``aq``; for FP8
+// the values left are the e4m3 values (the scale is the caller's).  Every
+// lane of the warp must call it (block maxima use shuffles).
+__device__ __forceinline__ void act_quant8(int aq, float s, float (&v)[8]) {
+  uint32_t a, b;
+  if (aq == kActMxfp4) mx_quant8(v, a, b);
+  else if (aq == kActFp8) fp8_quant8(v, s, a, b);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

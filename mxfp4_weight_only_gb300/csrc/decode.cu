@@ -91,6 +91,8 @@ struct GemmParams {
   const int32_t* emap;     // global -> local expert ids, or null
   int G;                   // entries of emap
   int rwi;                 // router weight on the input (gate_up scales h), unweighted combine
+  int aq;                  // activation quantisation of this GEMM's input (ActQuant)
+  float ascale;            // kActFp8: the input's static scale, applied to the float32 sums
 };
 
 // (c0, c1) += (s0, s1) * (x0, x1) as one packed f32x2 FMA (same rounding as two fmaf).
@@ -171,7 +173,9 @@ __device__ __forceinline__ void load8(const void* row, int k0, float (&v)[8]) {
 // Activation fragments of one 8-pair column block (pairs slot0 + g, g = lane/4)
 // over the calling warp's blocks [wb0, wb0 + cnt), as f16 scaled by a power of
 // two per pair; inv receives the undo factors for accumulator columns 2t, 2t+1.
-template <WeightKind KIND, bool GATE_UP, int NBW>
+// AQ: the kernel variant for quantised activations (p.aq); the plain variant
+// carries none of that code.
+template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
 __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* spair, int slot0, int base, int npairs,
                                            int wb0, int cnt, int g, int t, uint32_t (&xf)[NBW][4], float (&inv)[2]) {
   const int slot = slot0 + g;
@@ -179,10 +183,10 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   const void* row = nullptr;
   if (valid) {
     if (GATE_UP) {
-      const int tok = spair[base + slot] / p.topk;
+      const int tok = chk(spair[chk(base + slot, p.P, p.status)], p.P, p.status) / p.topk;
       row = reinterpret_cast<const uint16_t*>(p.src) + (size_t)tok * p.K;
     } else {
-      row = reinterpret_cast<const float*>(p.src) + (size_t)(base + slot) * p.K;
+      row = reinterpret_cast<const float*>(p.src) + (size_t)chk(base + slot, p.P, p.status) * p.K;
     }
   }
   float mx = 0.f;
@@ -203,8 +207,13 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   // inputs from 2^-17 on are exact) and smaller ones are rounded to the f16
   // subnormal grid, an error of at most 2^-25 each: summed over a K of 4096,
   // 2^-9 of the range's largest value.
+  //
+  // Quantised activations (p.aq): MXFP4 values code * 2^(s-127) are at most
+  // 6/5 of their block's largest magnitude, so the same power of two keeps
+  // them below 2^15 * 1.2 (finite in f16); FP8 leaves the e4m3 values (exact
+  // in f16, at most 448) unscaled and folds the static scale into inv.
   int ex = 0;
-  if (mx > 0.f) {
+  if (mx > 0.f && !(AQ && p.aq == kActFp8)) {
     const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
     ex = (lg >= -4 && lg <= 14) ? 0 : min(max(14 - lg, -126), 126);
   }
@@ -218,6 +227,7 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
 #pragma unroll
       for (int q = 0; q < 8; ++q) v[q] = 0.f;
     }
+    if (AQ) act_quant8(p.aq, p.ascale, v);  // warp-uniform: every lane calls it
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] *= sc;
     if (KIND == WeightKind::kMxfp4) {
@@ -236,14 +246,20 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   const int ex1 = __shfl_sync(0xffffffffu, ex, (2 * t + 1) * 4);
   inv[0] = exp2_int(-ex0);
   inv[1] = exp2_int(-ex1);
+  if (AQ && p.aq == kActFp8) {
+    inv[0] = p.ascale;  // ex is 0 for FP8
+    inv[1] = p.ascale;
+  }
 }
 
 // Scales of rows r and r+8 of one 16-row tile for blocks b, b+1 (b even).
 template <WeightKind KIND>
-__device__ __forceinline__ void load_scales2(const uint8_t* ss, int srow, int r, int b, float (&s)[2][2]) {
+__device__ __forceinline__ void load_scales2(const uint8_t* ss, int srow, int r, int b, float (&s)[2][2],
+                                             uint32_t* status) {
   if (KIND == WeightKind::kMxfp4) {
     const uint32_t u0 = *reinterpret_cast<const uint16_t*>(ss + r * srow + b);
     const uint32_t u1 = *reinterpret_cast<const uint16_t*>(ss + (r + 8) * srow + b);
+    chk_e8m0(u0 | (u1 << 16), 4, status);
     e8m0x2_to_float2(u0, s[0][0], s[0][1]);
     e8m0x2_to_float2(u1, s[1][0], s[1][1]);
   } else {
@@ -544,19 +560,19 @@ __device__ void produce_units(const GemmParams& p, const Grouping& gr, const Uni
       *c.abort_flag = 1;
       return;
     }
-    const int e = gr.act[cur.d];
+    const int e = chk(gr.act[cur.d], p.E, p.status);
     uint8_t* sw = c.stages + (size_t)ring.slot * p.stage_bytes;
     uint8_t* ss = sw + kRows * p.row_stride;
     if (lane == 0) mbar_arrive_expect_tx(&c.full[ring.slot], kRows * (Kh + p.srow_bytes));
     __syncwarp();
     {
-      const int row = item_row<GATE_UP>(lane, j, p.I);
+      const int row = chk(item_row<GATE_UP>(lane, j, p.I), p.N, p.status);
       bulk_g2s(sw + lane * p.row_stride, p.w + ((size_t)e * p.N + row) * Kh, Kh, &c.full[ring.slot], policy);
     }
     if (lane < (GATE_UP ? 2 : 1)) {
       // scales: gemm1 gate rows then up rows (each contiguous); gemm2 all rows
       const int rows = GATE_UP ? kRows / 2 : kRows;
-      const int row0 = item_row<GATE_UP>(lane * (kRows / 2), j, p.I);
+      const int row0 = chk(item_row<GATE_UP>(lane * (kRows / 2), j, p.I), p.N - rows + 1, p.status);
       const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws) + ((size_t)e * p.N + row0) * p.srow_bytes;
       bulk_g2s(ss + lane * (kRows / 2) * p.srow_bytes, src, rows * p.srow_bytes, &c.full[ring.slot], policy);
     }
@@ -597,14 +613,14 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
   for (int u = r.u0; u < r.u1; ++u) {
     if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
     const int d = cur.d, grp = cur.grp, j = cur.j;
-    const int e = gr.act[d];
-    const int base = gr.base(d, e);
-    const int npairs = gr.end(d, e) - base;
+    const int e = chk(gr.act[d], p.E, p.status);
+    const int base = chk(gr.base(d, e), p.P + 1, p.status);
+    const int npairs = chk(gr.end(d, e), p.P + 1, p.status) - base;
     if (e != cur_e || grp != cur_grp) {
       cur_e = e;
       cur_grp = grp;
       const int slot = grp * kGroup + col;
-      my_pair = slot < npairs ? gr.spair[base + slot] : -1;
+      my_pair = slot < npairs ? chk(gr.spair[chk(base + slot, p.P, p.status)], p.P, p.status) : -1;
       my_w = (GATE_UP && p.rwi && my_pair >= 0) ? p.topk_w[my_pair] : 0.f;
     }
     if (!mbar_wait(&c.red_full[rr.slot], rr.parity, p.status, p.wait_ns)) {
@@ -635,7 +651,8 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
             hg += bf16_lo(bias[kOut * j + row]);
             hu += bf16_lo(bias[p.I + kOut * j + row]);
           }
-          p.dst[(size_t)(base + grp * kGroup + col) * p.I + kOut * j + row] = silu(hg) * hu;
+          p.dst[(size_t)chk(base + grp * kGroup + col, p.P, p.status) * p.I + chk(kOut * j + row, p.I, p.status)] =
+              silu(hg) * hu;
         }
       }
     } else {
@@ -647,7 +664,7 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
         for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + row * kGroup + col];
         if (my_pair >= 0) {
           if (bias) y += bf16_lo(bias[kRows * j + row]);
-          p.dst[(size_t)my_pair * p.N + kRows * j + row] = y;
+          p.dst[(size_t)my_pair * p.N + chk(kRows * j + row, p.N, p.status)] = y;
         }
       }
     }
@@ -678,7 +695,7 @@ __device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t
       for (int tl = 0; tl < kTiles; ++tl) {
         const int row = 16 * tl + g;
         float sc[2][2];  // [row / row+8][block b / b+1]
-        load_scales2<KIND>(ss, p.srow_bytes, row, b, sc);
+        load_scales2<KIND>(ss, p.srow_bytes, row, b, sc, p.status);
         float m[2][2][2];  // [row / row+8][block][column 2t / 2t+1]
 #pragma unroll
         for (int r2 = 0; r2 < 2; ++r2)
@@ -707,7 +724,7 @@ __device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t
 // Consumer warps: split K, MMA each unit's weight rows against up to 8
 // activation columns held in registers, hand the partial sums to the
 // epilogue warp.
-template <WeightKind KIND, bool GATE_UP, int NBW>
+template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
 __device__ void consume_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
                               RingPos& wr, RingPos& rr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -729,11 +746,11 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
     if (*c.abort_flag) return;
     if (u > r.u0) cur.next(gr.gpre, p.tiles, u);
     const int d = cur.d, grp = cur.grp;
-    const int e = gr.act[d];
-    const int base = gr.base(d, e);
-    const int npairs = gr.end(d, e) - base;
+    const int e = chk(gr.act[d], p.E, p.status);
+    const int base = chk(gr.base(d, e), p.P + 1, p.status);
+    const int npairs = chk(gr.end(d, e), p.P + 1, p.status) - base;
     if (e != cur_e || grp != cur_grp) {
-      load_frags<KIND, GATE_UP, NBW>(p, gr.spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
+      load_frags<KIND, GATE_UP, NBW, AQ>(p, gr.spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
       fold = __any_sync(0xffffffffu, inv[0] != 1.f || inv[1] != 1.f);
       cur_e = e;
       cur_grp = grp;
@@ -777,7 +794,7 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
 // ------------------------------------------------------------------ kernels
 
 // One GEMM stage (gate_up with the activation, or down) as its own launch.
-template <WeightKind KIND, bool GATE_UP, int NBW>
+template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const CtaSmem c = carve_smem(smem);
@@ -802,7 +819,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
     return;
   }
   if (!GATE_UP) grid_dep_wait();  // the activations come from the gate_up kernel
-  consume_units<KIND, GATE_UP, NBW>(p, gr, r, c, wr, rr);
+  consume_units<KIND, GATE_UP, NBW, AQ>(p, gr, r, c, wr, rr);
 }
 
 // Both GEMM stages in one persistent, cooperative launch (grid = the CTAs
@@ -821,7 +838,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
 // units, measured slower: every CTA then reloads its activation fragments in
 // twice as many places, and each reload is a global-memory round trip of
 // about 2 us under the full weight stream.)
-template <WeightKind KIND, int NBW>
+template <WeightKind KIND, int NBW, bool AQ>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const GemmParams p1, const GemmParams p2) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const CtaSmem c = carve_smem(smem);
@@ -854,7 +871,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const Gemm
     reduce_units<false>(p2, gr, r2, c, rr);
     return;
   }
-  consume_units<KIND, true, NBW>(p1, gr, r1, c, wr, rr);
+  consume_units<KIND, true, NBW, AQ>(p1, gr, r1, c, wr, rr);
   if (r2.u0 < r2.u1) {
     // the down units' activations come from the gate_up units of the same
     // experts: wait for the CTAs whose gate_up runs hold those units only
@@ -868,7 +885,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const Gemm
         *c.abort_flag = 1;
     }
     named_bar_sync(1, kConsumerWarps * 32);
-    consume_units<KIND, false, NBW>(p2, gr, r2, c, wr, rr);
+    consume_units<KIND, false, NBW, AQ>(p2, gr, r2, c, wr, rr);
   }
   // CTA 0 advances the epoch once every CTA has published (so every CTA has
   // read it); by the end of its own work that has long happened
@@ -929,10 +946,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   *reinterpret_cast<uint2*>(out + (size_t)t * H + 4 * c4) = o;
 }
 
-template <WeightKind KIND, bool GATE_UP, int NBW>
+template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
 cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
   const size_t smem = kSmemFixed + (size_t)gp.n_stages * gp.stage_bytes;
-  auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW>;
+  auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW, AQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, false, gp);
@@ -941,12 +958,21 @@ cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
 // activation blocks of 32 per consumer warp (even), which sizes the register fragments
 int blocks_per_warp(int K) { return 2 * (((K >> 5) + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps)); }
 
-template <WeightKind KIND, bool GATE_UP>
+template <WeightKind KIND, bool GATE_UP, bool AQ>
 cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
   const int nbw = blocks_per_warp(gp.K);
-  if (nbw <= 8) return launch_gemm<KIND, GATE_UP, 8>(gp, grid, s);
-  if (nbw <= 16) return launch_gemm<KIND, GATE_UP, 16>(gp, grid, s);
+  if (nbw <= 8) return launch_gemm<KIND, GATE_UP, 8, AQ>(gp, grid, s);
+  if (nbw <= 16) return launch_gemm<KIND, GATE_UP, 16, AQ>(gp, grid, s);
   return cudaErrorInvalidValue;  // K above 7168: outside the size limits
+}
+
+// The kernel variants a call uses: int4 weights never come with quantised
+// activations (the library rejects the combination).
+template <bool GATE_UP>
+cudaError_t dispatch_gemm(const GemmParams& gp, WeightKind kind, int grid, cudaStream_t s) {
+  if (kind == WeightKind::kInt4) return dispatch_nbw<WeightKind::kInt4, GATE_UP, false>(gp, grid, s);
+  return gp.aq != kActNone ? dispatch_nbw<WeightKind::kMxfp4, GATE_UP, true>(gp, grid, s)
+                           : dispatch_nbw<WeightKind::kMxfp4, GATE_UP, false>(gp, grid, s);
 }
 
 // The fused kernel holds fragments for up to 8 blocks per warp (K <= 3584 in
@@ -958,9 +984,9 @@ constexpr int kFusedNbw = 8;
 // wait on one another, so it is launched as a cooperative grid of this size:
 // the launch then either places every CTA at once or fails, instead of
 // leaving CTAs waiting for others that cannot be scheduled.
-template <WeightKind KIND>
+template <WeightKind KIND, bool AQ>
 int fused_resident_ctas(size_t smem, int sms) {
-  auto kern = decode_fused_kernel<KIND, kFusedNbw>;
+  auto kern = decode_fused_kernel<KIND, kFusedNbw, AQ>;
   int dev = 0, coop = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return 0;
@@ -969,10 +995,10 @@ int fused_resident_ctas(size_t smem, int sms) {
   return per_sm * sms;
 }
 
-template <WeightKind KIND>
+template <WeightKind KIND, bool AQ>
 cudaError_t launch_fused(const GemmParams& g1, const GemmParams& g2, int grid, cudaStream_t s) {
   const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
-  auto kern = decode_fused_kernel<KIND, kFusedNbw>;
+  auto kern = decode_fused_kernel<KIND, kFusedNbw, AQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(grid), dim3(kDecThreads), smem, s, true, true, g1, g2);
@@ -1030,8 +1056,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g1.emap = a.opt.emap;
   g1.G = a.opt.G;
   g1.rwi = a.opt.rwi;
+  g1.aq = a.opt.aq;
+  g1.ascale = a.opt.s13;
 
   GemmParams g2 = g1;
+  g2.ascale = a.opt.s2;
   g2.w = a.w2;
   g2.ws = a.w2_s;
   g2.N = a.H;
@@ -1042,6 +1071,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g2.bias = a.opt.b2;
 
   const bool fp4 = a.kind == WeightKind::kMxfp4;
+  const bool aq = a.opt.aq != kActNone;  // MXFP4 weights only (checked by the library)
   // one launch for both GEMMs when both fit the fused kernel's fragments and a
   // resident grid fits the flag array
   bool fused = a.sync != nullptr && blocks_per_warp(a.H) <= kFusedNbw && blocks_per_warp(a.I) <= kFusedNbw;
@@ -1050,8 +1080,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     fill_stage_geometry(g1, a.kind, &g2);
     fill_stage_geometry(g2, a.kind, &g1);
     const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
-    fused_grid = fp4 ? fused_resident_ctas<WeightKind::kMxfp4>(smem, a.num_sms)
-                     : fused_resident_ctas<WeightKind::kInt4>(smem, a.num_sms);
+    fused_grid = !fp4 ? fused_resident_ctas<WeightKind::kInt4, false>(smem, a.num_sms)
+                 : aq ? fused_resident_ctas<WeightKind::kMxfp4, true>(smem, a.num_sms)
+                      : fused_resident_ctas<WeightKind::kMxfp4, false>(smem, a.num_sms);
     g1.wait_extra = a.wait.extra_waiters;
     fused = fused_grid >= 1 && g1.n_stages >= 2 && fused_grid + a.wait.extra_waiters <= kMaxSyncCtas;
   }
@@ -1065,8 +1096,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e;
   if (fused) {
     timing_mark(1, false, s);
-    e = fp4 ? launch_fused<WeightKind::kMxfp4>(g1, g2, fused_grid, s)
-            : launch_fused<WeightKind::kInt4>(g1, g2, fused_grid, s);
+    e = !fp4 ? launch_fused<WeightKind::kInt4, false>(g1, g2, fused_grid, s)
+        : aq ? launch_fused<WeightKind::kMxfp4, true>(g1, g2, fused_grid, s)
+             : launch_fused<WeightKind::kMxfp4, false>(g1, g2, fused_grid, s);
     timing_mark(1, true, s);
     if (e != cudaSuccess) {
       // a cooperative grid that cannot be placed (for example under an SM
@@ -1086,13 +1118,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   }
   if (!fused) {
     timing_mark(1, false, s);
-    e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, true>(g1, a.num_sms, s)
-            : dispatch_nbw<WeightKind::kInt4, true>(g1, a.num_sms, s);
+    e = dispatch_gemm<true>(g1, a.kind, a.num_sms, s);
     timing_mark(1, true, s);
     if (e != cudaSuccess) return e;
     timing_mark(2, false, s);
-    e = fp4 ? dispatch_nbw<WeightKind::kMxfp4, false>(g2, a.num_sms, s)
-            : dispatch_nbw<WeightKind::kInt4, false>(g2, a.num_sms, s);
+    e = dispatch_gemm<false>(g2, a.kind, a.num_sms, s);
     timing_mark(2, true, s);
     if (e != cudaSuccess) return e;
   }

@@ -10,6 +10,8 @@
 namespace moe {
 
 constexpr uint32_t kStatusWaitTimeout = MOE_STATUS_WAIT_TIMEOUT;
+constexpr uint32_t kStatusBadIndex = MOE_STATUS_BAD_INDEX;
+constexpr uint32_t kStatusNanScale = MOE_STATUS_NAN_SCALE;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
 constexpr int kMaxExperts = 1024;
@@ -44,6 +46,8 @@ struct LayerOptions {
   const int32_t* emap = nullptr;   // [G] global expert id -> local id or -1
   int G = 0;
   int rwi = 0;                     // router weight on the input, unweighted combine
+  int aq = 0;                      // activation quantisation of both GEMM inputs (ActQuant)
+  float s13 = 1.f, s2 = 1.f;       // static FP8 input scales of the gate_up / down GEMMs
 };
 
 // Byte offsets of the workspace regions for one problem.
@@ -85,6 +89,7 @@ struct RouteOut {
   int32_t* n_mtiles;     // [1]
   int32_t* mtiles_dn;    // [P / kTcRowsDown + E + 1]
   int32_t* n_mtiles_dn;  // [1]
+  uint32_t* status = nullptr;  // the call's status word (checked build), or none
 };
 
 // Launch ``kern`` on ``s``; with ``pdl`` the launch may begin before the previous
@@ -174,6 +179,11 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Activation quantiser (ActQuant aq = 1 MXFP4 or 2 FP8) of rows x K values
+// (bf16, or f32 with src_f32): codes to q, MX scale bytes to qs.
+cudaError_t launch_act_quant(int aq, const void* x, bool src_f32, long long rows, int K, float s, uint8_t* q,
+                             uint8_t* qs, int num_sms, cudaStream_t st);
 
 struct PrefillArgs {
   int E, H, I, topk, T;

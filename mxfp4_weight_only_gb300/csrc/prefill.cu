@@ -114,6 +114,9 @@ struct TcParams {
   uint64_t wait_ns;   // limit of every bounded wait
   const uint16_t* bias;  // bf16 [E][N] added to the outputs (gate_up: b13, down: b2), or null
   int rwi;            // router weight on the input: gate_up scales h by it, down adds unweighted
+  int E, P;           // experts, pairs (T * topk): the bounds the checked build tests indices against
+  float ascale;       // FP8 activations: the static scale of this GEMM's input (applied to the
+                      // float32 sums; the operands hold the e4m3 values); 1 otherwise
 };
 
 // ------------------------------------------------------------------ tcgen05 / TMA helpers
@@ -364,10 +367,10 @@ __device__ __forceinline__ ItemInfo decode_item(const TcParams& p, int item) {
   const int mp = item / p.n_tiles;
   it.nt = item - mp * p.n_tiles;
   const int code = p.mtiles[mp];
-  it.e = code >> 20;
+  it.e = chk(code >> 20, p.E, p.status);
   const int mi = code & 0xFFFFF;
-  it.row0 = p.offsets[it.e] + kRows * mi;
-  it.rows = min(kRows, p.counts[it.e] - kRows * mi);
+  it.row0 = chk(p.offsets[it.e] + kRows * mi, p.P, p.status);
+  it.rows = chk(min(kRows, p.counts[it.e] - kRows * mi) - 1, p.P - it.row0, p.status) + 1;
   return it;
 }
 
@@ -537,6 +540,8 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     auto load_scales = [&](const uint8_t* sr, int g, uint2& e8, float (&f4)[4]) {
       if (KIND == WeightKind::kMxfp4) {
         e8 = __ldg(reinterpret_cast<const uint2*>(sr + 8 * g));
+        chk_e8m0(e8.x, 4, p.status);
+        chk_e8m0(e8.y, 4, p.status);
       } else {
         const float* sf = reinterpret_cast<const float*>(sr) + 8 * g + hk;
 #pragma unroll
@@ -634,7 +639,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           aex[c] = 0;
           wgt[c] = 0.f;
           if (32 * c + lane < it.rows) {
-            const int pair = p.sorted_pair[it.row0 + 32 * c + lane];
+            const int pair = chk(p.sorted_pair[it.row0 + 32 * c + lane], p.P, p.status);
             tok[c] = pair / p.topk;
             wgt[c] = (GATE_UP || !p.rwi) ? p.topk_w[pair] : 1.f;
             if (!GATE_UP) aex[c] = p.aexp[it.row0 + 32 * c + lane];
@@ -695,7 +700,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           float av[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float hg = __uint_as_float(v[i]), hu = __uint_as_float(v[16 + i]);
+            float hg = __uint_as_float(v[i]) * p.ascale, hu = __uint_as_float(v[16 + i]) * p.ascale;
             if (p.rwi) {
               const float wt = __shfl_sync(0xffffffffu, wgt[c], (lo_half ? 0 : 16) + i);
               hg *= wt;
@@ -718,7 +723,7 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
           // within [-126, 126], the intermediate between acc and y)
           auto undo = [&](float acc, int ea) {
             const int k = ewr + ea, k1 = k >> 1;
-            return acc * exp2_int(-k1) * exp2_int(k1 - k);
+            return acc * exp2_int(-k1) * exp2_int(k1 - k) * p.ascale;
           };
           if (nvalid == 32) {
 #pragma unroll
@@ -755,18 +760,29 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
 
 // xs[i] = x[token of sorted pair i]: one warp per row (H <= 4096: at most 16
 // sixteen-byte chunks per lane, all loads issued before the stores), eight
-// rows per CTA.
+// rows per CTA.  With quantised activations (aq) the row is stored
+// quantised-dequantised: MXFP4 code * 2^(s-127), or the FP8 e4m3 value; both
+// exact in bf16.  A 32-value block is the chunks of lanes 4m .. 4m+3.
 constexpr int kGatherRowsPerCta = 8;
+
+__device__ __forceinline__ uint4 act_quant_bf16x8(uint4 u, int aq, float s) {
+  float v[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+  act_quant8(aq, s, v);
+  return make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]), f32x2_to_bf16x2(v[4], v[5]),
+                    f32x2_to_bf16x2(v[6], v[7]));
+}
 
 __global__ void __launch_bounds__(32 * kGatherRowsPerCta) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                                             const int32_t* __restrict__ sorted_pair,
                                                                             const int32_t* __restrict__ n_valid,
-                                                                            int topk, int H,
-                                                                            uint16_t* __restrict__ xs) {
+                                                                            int topk, int H, int aq, float s,
+                                                                            uint16_t* __restrict__ xs, int P,
+                                                                            uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * kGatherRowsPerCta + (threadIdx.x >> 5);
-  if (i >= *n_valid) return;
-  const int tok = sorted_pair[i] / topk;
+  if (i >= *n_valid) return;  // whole warps leave: the row index is per warp
+  const int tok = chk(sorted_pair[chk(i, P, status)], P, status) / topk;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)i * H);
   const int n16 = H / 8;  // sixteen-byte chunks per row
@@ -774,6 +790,15 @@ __global__ void __launch_bounds__(32 * kGatherRowsPerCta) gather_rows_kernel(con
 #pragma unroll
   for (int k = 0; k < 16; ++k)
     if (lane + 32 * k < n16) v[k] = __ldg(src + lane + 32 * k);
+  if (aq != kActNone) {
+    // chunks beyond the row are whole blocks (H % 32 == 0) of zeros
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (32 * k >= n16) break;  // warp-uniform
+      if (lane + 32 * k >= n16) v[k] = make_uint4(0u, 0u, 0u, 0u);
+      v[k] = act_quant_bf16x8(v[k], aq, s);
+    }
+  }
 #pragma unroll
   for (int k = 0; k < 16; ++k)
     if (lane + 32 * k < n16) dst[lane + 32 * k] = v[k];
@@ -782,22 +807,31 @@ __global__ void __launch_bounds__(32 * kGatherRowsPerCta) gather_rows_kernel(con
 // Row i of the activated intermediate (f32) -> f16, scaled by 2^aexp[i] so
 // that the row's largest magnitude lies in [2^14, 2^15): every value within
 // 2^28 of it keeps 11 significant bits.  aexp is clamped to [-126, 126]; an
-// all-zero row gets 0.  One CTA of 256 threads per row, I <= 4096.
+// all-zero row gets 0.  One CTA of 256 threads per row, I <= 4096, 8 values
+// per thread and chunk.  With quantised activations the row is quantised
+// first (MXFP4 blocks of 32 = the chunks of lanes 4m .. 4m+3; the maximum is
+// taken over the dequantised values); FP8 rows keep their e4m3 values (exact
+// in f16) with aexp 0.
 __global__ void __launch_bounds__(256) act_to_f16_kernel(const float* __restrict__ af,
-                                                         const int32_t* __restrict__ n_valid, int I,
+                                                         const int32_t* __restrict__ n_valid, int I, int aq, float s,
                                                          uint16_t* __restrict__ a16, int32_t* __restrict__ aexp) {
   __shared__ float s_max[8];
   const int row = blockIdx.x;
   if (row >= *n_valid) return;
   const float4* src = reinterpret_cast<const float4*>(af + (size_t)row * I);
-  const int n4 = I / 4;
-  float4 v[4];
+  const int n8 = I / 8;
+  float v[2][8];
   float m = 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
     const int c = threadIdx.x + 256 * i;
-    v[i] = c < n4 ? __ldcs(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+    const float4 a = c < n8 ? __ldcs(src + 2 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 b = c < n8 ? __ldcs(src + 2 * c + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
+    v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
+    if (aq != kActNone) act_quant8(aq, s, v[i]);  // block-uniform: every lane calls it
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(v[i][q]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -808,14 +842,15 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const float* __restrict
   for (int w = 1; w < 8; ++w) m = fmaxf(m, s_max[w]);
   // floor(log2 m) from the exponent field (subnormal m counts as 2^-127)
   const int lg = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
-  const int ea = m > 0.f ? max(min(14 - lg, 126), -126) : 0;
+  const int ea = (m > 0.f && aq != kActFp8) ? max(min(14 - lg, 126), -126) : 0;
   const float sc = exp2_int(ea);
-  uint2* dst = reinterpret_cast<uint2*>(a16 + (size_t)row * I);
+  uint4* dst = reinterpret_cast<uint4*>(a16 + (size_t)row * I);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
     const int c = threadIdx.x + 256 * i;
-    if (c < n4)
-      dst[c] = make_uint2(f32x2_to_f16x2(v[i].x * sc, v[i].y * sc), f32x2_to_f16x2(v[i].z * sc, v[i].w * sc));
+    if (c < n8)
+      dst[c] = make_uint4(f32x2_to_f16x2(v[i][0] * sc, v[i][1] * sc), f32x2_to_f16x2(v[i][2] * sc, v[i][3] * sc),
+                          f32x2_to_f16x2(v[i][4] * sc, v[i][5] * sc), f32x2_to_f16x2(v[i][6] * sc, v[i][7] * sc));
   }
   if (threadIdx.x == 0) aexp[row] = ea;
 }
@@ -888,8 +923,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
 
   timing_mark(1, false, s);
   gather_rows_kernel<<<(unsigned)((P + kGatherRowsPerCta - 1) / kGatherRowsPerCta), 32 * kGatherRowsPerCta, 0, s>>>(
-      reinterpret_cast<const uint16_t*>(a.x), a.route.sorted_pair, a.route.offsets + a.E, a.topk, a.H,
-      reinterpret_cast<uint16_t*>(a.xs));
+      reinterpret_cast<const uint16_t*>(a.x), a.route.sorted_pair, a.route.offsets + a.E, a.topk, a.H, a.opt.aq,
+      a.opt.s13, reinterpret_cast<uint16_t*>(a.xs), (int)P, a.status);
   timing_mark(1, true, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -915,6 +950,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.wait_ns = a.wait_ns;
   p.bias = a.opt.b13;
   p.rwi = a.opt.rwi;
+  p.ascale = a.opt.aq == kActFp8 ? a.opt.s13 : 1.f;
+  p.E = a.E;
+  p.P = (int)P;
   timing_mark(2, false, s);
   e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, true>(map_x, p, 2 * a.num_sms, s)
                                    : launch_tc<WeightKind::kInt4, true>(map_x, p, 2 * a.num_sms, s);
@@ -922,8 +960,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
 
   timing_mark(3, false, s);
-  act_to_f16_kernel<<<(unsigned)P, 256, 0, s>>>(a.af, a.route.offsets + a.E, a.I, reinterpret_cast<uint16_t*>(a.a16),
-                                                 a.aexp);
+  act_to_f16_kernel<<<(unsigned)P, 256, 0, s>>>(a.af, a.route.offsets + a.E, a.I, a.opt.aq, a.opt.s2,
+                                                 reinterpret_cast<uint16_t*>(a.a16), a.aexp);
   timing_mark(3, true, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -937,6 +975,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.mtiles = a.route.mtiles_dn;
   p2.n_mtiles = a.route.n_mtiles_dn;
   p2.bias = a.opt.b2;
+  p2.ascale = a.opt.aq == kActFp8 ? a.opt.s2 : 1.f;
   timing_mark(4, false, s);
   e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, false>(map_a, p2, 2 * a.num_sms, s)
                                    : launch_tc<WeightKind::kInt4, false>(map_a, p2, 2 * a.num_sms, s);

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       const unsigned peers = __match_any_sync(0xffffffffu, valid ? my_e : -1);
       const int rank = __popc(peers & lt_mask);
       if (valid) {
-        const int pos = base[my_e] + rank;
+        const int pos = chk(base[my_e] + rank, P, r.status);
         r.sorted_pair[pos] = tid;
         r.pair_pos[tid] = pos;
       } else if (tid < P) {
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       int run = 0;
       const int rank = chunk_rank(e, E, wcnt, &run);
       if (e >= 0) {
-        const int pos = base[e] + rank;
+        const int pos = chk(base[e] + rank, P, r.status);
         r.sorted_pair[pos] = p;
         r.pair_pos[p] = pos;
       } else if (p < P) {
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   if (p < P) {
     const int e = local_expert(ids, p, emap, G, E);
     if (e >= 0) {
-      const int pos = start[e] + rank[p];
+      const int pos = chk(start[e] + rank[p], P, r.status);
       r.sorted_pair[pos] = p;
       r.pair_pos[p] = pos;
     } else {

@@ -22,7 +22,7 @@ pages give the scheme names only; the readings used here:
   the quantiser takes it in float32: the oracle rounds its float64
   intermediate to float32 first, the precision the kernels compute it in.
 
-Pinned by tests/test_oracle_pins.py against ml_dtypes / torch casts, closed
+Pinned by tests/test_oracle_actquant_pins.py against ml_dtypes / torch casts, closed
 forms of the scale rule and every finite e4m3 code.
 """
 
@@ -74,7 +74,8 @@ def quantize_fp8_act(v: np.ndarray, scale: float):
     """Activations (float32-representable) -> (e4m3fn codes, dequantised
     float64 values q * scale), with r = fl32(v / scale)."""
     s = np.float32(scale)
-    r = np.asarray(v, dtype=np.float32) / s  # IEEE float32 division
+    with np.errstate(over="ignore"):  # a quotient beyond float32 is inf, and saturates
+        r = np.asarray(v, dtype=np.float32) / s  # IEEE float32 division
     codes, q = e4m3_round(r.astype(np.float64))
     return codes, q * np.float64(s)
 

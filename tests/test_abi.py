@@ -42,8 +42,18 @@ def test_library_exports_every_declared_symbol(lib):
         assert n in _native.SIGNATURES, n
 
 
+def test_checked_library_exports_every_declared_symbol(lib):
+    from mxfp4_weight_only_gb300 import _native, build
+
+    checked = _native.load(checked=True)
+    assert checked is not lib and checked._name == build.lib_path(checked=True)
+    for n in _declared_functions():
+        assert hasattr(checked, n), n
+    assert checked.moe_abi_version() == lib.moe_abi_version()
+
+
 def test_version_and_error_strings(lib):
-    assert lib.moe_abi_version() == 101
+    assert lib.moe_abi_version() == 102
     assert lib.moe_error_string(0) == b"ok"
     assert b"SwiGLU" in lib.moe_error_string(-4)
 
@@ -114,3 +124,29 @@ def test_option_errors_are_host_side(lib):
     assert call(MoeOptions(None, None, 64, (1 << 20) + 1, 0)) == -2
     assert call(MoeOptions(17, None, None, 0, 0)) == -3  # bias not 2-byte aligned
     assert call(MoeOptions(None, None, 66, 8, 0)) == -3  # map not 4-byte aligned
+    # activation quantisation: mode, FP8 scales, no router weight on the input
+    assert call(MoeOptions(None, None, None, 0, 0, 3, 1.0, 1.0)) == -2
+    assert call(MoeOptions(None, None, None, 0, 0, -1, 1.0, 1.0)) == -2
+    for s13, s2 in ((0.0, 1.0), (1.0, -2.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        assert call(MoeOptions(None, None, None, 0, 0, 2, s13, s2)) == -2
+    assert call(MoeOptions(None, None, None, 0, 1, 1, 1.0, 1.0)) == -2
+    assert call(MoeOptions(None, None, None, 0, 1, 2, 0.5, 0.5)) == -2
+    # not with int4 weights
+    opt = MoeOptions(None, None, None, 0, 0, 1, 1.0, 1.0)
+    assert lib.moe_a16w4_int4g32_ex(ctypes.byref(d), p, p, p, p, p, p, p, ctypes.byref(opt), p,
+                                    ctypes.c_void_p(256), 1 << 30, None) == -2
+
+
+def test_quantize_act_errors_are_host_side(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.moe_quantize_act(0, p, 0, 4, 64, 1.0, p, p, None) == -2  # no quantisation mode
+    assert lib.moe_quantize_act(3, p, 0, 4, 64, 1.0, p, p, None) == -2
+    assert lib.moe_quantize_act(1, p, 2, 4, 64, 1.0, p, p, None) == -2  # dtype flag
+    assert lib.moe_quantize_act(1, p, 0, 4, 48, 1.0, p, p, None) == -2  # K % 32
+    assert lib.moe_quantize_act(1, p, 0, -1, 64, 1.0, p, p, None) == -2
+    assert lib.moe_quantize_act(2, p, 0, 4, 64, 0.0, p, None, None) == -2  # FP8 scale
+    assert lib.moe_quantize_act(2, p, 0, 4, 64, float("nan"), p, None, None) == -2
+    assert lib.moe_quantize_act(1, p, 0, 4, 64, 1.0, p, None, None) == -1  # MX scales need an output
+    assert lib.moe_quantize_act(1, None, 0, 4, 64, 1.0, p, p, None) == -1
+    assert lib.moe_quantize_act(2, ctypes.c_void_p(8), 0, 4, 64, 1.0, p, None, None) == -3
+    assert lib.moe_quantize_act(1, None, 0, 0, 64, 1.0, None, None, None) == 0  # no rows: nothing to do
