@@ -550,6 +550,29 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
                 rows.update(prefill_row(torch, m, dev, copies, peaks, dev_batch, prefill_tokens, opts=opts,
                                         label=f"mxfp4_{name}_prefill_T{prefill_tokens}_skewed"))
         rows["mxfp4_act_quant_decode"] = aq
+        # the quantiser as a call, on the prefill intermediate's shape (T=4096
+        # x top-15 rows of I floats, > L2): HBM-bound, bytes = input + codes
+        nrows = prefill_tokens * SHAPE.topk
+        xa = torch.randn((nrows, SHAPE.I), dtype=torch.float32, device=dev)
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        qa = {}
+        for name, (mode, per_val) in {"mxfp4": ("mxfp4", 0.5 + 1 / 32), "fp8": ("fp8", 1.0)}.items():
+            tl = []
+            for i in range(5):
+                s_ev.record()
+                m.moe_quantize_act(xa, mode, 0.02)
+                e_ev.record()
+                e_ev.synchronize()
+                if i:
+                    tl.append(s_ev.elapsed_time(e_ev))
+            ms = statistics.median(tl)
+            nb = nrows * SHAPE.I * (4 + per_val)
+            qa[name] = {"ms": round(ms, 4), "GBps": round(nb / (ms * 1e-3) / 1e9, 1),
+                        "hbm_frac": round(nb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3), "bytes": int(nb),
+                        "rows": nrows, "K": SHAPE.I, "src": "float32"}
+        rows["moe_quantize_act"] = qa
+        del xa
+        torch.cuda.empty_cache()
     if not ({"requant", "int4"} & which):
         return rows
     # requantiser over all experts (w13 and w2), then the int4 MoE

@@ -373,12 +373,40 @@ __device__ __forceinline__ void mx_quant8(float (&v)[8], uint32_t& codes, uint32
 // FP8 quantisation with a static scale: codes of r = fl32(v / s) (correctly
 // rounded division), and v replaced by the e4m3 values (NOT times s: the
 // callers apply s to their float32 results).
+//
+// Without a division per value: y = v * fl32(1/s) lies within 1.5 float32
+// ulps of fl32(v / s) (two roundings of 2^-24 each against the one of the
+// division), so y * (1 -+ 2^-21), 3.5 ulps either side even after their own
+// rounding, bracket fl32(v / s).  Rounding is monotone: where both ends give
+// the same e4m3 code, so does fl32(v / s).  Where they differ (a quotient
+// within a few ulps of a rounding midpoint, exact ties included) the correctly
+// rounded division decides.  The bound needs 1/s and y to be normal floats:
+// scales outside [2^-126, 2^126] always divide; quotients too small for the
+// bound round to zero at both ends and in fact.
 __device__ __forceinline__ void fp8_quant8(float (&v)[8], float s, uint32_t& c0, uint32_t& c1) {
-  float r[8];
+  bool exact = !(s >= 0x1p-126f && s <= 0x1p126f);
+  if (!exact) {
+    const float rs = __frcp_rn(s);
+    float lo[8], hi[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) r[q] = __fdiv_rn(v[q], s);
-  c0 = f32x4_to_e4m3x4(r[0], r[1], r[2], r[3]);
-  c1 = f32x4_to_e4m3x4(r[4], r[5], r[6], r[7]);
+    for (int q = 0; q < 8; ++q) {
+      const float y = v[q] * rs;
+      lo[q] = y * (1.f - 0x1p-21f);
+      hi[q] = y * (1.f + 0x1p-21f);
+    }
+    c0 = f32x4_to_e4m3x4(lo[0], lo[1], lo[2], lo[3]);
+    c1 = f32x4_to_e4m3x4(lo[4], lo[5], lo[6], lo[7]);
+    // (dividing only the open values, one branch per value, measured slower
+    // than dividing the whole chunk)
+    exact = c0 != f32x4_to_e4m3x4(hi[0], hi[1], hi[2], hi[3]) || c1 != f32x4_to_e4m3x4(hi[4], hi[5], hi[6], hi[7]);
+  }
+  if (exact) {
+    float r[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r[q] = __fdiv_rn(v[q], s);
+    c0 = f32x4_to_e4m3x4(r[0], r[1], r[2], r[3]);
+    c1 = f32x4_to_e4m3x4(r[4], r[5], r[6], r[7]);
+  }
   uint32_t h[4];
   e4m3x4_to_f16x4(c0, h[0], h[1]);
   e4m3x4_to_f16x4(c1, h[2], h[3]);

@@ -124,6 +124,29 @@ def test_quantize_act_fp8_ties_and_saturation(mw):
     assert np.array_equal(q.cpu().numpy(), rc)
 
 
+@pytest.mark.parametrize("scale", [0.0123, 37.0, 3.3e-5, 1.7e30])
+def test_quantize_act_fp8_near_midpoints(mw, scale):
+    # v = fl32(m * scale) and its float32 neighbours, m every e4m3 midpoint:
+    # quotients v / scale within a few ulps of a rounding decision (the
+    # kernels' multiply-by-reciprocal path must hand these to the division)
+    vals = torch.arange(0, 0x7F, dtype=torch.uint8)
+    grid = np.unique(vals.view(torch.float8_e4m3fn).double().numpy())
+    mids = ((grid[:-1] + grid[1:]) / 2 * scale).astype(np.float32)
+    near = [mids]
+    for k in (1, 2, 3):
+        near.append(np.nextafter(near[-1], np.float32(np.inf)))
+    down = [mids]
+    for k in (1, 2, 3):
+        down.append(np.nextafter(down[-1], np.float32(0)))
+    v = np.concatenate(near + down[1:])
+    v = np.concatenate([v, -v])
+    v = np.concatenate([v, np.zeros((-v.size) % 32, np.float32)]).reshape(-1, 32)
+    q, _ = mw.moe_quantize_act(dev(v), "fp8", scale)
+    torch.cuda.synchronize()
+    rc, _ = actquant.quantize_fp8_act(v.astype(np.float64), scale)
+    assert np.array_equal(q.cpu().numpy(), rc)
+
+
 # ------------------------------------------------------------------ the layer
 
 
