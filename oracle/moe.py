@@ -86,6 +86,8 @@ def _deq(kind: str, w: np.ndarray, s: np.ndarray) -> np.ndarray:
         return formats.dequant_mxfp4(w, s)
     if kind == "int4g32":
         return dequant_int4(w, s)
+    if kind == "int4g32_bf16":  # scales as bfloat16 bit patterns
+        return dequant_int4(w, formats.bf16_to_f64(s).astype(np.float32))
     raise ValueError(kind)
 
 

@@ -19,14 +19,15 @@ def _floor_log2(a: Fraction) -> int:
     return e
 
 
-def round_fp32(x: Fraction) -> Fraction:
-    """Nearest binary32 value to the rational x (ties to even); finite range only."""
+def round_fp32(x: Fraction, mant_bits: int = 23) -> Fraction:
+    """Nearest binary32 value to the rational x (ties to even); finite range only.
+    ``mant_bits`` = 7 gives bfloat16 (binary32's exponent range, 8 significant bits)."""
     if x == 0:
         return Fraction(0)
     sign = -1 if x < 0 else 1
     a = abs(x)
     e = max(_floor_log2(a), -126)
-    quantum = Fraction(2) ** (e - 23)
+    quantum = Fraction(2) ** (e - mant_bits)
     n = a / quantum
     m = round(n)  # Python rounds a Fraction half to even
     return sign * m * quantum

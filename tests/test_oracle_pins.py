@@ -418,14 +418,18 @@ def test_int4_dequant_bruteforce():
 # ----------------------------------------------------------------------------- requantiser
 
 
-def _requant_exact(vals_f64, K):
-    """Exact-rational restatement of the int4 rule on decoded values (one row)."""
+def _requant_exact(vals_f64, K, bf16_scale=False):
+    """Exact-rational restatement of the int4 rule on decoded values (one row);
+    with ``bf16_scale`` the scale is rounded on to bfloat16 (8 significant bits)
+    before the elements are divided by it."""
     q = []
     scales = []
     for g0 in range(0, K, 32):
         blk = [Fraction(float(v)) for v in vals_f64[g0:g0 + 32]]
         amax = max(abs(b) for b in blk)
         sc = round_fp32(amax / 7)
+        if bf16_scale:
+            sc = round_fp32(sc, mant_bits=7)
         scales.append(sc)
         for b in blk:
             if sc == 0:
@@ -451,6 +455,44 @@ def test_requant_matches_exact_rational_ieee(s_lo, s_hi):
             q_got = np.where(codes >= 8, codes - 16, codes)
             assert list(q_got) == q_ref
             assert [f32(v) for v in os_[e, n]] == s_ref
+
+
+@pytest.mark.parametrize("s_lo,s_hi", [(0, 6), (100, 130), (245, 252)])
+def test_requant_bf16_scales_match_exact_rational_ieee(s_lo, s_hi):
+    g = np.random.default_rng(s_lo + 7)
+    E, N, K = 2, 3, 96
+    w = g.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    w[1, 2, 16:32] = 0  # an all-zero group
+    sc = g.integers(s_lo, s_hi + 1, size=(E, N, K // 32), dtype=np.uint8)
+    oq, os_ = requant.requant_mxfp4_to_int4g32(w, sc, scale_dtype="bf16")
+    assert os_.dtype == np.uint16
+    vals = formats.dequant_mxfp4(w, sc)
+    for e in range(E):
+        for n in range(N):
+            q_ref, s_ref = _requant_exact(vals[e, n], K, bf16_scale=True)
+            codes = formats.unpack_nibbles(oq[e, n]).astype(np.int64)
+            assert list(np.where(codes >= 8, codes - 16, codes)) == q_ref
+            assert [Fraction(float(v)) for v in formats.bf16_to_f64(os_[e, n])] == s_ref
+
+
+def test_requant_bf16_scales_differ_from_f32_and_stay_in_range():
+    g = np.random.default_rng(33)
+    w = g.integers(0, 256, size=(4, 16, 128), dtype=np.uint8)
+    sc = g.integers(100, 140, size=(4, 16, 8), dtype=np.uint8)
+    q32, s32 = requant.requant_mxfp4_to_int4g32(w, sc)
+    qb, sb = requant.requant_mxfp4_to_int4g32(w, sc, scale_dtype="bf16")
+    sbf = formats.bf16_to_f64(sb)
+    # the stored scale is the float32 one rounded to bf16 (8 significant bits:
+    # relative change <= 2^-8)
+    assert np.array_equal(sbf, formats.bf16_to_f64(formats.f32_to_bf16_rne(s32)))
+    assert np.all(np.abs(sbf - s32) <= 2.0 ** -8 * s32)
+    assert not np.array_equal(sbf, s32.astype(np.float64))
+    codes = formats.unpack_nibbles(qb).astype(np.int64)
+    q = np.where(codes >= 8, codes - 16, codes)
+    assert q.min() >= -7 and q.max() <= 7
+    # dequantisation through the MoE oracle's bf16-scale kind uses the stored scale
+    deq = moe._deq("int4g32_bf16", qb[0], sb[0])
+    assert np.array_equal(deq, moe.dequant_int4(qb[0], sbf[0].astype(np.float32)))
 
 
 def test_requant_all_code_pairs_scale_invariant():
