@@ -615,6 +615,42 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
         rows.update(prefill_row(torch, m, dev, q_copies, peaks, dev_batch, prefill_tokens, kind="int4"))
     del q_copies
     torch.cuda.empty_cache()
+    # the same with bfloat16 group scales (half the scale bytes)
+    b_copies, breq_ms = [], []
+    for c in range(len(copies)):
+        w13, s13, w2, s2 = copies[c]
+        q13, q2 = torch.empty_like(w13), torch.empty_like(w2)
+        b13 = torch.empty(s13.shape, dtype=torch.bfloat16, device=dev)
+        b2 = torch.empty(s2.shape, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        s_ev.record()
+        m.requant_mxfp4_to_int4g32(w13, s13, q13, b13, experts_per_chunk=8, scale_dtype=torch.bfloat16)
+        m.requant_mxfp4_to_int4g32(w2, s2, q2, b2, experts_per_chunk=8, scale_dtype=torch.bfloat16)
+        e_ev.record()
+        e_ev.synchronize()
+        breq_ms.append(s_ev.elapsed_time(e_ev))
+        b_copies.append((q13, b13, q2, b2))
+    bms = statistics.median(breq_ms[1:] or breq_ms)
+    bbytes = rbytes - SHAPE.E * (2 * SHAPE.I * SHAPE.H // 16 + SHAPE.H * SHAPE.I // 16)
+    rows["requant_112_experts_bf16_scales"] = {"ms": round(bms, 3), "GBps": round(bbytes / (bms * 1e-3) / 1e9, 1),
+                                               "hbm_frac": round(bbytes / (bms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                                               "bytes": bbytes, "experts_per_chunk": 8}
+    ib = {}
+    ib_bytes = 2 * SHAPE.I * SHAPE.H // 2 + 2 * SHAPE.I * SHAPE.H // 16 + SHAPE.H * SHAPE.I // 2 + SHAPE.H * SHAPE.I // 16
+    for T in (1, 7, 32):
+        g, _, nbytes, _ = capture(T, 8, kind="int4", weights=b_copies)
+        nbytes = nbytes // (W13_BYTES + W2_BYTES) * ib_bytes
+        time_graph(g, 2)
+        ms = time_graph(g, reps) / reps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        ib[f"T{T}"] = {"us_per_call": round(ms * 1000 / 8, 2), "GBps": round(gbs, 1),
+                       "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
+    rows["int4g32_bf16_scales_decode"] = ib
+    if "prefill" in which:
+        rows.update(prefill_row(torch, m, dev, b_copies, peaks, dev_batch, prefill_tokens, kind="int4",
+                                label=f"int4g32_bf16_scales_prefill_T{prefill_tokens}_skewed"))
+    del b_copies
+    torch.cuda.empty_cache()
     return rows
 
 

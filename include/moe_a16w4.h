@@ -212,6 +212,30 @@ int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, 
                              uint8_t* out_q, float* out_s, int32_t experts_per_chunk, void* stream);
 
 /*
+ * int4_per_group_32 with bfloat16 group scales.  Source: vLLM PR #51274,
+ * commit message -- the MXFP4 expert weights are converted "to int4 with
+ * groupwise bf16 scales" (the float32-scale calls above follow the other
+ * reading).  Reading used: the scale fl32(amax / 7) is rounded to bf16
+ * (nearest even) and the elements are quantised against that stored scale,
+ * q = round-half-even(fl32(w / scale_bf16)) in [-8, 7] (never -8 in fact).
+ *   requant_mxfp4_to_int4g32_bf16s: as requant_mxfp4_to_int4g32 with
+ *     out_s bf16 [E, N, K/32] (16-byte aligned); bit-exact for scale bytes
+ *     0..252.
+ *   moe_a16w4_int4g32_bf16s(_ex): as moe_a16w4_int4g32(_ex) with
+ *     w13_s bf16 [E, 2I, H/32] and w2_s bf16 [E, H, I/32] (16-byte aligned);
+ *     weight value q * s.  act_quant is rejected as for float32 scales.
+ */
+int requant_mxfp4_to_int4g32_bf16s(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale,
+                                   uint8_t* out_q, void* out_s, int32_t experts_per_chunk, void* stream);
+int moe_a16w4_int4g32_bf16s(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13_q, const void* w13_s, const uint8_t* w2_q, const void* w2_s,
+                            void* out, void* workspace, size_t workspace_bytes, void* stream);
+int moe_a16w4_int4g32_bf16s_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                               const uint8_t* w13_q, const void* w13_s, const uint8_t* w2_q, const void* w2_s,
+                               const moe_options_t* opt, void* out, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
  * The grouping step alone.  Source: the Mxfp4MoEMethod page, ``apply`` -- the
  * fused-MoE kernel receives topk_ids and topk_weights [T, topk] (ids of
  * non-local experts arrive as -1 through ``expert_map``) and must bring each

@@ -139,28 +139,35 @@ def moe_a16w4_int4g32(x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out=None, w
                       path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
                       router_weight_on_input: bool = False, act_quant=None, w13_input_scale: float = 1.0,
                       w2_input_scale: float = 1.0):
-    """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 scales); options as
-    ``moe_a16w4_mxfp4`` (the library rejects ``act_quant`` with int4 weights)."""
-    return _moe("moe_a16w4_int4g32", x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out, workspace, path,
-                stream, torch.float32, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant,
-                w13_input_scale, w2_input_scale)
+    """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 or bfloat16 group
+    scales: bfloat16 selects ``moe_a16w4_int4g32_bf16s``); options as ``moe_a16w4_mxfp4``
+    (the library rejects ``act_quant`` with int4 weights)."""
+    bf16 = w13_s.dtype == torch.bfloat16
+    return _moe("moe_a16w4_int4g32_bf16s" if bf16 else "moe_a16w4_int4g32", x, topk_ids, topk_w, w13_q, w13_s,
+                w2_q, w2_s, out, workspace, path, stream, torch.bfloat16 if bf16 else torch.float32, w13_bias,
+                w2_bias, expert_map, router_weight_on_input, act_quant, w13_input_scale, w2_input_scale)
 
 
-def requant_mxfp4_to_int4g32(w, scale, out_q=None, out_s=None, experts_per_chunk: int = 8, stream=None):
-    """Lossy MXFP4 -> int4_per_group_32 conversion; returns ``(q uint8, s float32)``."""
+def requant_mxfp4_to_int4g32(w, scale, out_q=None, out_s=None, experts_per_chunk: int = 8, stream=None,
+                             scale_dtype=torch.float32):
+    """Lossy MXFP4 -> int4_per_group_32 conversion; returns ``(q uint8, s)`` with ``s``
+    float32, or bfloat16 (``scale_dtype=torch.bfloat16``: ``requant_mxfp4_to_int4g32_bf16s``)."""
     E, N, Kh = w.shape
     K = 2 * Kh
+    if scale_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("scale_dtype must be torch.float32 or torch.bfloat16")
     _need(w, "w", torch.uint8, (E, N, Kh))
     _need(scale, "scale", torch.uint8, (E, N, K // 32))
     if out_q is None:
         out_q = torch.empty_like(w)
     if out_s is None:
-        out_s = torch.empty((E, N, K // 32), dtype=torch.float32, device=w.device)
+        out_s = torch.empty((E, N, K // 32), dtype=scale_dtype, device=w.device)
     _need(out_q, "out_q", torch.uint8, (E, N, Kh))
-    _need(out_s, "out_s", torch.float32, (E, N, K // 32))
-    rc = _lib().requant_mxfp4_to_int4g32(E, N, K, _ptr(w), _ptr(scale), _ptr(out_q), _ptr(out_s),
-                                         experts_per_chunk, _stream(stream))
-    _native.check("requant_mxfp4_to_int4g32", rc)
+    _need(out_s, "out_s", scale_dtype, (E, N, K // 32))
+    fn = "requant_mxfp4_to_int4g32_bf16s" if scale_dtype == torch.bfloat16 else "requant_mxfp4_to_int4g32"
+    rc = getattr(_lib(), fn)(E, N, K, _ptr(w), _ptr(scale), _ptr(out_q), _ptr(out_s), experts_per_chunk,
+                             _stream(stream))
+    _native.check(fn, rc)
     return out_q, out_s
 
 

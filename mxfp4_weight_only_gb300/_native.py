@@ -51,6 +51,11 @@ SIGNATURES = {
     "moe_a16w4_int4g32_ex": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _OptP, _vp, _vp,
                                             ctypes.c_size_t, _vp]),
     "requant_mxfp4_to_int4g32": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
+    "requant_mxfp4_to_int4g32_bf16s": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
+    "moe_a16w4_int4g32_bf16s": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                               ctypes.c_size_t, _vp]),
+    "moe_a16w4_int4g32_bf16s_ex": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _OptP, _vp, _vp,
+                                                  ctypes.c_size_t, _vp]),
     "moe_route": (ctypes.c_int, [_DimsP, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_router_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_read_status": (ctypes.c_int, [_DimsP, _vp, ctypes.POINTER(ctypes.c_uint32), _vp]),

@@ -288,8 +288,23 @@ int moe_a16w4_int4g32_ex(const moe_dims_t* d, const void* x, const int32_t* topk
                  WeightKind::kInt4);
 }
 
-int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale,
-                             uint8_t* out_q, float* out_s, int32_t experts_per_chunk, void* stream) {
+int moe_a16w4_int4g32_bf16s(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                            const uint8_t* w13_q, const void* w13_s, const uint8_t* w2_q, const void* w2_s,
+                            void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_moe(d, x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, nullptr, out, workspace, workspace_bytes,
+                 stream, WeightKind::kInt4Bf16);
+}
+
+int moe_a16w4_int4g32_bf16s_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
+                               const uint8_t* w13_q, const void* w13_s, const uint8_t* w2_q, const void* w2_s,
+                               const moe_options_t* opt, void* out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  return run_moe(d, x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, opt, out, workspace, workspace_bytes, stream,
+                 WeightKind::kInt4Bf16);
+}
+
+static int requant_entry(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale, uint8_t* out_q,
+                         void* out_s, int32_t experts_per_chunk, bool bf16, void* stream) {
   if (E < 1 || N < 1 || K < 32 || K % 32 || experts_per_chunk < 1) return MOE_ERR_BAD_DIMS;
   if (!w || !scale || !out_q || !out_s) return MOE_ERR_NULL;
   if (!aligned(w, 16) || !aligned(out_q, 16) || !aligned(out_s, 16)) return MOE_ERR_ALIGN;
@@ -300,11 +315,22 @@ int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, 
   for (int lo = 0; lo < E; lo += experts_per_chunk) {
     const int hi = lo + experts_per_chunk < E ? lo + experts_per_chunk : E;
     const long long g0 = (long long)lo * groups_per_expert;
-    if (launch_requant(w + g0 * 16, scale + g0, out_q + g0 * 16, out_s + g0, (long long)(hi - lo) * groups_per_expert,
+    void* os = reinterpret_cast<uint8_t*>(out_s) + g0 * (bf16 ? 2 : 4);
+    if (launch_requant(w + g0 * 16, scale + g0, out_q + g0 * 16, os, (long long)(hi - lo) * groups_per_expert, bf16,
                        s) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+int requant_mxfp4_to_int4g32(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale,
+                             uint8_t* out_q, float* out_s, int32_t experts_per_chunk, void* stream) {
+  return requant_entry(E, N, K, w, scale, out_q, out_s, experts_per_chunk, false, stream);
+}
+
+int requant_mxfp4_to_int4g32_bf16s(int32_t E, int32_t N, int32_t K, const uint8_t* w, const uint8_t* scale,
+                                   uint8_t* out_q, void* out_s, int32_t experts_per_chunk, void* stream) {
+  return requant_entry(E, N, K, w, scale, out_q, out_s, experts_per_chunk, true, stream);
 }
 
 int moe_route(const moe_dims_t* d, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
@@ -399,6 +425,6 @@ const char* moe_error_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 102; }
+int moe_abi_version(void) { return 103; }
 
 }  // extern "C"

@@ -262,10 +262,15 @@ __device__ __forceinline__ void load_scales2(const uint8_t* ss, int srow, int r,
     chk_e8m0(u0 | (u1 << 16), 4, status);
     e8m0x2_to_float2(u0, s[0][0], s[0][1]);
     e8m0x2_to_float2(u1, s[1][0], s[1][1]);
-  } else {
+  } else if (KIND == WeightKind::kInt4) {
     const float2 f0 = *reinterpret_cast<const float2*>(ss + r * srow + 4 * b);
     const float2 f1 = *reinterpret_cast<const float2*>(ss + (r + 8) * srow + 4 * b);
     s[0][0] = f0.x; s[0][1] = f0.y; s[1][0] = f1.x; s[1][1] = f1.y;
+  } else {
+    // bfloat16 scales: a bf16 value is the high half of its float
+    const uint32_t u0 = *reinterpret_cast<const uint32_t*>(ss + r * srow + 2 * b);
+    const uint32_t u1 = *reinterpret_cast<const uint32_t*>(ss + (r + 8) * srow + 2 * b);
+    s[0][0] = bf16_lo(u0); s[0][1] = bf16_hi(u0); s[1][0] = bf16_lo(u1); s[1][1] = bf16_hi(u1);
   }
 }
 
@@ -971,6 +976,7 @@ cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
 template <bool GATE_UP>
 cudaError_t dispatch_gemm(const GemmParams& gp, WeightKind kind, int grid, cudaStream_t s) {
   if (kind == WeightKind::kInt4) return dispatch_nbw<WeightKind::kInt4, GATE_UP, false>(gp, grid, s);
+  if (kind == WeightKind::kInt4Bf16) return dispatch_nbw<WeightKind::kInt4Bf16, GATE_UP, false>(gp, grid, s);
   return gp.aq != kActNone ? dispatch_nbw<WeightKind::kMxfp4, GATE_UP, true>(gp, grid, s)
                            : dispatch_nbw<WeightKind::kMxfp4, GATE_UP, false>(gp, grid, s);
 }
@@ -1006,7 +1012,7 @@ cudaError_t launch_fused(const GemmParams& g1, const GemmParams& g2, int grid, c
 
 int stage_bytes_for(int K, WeightKind kind, int* row_stride, int* srow_bytes) {
   *row_stride = (K >> 1) + 16;
-  *srow_bytes = (K >> 5) * (kind == WeightKind::kMxfp4 ? 1 : 4);
+  *srow_bytes = (K >> 5) * scale_bytes(kind);
   const int raw = kRows * *row_stride + kRows * *srow_bytes;
   return (raw + 127) & ~127;
 }
@@ -1070,7 +1076,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g2.dst = a.ybuf;
   g2.bias = a.opt.b2;
 
-  const bool fp4 = a.kind == WeightKind::kMxfp4;
   const bool aq = a.opt.aq != kActNone;  // MXFP4 weights only (checked by the library)
   // one launch for both GEMMs when both fit the fused kernel's fragments and a
   // resident grid fits the flag array
@@ -1080,7 +1085,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     fill_stage_geometry(g1, a.kind, &g2);
     fill_stage_geometry(g2, a.kind, &g1);
     const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
-    fused_grid = !fp4 ? fused_resident_ctas<WeightKind::kInt4, false>(smem, a.num_sms)
+    fused_grid = a.kind == WeightKind::kInt4       ? fused_resident_ctas<WeightKind::kInt4, false>(smem, a.num_sms)
+                 : a.kind == WeightKind::kInt4Bf16 ? fused_resident_ctas<WeightKind::kInt4Bf16, false>(smem, a.num_sms)
                  : aq ? fused_resident_ctas<WeightKind::kMxfp4, true>(smem, a.num_sms)
                       : fused_resident_ctas<WeightKind::kMxfp4, false>(smem, a.num_sms);
     g1.wait_extra = a.wait.extra_waiters;
@@ -1096,7 +1102,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e;
   if (fused) {
     timing_mark(1, false, s);
-    e = !fp4 ? launch_fused<WeightKind::kInt4, false>(g1, g2, fused_grid, s)
+    e = a.kind == WeightKind::kInt4       ? launch_fused<WeightKind::kInt4, false>(g1, g2, fused_grid, s)
+        : a.kind == WeightKind::kInt4Bf16 ? launch_fused<WeightKind::kInt4Bf16, false>(g1, g2, fused_grid, s)
         : aq ? launch_fused<WeightKind::kMxfp4, true>(g1, g2, fused_grid, s)
              : launch_fused<WeightKind::kMxfp4, false>(g1, g2, fused_grid, s);
     timing_mark(1, true, s);

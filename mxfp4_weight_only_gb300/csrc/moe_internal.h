@@ -37,7 +37,12 @@ constexpr int kTcK = 64;         // K per pipeline step (one 128-byte swizzle ro
 constexpr int kTcRowsUp = 192;   // sorted rows per gate_up work item (MMA N, at most)
 constexpr int kTcRowsDown = 128; // sorted rows per down work item (MMA N, at most)
 
-enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1 };
+// Expert weight formats: MXFP4 (E2M1 + E8M0 per 32), int4_per_group_32 with
+// float32 group scales, or with bfloat16 group scales.
+enum class WeightKind : int { kMxfp4 = 0, kInt4 = 1, kInt4Bf16 = 2 };
+
+// Bytes of one 32-group scale.
+__host__ __device__ constexpr int scale_bytes(WeightKind k) { return k == WeightKind::kMxfp4 ? 1 : k == WeightKind::kInt4 ? 4 : 2; }
 
 // Optional inputs of a call (moe_options_t), as the kernels read them.
 struct LayerOptions {
@@ -154,8 +159,9 @@ cudaError_t launch_route(const int32_t* topk_ids, int E, int T, int topk, const 
 cudaError_t launch_router_topk(const float* logits, int T, int G, int topk, int renorm, int32_t* ids, float* w,
                                cudaStream_t s);
 
-cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, float* out_s,
-                           long long n_groups, cudaStream_t s);
+// out_s: float32 scales, or bf16 (uint16) with ``bf16``.
+cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, void* out_s,
+                           long long n_groups, bool bf16, cudaStream_t s);
 
 struct DecodeArgs {
   WeightKind kind;

@@ -347,9 +347,18 @@ __device__ __forceinline__ int weight_row_exponent(const uint8_t* sr, int Kb) {
     return min(140 - (int)(m & 0xFFu), 126);
   } else {
     float m = 0.f;
-    for (int i = 0; i < Kb; i += 4) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(sr) + i / 4);
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+    if (KIND == WeightKind::kInt4) {
+      for (int i = 0; i < Kb; i += 4) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(sr) + i / 4);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+      }
+    } else {
+      for (int i = 0; i < Kb; i += 8) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(sr) + i / 8);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(wd[j])), fabsf(bf16_hi(wd[j]))));
+      }
     }
     if (m == 0.f) return 0;
     const int em = max((int)((__float_as_uint(m) >> 23) & 0xFFu), 1) - 127;  // floor(log2 m), subnormals as -126
@@ -529,23 +538,36 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
     uint32_t ws = 0, wph = 0, used = 0;
     bool stop = false;
     // weight and scale rows of this thread for an item
-    constexpr int kSB = KIND == WeightKind::kMxfp4 ? 1 : 4;  // bytes per scale
+    constexpr int kSB = scale_bytes(KIND);  // bytes per scale
     auto rows_of = [&](const ItemInfo& it, const uint8_t*& wr, const uint8_t*& sr) {
       const size_t row = (size_t)it.e * p.N + (GATE_UP ? 64 * it.nt : kTcW * it.nt) + lrow;
       wr = p.w + row * Kh + 16 * hk;  // block 2 * step + hk at + 32 * step
       sr = reinterpret_cast<const uint8_t*>(p.ws) + row * Kb * kSB;
     };
     // scales of one load group: MXFP4 the group's 8 E8M0 bytes; int4 this
-    // thread's 4 fp32 scales (blocks hk, 2 + hk, 4 + hk, 6 + hk of the group)
+    // thread's 4 scales (blocks hk, 2 + hk, 4 + hk, 6 + hk of the group), fp32
+    // or bf16
     auto load_scales = [&](const uint8_t* sr, int g, uint2& e8, float (&f4)[4]) {
       if (KIND == WeightKind::kMxfp4) {
         e8 = __ldg(reinterpret_cast<const uint2*>(sr + 8 * g));
         chk_e8m0(e8.x, 4, p.status);
         chk_e8m0(e8.y, 4, p.status);
+      } else if (KIND == WeightKind::kInt4) {
+        // the group's 8 fp32 scales in two 16-byte loads (four scalar loads
+        // of this thread's scales: the int4 prefill layer 5.69 ms, not 5.13)
+        const float4* sf = reinterpret_cast<const float4*>(sr) + 2 * g;
+        const float4 a = __ldg(sf), b = __ldg(sf + 1);
+        f4[0] = hk ? a.y : a.x;
+        f4[1] = hk ? a.w : a.z;
+        f4[2] = hk ? b.y : b.x;
+        f4[3] = hk ? b.w : b.z;
       } else {
-        const float* sf = reinterpret_cast<const float*>(sr) + 8 * g + hk;
+        // the group's 8 bf16 scales in one 16-byte load; this thread's are
+        // the halves hk of each word
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(sr) + g);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) f4[i] = __ldg(sf + 2 * i);
+        for (int i = 0; i < 4; ++i) f4[i] = hk ? bf16_hi(wd[i]) : bf16_lo(wd[i]);
       }
     };
     // one group = 4 steps = 8 blocks of the row: 4 blocks of this thread, 8
@@ -954,8 +976,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.E = a.E;
   p.P = (int)P;
   timing_mark(2, false, s);
-  e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, true>(map_x, p, 2 * a.num_sms, s)
-                                   : launch_tc<WeightKind::kInt4, true>(map_x, p, 2 * a.num_sms, s);
+  e = a.kind == WeightKind::kMxfp4  ? launch_tc<WeightKind::kMxfp4, true>(map_x, p, 2 * a.num_sms, s)
+      : a.kind == WeightKind::kInt4 ? launch_tc<WeightKind::kInt4, true>(map_x, p, 2 * a.num_sms, s)
+                                    : launch_tc<WeightKind::kInt4Bf16, true>(map_x, p, 2 * a.num_sms, s);
   timing_mark(2, true, s);
   if (e != cudaSuccess) return e;
 
@@ -977,8 +1000,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p2.bias = a.opt.b2;
   p2.ascale = a.opt.aq == kActFp8 ? a.opt.s2 : 1.f;
   timing_mark(4, false, s);
-  e = a.kind == WeightKind::kMxfp4 ? launch_tc<WeightKind::kMxfp4, false>(map_a, p2, 2 * a.num_sms, s)
-                                   : launch_tc<WeightKind::kInt4, false>(map_a, p2, 2 * a.num_sms, s);
+  e = a.kind == WeightKind::kMxfp4  ? launch_tc<WeightKind::kMxfp4, false>(map_a, p2, 2 * a.num_sms, s)
+      : a.kind == WeightKind::kInt4 ? launch_tc<WeightKind::kInt4, false>(map_a, p2, 2 * a.num_sms, s)
+                                    : launch_tc<WeightKind::kInt4Bf16, false>(map_a, p2, 2 * a.num_sms, s);
   timing_mark(4, true, s);
   if (e != cudaSuccess) return e;
 

@@ -21,6 +21,11 @@
 // fl32(amax / 7) = fl32(cmax / 7) * 2^(s-127).  Groups whose scale byte puts values near the subnormal range or
 // near overflow take the per-element division path, so results are bit-exact
 // for every scale byte in [0, 252].
+//
+// bf16 scales (the "groupwise bf16 scales" of the PR #51274 commit message):
+// the scale is rounded to bf16 (nearest even) before the elements are divided
+// by it; bf16 rounding commutes with the power of two like float32 rounding
+// does, so the same two-code tables hold, built from the rounded scales.
 #include "common.cuh"
 
 namespace moe {
@@ -53,6 +58,7 @@ __device__ __forceinline__ uint32_t lookup_word(uint32_t w, const uint8_t* tab) 
 // the fp32 scale.  ltab[cmax][byte]: the output byte of a packed byte (two
 // signed codes) in a group whose largest magnitude code is cmax; lut_s[cmax]
 // = fl32(cmax / 7).
+template <bool BF16>
 __device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const uint8_t (*ltab)[256],
                                               const float* lut_s, uint4& q_out, float& s_out) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
@@ -84,6 +90,7 @@ __device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const 
     // exact per-element path (values near the subnormal range or near overflow)
     const float amax = e2m1_mag(cmax) * sc_unit;
     oscale = __fdiv_rn(amax, 7.0f);
+    if (BF16) oscale = bf16_lo(f32_to_bf16_bits(oscale));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t r = 0;
@@ -103,10 +110,13 @@ __device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const 
   s_out = oscale;
 }
 
+// BF16: scales rounded to bf16 before the division, stored as bf16 (out_s
+// holds uint16 then).
+template <bool BF16>
 __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t* __restrict__ w,
                                                                   const uint8_t* __restrict__ scale,
                                                                   uint8_t* __restrict__ out_q,
-                                                                  float* __restrict__ out_s,
+                                                                  void* __restrict__ out_s,
                                                                   long long n_groups) {
   // per cmax (largest magnitude code of a group, 1..7): fl32(cmax / 7), the
   // int4 code of each signed E2M1 code, and from those the output byte of
@@ -114,7 +124,11 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
   __shared__ float lut_s[8];
   __shared__ uint8_t qcode[8][16];
   __shared__ uint8_t ltab[8][256];
-  if (threadIdx.x < 8) lut_s[threadIdx.x] = threadIdx.x ? __fdiv_rn(e2m1_mag(threadIdx.x), 7.0f) : 0.f;
+  if (threadIdx.x < 8) {
+    float u = threadIdx.x ? __fdiv_rn(e2m1_mag(threadIdx.x), 7.0f) : 0.f;
+    if (BF16) u = bf16_lo(f32_to_bf16_bits(u));
+    lut_s[threadIdx.x] = u;
+  }
   __syncthreads();
   if (threadIdx.x < 128) {
     const uint32_t cm = threadIdx.x >> 4, c = threadIdx.x & 15;
@@ -156,9 +170,10 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
       if (gi < n_groups) {
         uint4 q;
         float o;
-        requant_group(v[i], sb[i], ltab, lut_s, q, o);
+        requant_group<BF16>(v[i], sb[i], ltab, lut_s, q, o);
         __stcs(reinterpret_cast<uint4*>(out_q) + gi, q);
-        __stcs(out_s + gi, o);
+        if (BF16) reinterpret_cast<uint16_t*>(out_s)[gi] = (uint16_t)(__float_as_uint(o) >> 16);  // exact
+        else __stcs(reinterpret_cast<float*>(out_s) + gi, o);
       }
     }
   }
@@ -166,8 +181,8 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
 
 }  // namespace
 
-cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, float* out_s,
-                           long long n_groups, cudaStream_t s) {
+cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_q, void* out_s,
+                           long long n_groups, bool bf16, cudaStream_t s) {
   if (n_groups <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -177,13 +192,14 @@ cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_
   // one wave: as many CTAs as are resident at once (a second, partial wave
   // would leave most SMs idle at the end)
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel, kRequantThreads, 0);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<false>, kRequantThreads, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const long long want = (n_groups + kRequantThreads - 1) / kRequantThreads;
   const long long resident = (long long)sms * per_sm;
   const int grid = (int)(want < resident ? want : resident);
-  requant_kernel<<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
+  if (bf16) requant_kernel<true><<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
+  else requant_kernel<false><<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
   return cudaGetLastError();
 }
 

@@ -53,7 +53,7 @@ def test_checked_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_error_strings(lib):
-    assert lib.moe_abi_version() == 102
+    assert lib.moe_abi_version() == 103
     assert lib.moe_error_string(0) == b"ok"
     assert b"SwiGLU" in lib.moe_error_string(-4)
 
