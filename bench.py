@@ -558,13 +558,16 @@ def secondary_rows(torch, m, lib, dev, copies, capture, time_graph, peaks, disti
         qa = {}
         for name, (mode, per_val) in {"mxfp4": ("mxfp4", 0.5 + 1 / 32), "fp8": ("fp8", 1.0)}.items():
             tl = []
-            for i in range(5):
+            m.moe_quantize_act(xa, mode, 0.02)  # warm-up
+            for i in range(4):
+                # ten calls back to back: the binding's host work (output
+                # allocation, the call) overlaps the previous kernels
                 s_ev.record()
-                m.moe_quantize_act(xa, mode, 0.02)
+                for _ in range(10):
+                    m.moe_quantize_act(xa, mode, 0.02)
                 e_ev.record()
                 e_ev.synchronize()
-                if i:
-                    tl.append(s_ev.elapsed_time(e_ev))
+                tl.append(s_ev.elapsed_time(e_ev) / 10)
             ms = statistics.median(tl)
             nb = nrows * SHAPE.I * (4 + per_val)
             qa[name] = {"ms": round(ms, 4), "GBps": round(nb / (ms * 1e-3) / 1e9, 1),

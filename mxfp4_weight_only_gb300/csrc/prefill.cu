@@ -390,7 +390,6 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
   constexpr int kActStages = Lay::kActStages;
   constexpr int kWStages = Lay::kWStages;
   constexpr int kRows = Lay::kRows;
-  constexpr int kBoxBytes = Lay::kBoxBytes;
   constexpr uint32_t kAccCol0 = Lay::kAccCol0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
