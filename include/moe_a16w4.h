@@ -7,7 +7,11 @@
  * (quantization/mxfp4): ``create_weights`` fixes the weight layouts used below,
  * ``apply`` the forward call, ``_setup_kernel_k3_situ_gfx942`` the opt-in
  * MXFP4 -> int4_per_group_32 requantisation; vLLM PR #51274 (Summary, Changes)
- * the lossy opt-in int4 path and its eight-experts-per-chunk conversion.
+ * the lossy opt-in int4 path and its eight-experts-per-chunk conversion (with
+ * float32 or, per its commit message, bf16 group scales); vLLM PR #39136 the
+ * W4A4 / W4A8 schemes (quantised activations, moe_options_t.act_quant).
+ * The same sources built with -DMOE_CHECK give libmoe_a16w4_check.so, the
+ * bounds-checked build (MOE_STATUS_BAD_INDEX, MOE_STATUS_NAN_SCALE).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
