@@ -22,9 +22,11 @@ Error bound on h = W13 x (float32 sums of exact products in any order):
 rounding errors of a sum of K terms grow like sqrt(K) ulps of its partial
 sums; 16 leaves many standard deviations) that also covers an accumulation
 that truncates on every one of its K/16 tensor-core steps, for K <= 4096 --
-plus 2^-20 |h| (scale and bias roundings), plus 2^-25 * sum_k |w_nk|
-(activations rounded to the f16 subnormal grid in the weight-streaming
-kernels).  The worst-case bound K * 2^-23 * sum_k |x_k w_nk| would leave an
+plus 2^-20 |h| (scale and bias roundings), plus 2^-25 * max(1, 2^-14 *
+max_k |x_k|) * sum_k |w_nk| (activations rounded to the f16 grid in the
+weight-streaming kernels: unscaled, at most 2^-25 each; scaled so that the
+range's largest value lies in [2^14, 2^15), at most 2^-25 of the unit that
+maps to 2^-14 of it).  The worst-case bound K * 2^-23 * sum_k |x_k w_nk| would leave an
 allowance on every output and test nothing.
 
 With ``h_exact`` the caller's inputs make every product and partial sum of h
@@ -32,8 +34,10 @@ a dyadic number that float32 holds exactly (small integers times E2M1 weights
 with a narrow band of scales, FP8 input scales powers of two), so h carries
 no error at all, whatever the summation order, and only the SiLU's rounding
 remains.  Then a = SiLU(g) u: first-order propagation, a
-second-order term, and (8 + 2|g|) * 2^-23 |a| for the fast exponential and
-division of the kernels' SiLU.
+second-order term, and (8 + 2 min(|g|, 100)) * 2^-23 |a| for the fast
+exponential and division of the kernels' SiLU (the exponential's error grows
+with |g| until it underflows or overflows near |g| = 90, where SiLU(g) is g
+or 0 to within an ulp).
 """
 
 from __future__ import annotations
@@ -122,14 +126,17 @@ def stage2_allowance(x_bits, ids, w, w13, s13, w2, s2, mode, w13_input_scale=1.0
             dh = np.zeros_like(h)
         else:
             S2 = np.sqrt((Xe * Xe) @ (W13 * W13).T)
-            dh = 16.0 * np.sqrt(H) * 2.0 ** -23 * S2 + 2.0 ** -20 * np.abs(h) + 2.0 ** -25 * np.abs(W13).sum(1)
+            xmax = np.abs(Xe).max(1, keepdims=True)
+            dh = (16.0 * np.sqrt(H) * 2.0 ** -23 * S2 + 2.0 ** -20 * np.abs(h)
+                  + 2.0 ** -25 * np.maximum(1.0, 2.0 ** -14 * xmax) * np.abs(W13).sum(1))
         g, u, dg, du = h[:, :I], h[:, I:], dh[:, :I], dh[:, I:]
-        sig = 1.0 / (1.0 + np.exp(-g))
+        with np.errstate(over="ignore"):  # exp(-g) = inf for very negative g: sig = 0, exactly the limit
+            sig = 1.0 / (1.0 + np.exp(-g))
         silu = g * sig
         dsilu = sig * (1.0 + g * (1.0 - sig))
         a = silu * u
         da = (np.abs(dsilu) * np.abs(u) * dg + np.abs(silu) * du + dg * du + 0.5 * dg * dg * np.abs(u)
-              + (8.0 + 2.0 * np.abs(g)) * 2.0 ** -23 * np.abs(a))
+              + (8.0 + 2.0 * np.minimum(np.abs(g), 100.0)) * 2.0 ** -23 * np.abs(a))
         rng = _spread(a, da, mode, w2_input_scale)
         np.add.at(allow, toks, np.abs(wts[toks, ks])[:, None] * (rng @ np.abs(W2).T))
     return allow

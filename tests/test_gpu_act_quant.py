@@ -256,3 +256,45 @@ def test_act_quant_rejected_with_int4_weights(mw):
     f2 = torch.ones(s2.shape, dtype=torch.float32, device="cuda")
     with pytest.raises(mw.MoeError):
         mw.moe_a16w4_int4g32(bf16_dev(x), dev(ids), dev(w), q13, f13, q2, f2, act_quant="fp8")
+
+
+@pytest.mark.parametrize("mode,si13,si2", [("mxfp4", 1.0, 1.0), ("fp8", 0.5, 0.004)])
+@pytest.mark.parametrize("path,T,topk", [(PATH_DECODE, 7, 4), (PATH_DECODE, 40, 4), (PATH_PREFILL, 160, 3)])
+def test_layer_wide_activation_range(mw, mode, si13, si2, path, T, topk):
+    # every element of x scaled by its own power of two in [2^-20, 2^20]: MX
+    # block scales spread over 40 binades within a row (the decode kernels'
+    # f16 window), FP8 quotients from the subnormal range to saturation
+    E, H, I = 8, 1024, 512
+    g = synth.rng(950 + T)
+    xf = synth.gaussian(g, (T, H)) * np.exp2(g.integers(-20, 21, size=(T, H))).astype(np.float32)
+    x = synth.bf16_bits_from_f32(xf)
+    ids, w = synth.router_topk(g, T, E, topk)
+    w13, s13 = formats.quantize_mxfp4(synth.gaussian(g, (E, 2 * I, H), 0.02))
+    w2, s2 = formats.quantize_mxfp4(synth.gaussian(g, (E, H, I), 0.02))
+    prob = (x, ids, w, w13, s13, w2, s2)
+    got = run(mw, prob, path, mode, si13, si2)
+    ref = moe.moe_forward(*prob, act_quant=mode, w13_input_scale=si13, w2_input_scale=si2)
+    assert np.isfinite(ref).all()
+    assert_close_with_allowance(got, ref, stage2_allowance(*prob, mode, si13, si2))
+
+
+@pytest.mark.parametrize("mode,si13,si2,toks", [("mxfp4", 1.0, 1.0, (0, 4095)), ("fp8", 0.125, 0.0078125, (2047,))])
+def test_layer_k3_prefill_sampled(mw, mode, si13, si2, toks):
+    # the tensor-core kernels at the production shape: 4096 tokens, top-15
+    # with skewed routing, exact-h inputs, sampled outputs
+    S = synth.k3(4096)
+    g = synth.rng(21)
+    x = synth.bf16_bits_from_f32(g.integers(-8, 9, size=(S.T, S.H)).astype(np.float32))
+    ids, w = synth.router_topk(g, S.T, S.E, S.topk, expert_bias_std=2.0)
+    w13 = g.integers(0, 256, size=(S.E, 2 * S.I, S.H // 2), dtype=np.uint8)
+    w2 = g.integers(0, 256, size=(S.E, S.H, S.I // 2), dtype=np.uint8)
+    s13 = g.integers(117, 122, size=(S.E, 2 * S.I, S.H // 32), dtype=np.uint8)
+    s2 = g.integers(117, 122, size=(S.E, S.H, S.I // 32), dtype=np.uint8)
+    prob = (x, ids, w, w13, s13, w2, s2)
+    got = run(mw, prob, PATH_PREFILL, mode, si13, si2)
+    toks = np.array(toks)
+    cols = np.sort(synth.rng(22).choice(S.H, 64, replace=False))
+    ref = moe.moe_forward_sampled(*prob, toks, cols, act_quant=mode, w13_input_scale=si13, w2_input_scale=si2)
+    allow = stage2_allowance(*prob, mode, si13, si2, h_exact=True, tokens=toks, cols=cols)
+    assert_close_with_allowance(got[np.ix_(toks, cols)], ref, allow)
+    assert np.isfinite(got).all()

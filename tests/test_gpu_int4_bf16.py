@@ -94,35 +94,54 @@ def test_moe_int4_bf16_scales(mw, path, E, H, I, T, topk):
     assert_moe_close(run(mw, prob, path), moe.moe_forward(*prob, kind="int4g32_bf16"))
 
 
-def test_moe_int4_bf16_scales_k3_sampled(mw):
-    # the 112-expert, H=3584, I=3072, top-15 layer at one token (fused decode
-    # launch): weights requantised on the GPU, the oracle requantises the
-    # experts it needs from the same MXFP4 bytes
+@pytest.fixture(scope="module")
+def k3_bf16(mw):
+    """The 112-expert, H=3584, I=3072 layer's MXFP4 bytes and their bf16-scale
+    int4 requantisation on the GPU."""
     S = synth.k3(1)
     g = synth.rng(100)
     w13, s13 = synth.random_mxfp4_bytes(g, S.E, 2 * S.I, S.H)
     w2, s2 = synth.random_mxfp4_bytes(g, S.E, S.H, S.I)
     q13, b13 = gpu_requant(mw, w13, s13)
     q2, b2 = gpu_requant(mw, w2, s2)
-    g = synth.rng(333)
-    x = synth.activations_bf16(g, 1, S.H)
-    ids, w = synth.router_topk(g, 1, S.E, S.topk)
+    return (w13, s13, w2, s2), (q13, b13, q2, b2)
+
+
+def _oracle_experts(host, experts):
+    """The oracle's bf16-scale requantisation of the experts it needs."""
+    w13, s13, w2, s2 = host
+    oq13, ob13 = np.zeros_like(w13), np.zeros(s13.shape, np.uint16)
+    oq2, ob2 = np.zeros_like(w2), np.zeros(s2.shape, np.uint16)
+    for e in experts:
+        oq13[e:e + 1], ob13[e:e + 1] = requant.requant_mxfp4_to_int4g32(w13[e:e + 1], s13[e:e + 1],
+                                                                         scale_dtype="bf16")
+        oq2[e:e + 1], ob2[e:e + 1] = requant.requant_mxfp4_to_int4g32(w2[e:e + 1], s2[e:e + 1], scale_dtype="bf16")
+    return oq13, ob13, oq2, ob2
+
+
+@pytest.mark.parametrize("T,bias,toks", [(1, None, (0,)), (1024, 2.0, (1023,))])
+def test_moe_int4_bf16_scales_k3_sampled(mw, k3_bf16, T, bias, toks):
+    # the full-size layer: T=1 on the fused decode launch, T=1024 with skewed
+    # routing on the tensor-core kernels; the oracle requantises the experts
+    # it needs from the same MXFP4 bytes
+    host, (q13, b13, q2, b2) = k3_bf16
+    S = synth.k3(T)
+    g = synth.rng(333 + T)
+    x = synth.activations_bf16(g, T, S.H)
+    ids, w = synth.router_topk(g, T, S.E, S.topk, expert_bias_std=bias)
     xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
     out = mw.moe_a16w4_int4g32(xd, dev(ids), dev(w), q13, b13, q2, b2)
     torch.cuda.synchronize()
     got = formats.bf16_to_f64(bits(out))
+    toks = np.array(toks)
     cols = np.sort(g.choice(S.H, 64, replace=False))
-    oq13 = np.zeros_like(w13)
-    ob13 = np.zeros(s13.shape, np.uint16)
-    oq2 = np.zeros_like(w2)
-    ob2 = np.zeros(s2.shape, np.uint16)
-    for e in sorted({int(e) for e in ids[0]}):
-        oq13[e:e + 1], ob13[e:e + 1] = requant.requant_mxfp4_to_int4g32(w13[e:e + 1], s13[e:e + 1], scale_dtype="bf16")
-        oq2[e:e + 1], ob2[e:e + 1] = requant.requant_mxfp4_to_int4g32(w2[e:e + 1], s2[e:e + 1], scale_dtype="bf16")
-        # the GPU's requantised experts are the oracle's, byte for byte
+    need = sorted({int(e) for t in toks for e in ids[t]})
+    oq13, ob13, oq2, ob2 = _oracle_experts(host, need)
+    for e in need[:2]:  # the GPU's requantised experts are the oracle's, byte for byte
         assert np.array_equal(q13[e].cpu().numpy(), oq13[e]) and np.array_equal(bits(b13[e]), ob13[e])
-    ref = moe.moe_forward_sampled(x, ids, w, oq13, ob13, oq2, ob2, np.array([0]), cols, kind="int4g32_bf16")
-    assert_moe_close(got[np.ix_([0], cols)], ref)
+    ref = moe.moe_forward_sampled(x, ids, w, oq13, ob13, oq2, ob2, toks, cols, kind="int4g32_bf16")
+    assert_moe_close(got[np.ix_(toks, cols)], ref)
+    assert np.isfinite(got).all()
 
 
 def test_checked_build_clean_on_int4_bf16_scales(mw):
