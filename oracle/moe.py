@@ -31,6 +31,10 @@ Optional variants (not on the benchmarked path):
   outputs unweighted.
 * ``expert_map`` (``apply``, expert parallelism): global ids mapped to local
   ids (or -1) before the grouping, as in ``route.route``.
+* ``swiglu_limit`` (``Mxfp4MoEMethod.get_fused_moe_quant_config`` passes the
+  layer's ``swiglu_limit`` on as ``gemm1_clamp_limit``; no formula is
+  printed): read as the gate_up GEMM's output, bias included, clamped to
+  [-limit, limit] element by element before the SiLU gating.
 * ``act_quant`` (vLLM PR #39136, the ``w_mxfp4_a_mxfp4`` and ``w_mxfp4_a_fp8``
   schemes): both GEMMs take quantised-dequantised activations,
   ``actquant.act_qdq``; the stage-1 input is x (bf16, exact in float32), the
@@ -51,13 +55,15 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 
 def _expert_mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray, b13=None, b2=None,
-                act_quant=None, s13: float = 1.0, s2: float = 1.0) -> np.ndarray:
+                act_quant=None, s13: float = 1.0, s2: float = 1.0, limit=None) -> np.ndarray:
     I = W13.shape[0] // 2
     if act_quant:
         X = actquant.act_qdq(X, act_quant, s13)
     h = X @ W13.T
     if b13 is not None:
         h = h + b13
+    if limit is not None:
+        h = np.clip(h, -limit, limit)
     a = silu(h[:, :I]) * h[:, I:]
     if act_quant:
         a = actquant.act_qdq(a.astype(np.float32), act_quant, s2)
@@ -93,7 +99,7 @@ def _deq(kind: str, w: np.ndarray, s: np.ndarray) -> np.ndarray:
 
 def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4", b13=None, b2=None,
                 router_weight_on_input: bool = False, expert_map=None, act_quant=None,
-                w13_input_scale: float = 1.0, w2_input_scale: float = 1.0) -> np.ndarray:
+                w13_input_scale: float = 1.0, w2_input_scale: float = 1.0, swiglu_limit=None) -> np.ndarray:
     """Full MoE output, float64[T, H].  ``x_bits`` are bfloat16 bit patterns
     uint16[T, H]; ``b13`` / ``b2`` optional bias bit patterns uint16[E, 2I] /
     uint16[E, H]; ``expert_map`` optional int32[global experts] (global id ->
@@ -119,7 +125,7 @@ def moe_forward(x_bits, topk_ids, topk_w, w13, s13, w2, s2, kind: str = "mxfp4",
         if router_weight_on_input:
             Xp = Xp * w.reshape(-1)[pairs][:, None]
         y[pairs] = _expert_mlp(Xp, W13, W2, _bias_rows(b13, e), _bias_rows(b2, e), act_quant,
-                               w13_input_scale, w2_input_scale)
+                               w13_input_scale, w2_input_scale, swiglu_limit)
     out = np.zeros((T, H), dtype=np.float64)
     for k in range(topk):
         out += y[k::topk] if router_weight_on_input else w[:, k:k + 1] * y[k::topk]

@@ -550,3 +550,49 @@ def test_requant_never_reaches_minus_eight_and_reconstructs_max():
     # error per element at most half a step (scale/2) plus float32 rounding of the scale
     step = np.repeat(s.astype(np.float64), 32, axis=-1)
     assert np.all(np.abs(deq - src) <= step * 0.5 * (1 + 1e-6) + 1e-30)
+
+
+# ----------------------------------------------------------------------------- swiglu_limit clamp
+
+
+def test_moe_swiglu_limit_matches_torch_clamp():
+    x, ids, w, w13, s13, w2, s2 = _tiny_problem(61, T=6, topk=3)
+    g = synth.rng(62)
+    E, I2, H = w13.shape[0], w13.shape[1], w2.shape[1]
+    b13 = _bias_bits(g, (E, I2), 2.0)
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double()
+    W13 = torch.from_numpy(formats.dequant_mxfp4(w13, s13))
+    W2 = torch.from_numpy(formats.dequant_mxfp4(w2, s2))
+    B13 = torch.from_numpy(b13.view(np.int16)).view(torch.bfloat16).double()
+    I = I2 // 2
+    for limit in (0.3, 1.5):
+        ours = moe.moe_forward(x, ids, w, w13, s13, w2, s2, b13=b13, swiglu_limit=limit)
+        ref = torch.zeros(X.shape, dtype=torch.float64)
+        for t in range(ids.shape[0]):
+            for k in range(ids.shape[1]):
+                e = int(ids[t, k])
+                h = torch.clamp(torch.nn.functional.linear(X[t], W13[e], B13[e]), -limit, limit)
+                a = torch.nn.functional.silu(h[:I]) * h[I:]
+                ref[t] += float(w[t, k]) * torch.nn.functional.linear(a, W2[e])
+        assert np.allclose(ours, ref.numpy(), rtol=1e-12, atol=1e-14)
+        # the clamp is active: the result differs from the unclamped layer
+        assert not np.allclose(ours, moe.moe_forward(x, ids, w, w13, s13, w2, s2, b13=b13), rtol=1e-3)
+
+
+def test_moe_swiglu_limit_closed_forms():
+    x, ids, w, w13, s13, w2, s2 = _tiny_problem(63, E=2, T=3, topk=1)
+    base = moe.moe_forward(x, ids, w, w13, s13, w2, s2)
+    # a limit above every |h| changes nothing
+    assert np.array_equal(moe.moe_forward(x, ids, w, w13, s13, w2, s2, swiglu_limit=1e30), base)
+    # all-zero gate_up codes: h is the bias alone, so the output is the clamped
+    # bias pushed through SiLU gating and the down projection
+    zero13 = np.zeros_like(w13)
+    b13 = synth.bf16_bits_from_f32(np.full((2, w13.shape[1]), 3.0, np.float32))
+    limit = 0.75
+    out = moe.moe_forward(x, ids, w, zero13, s13, w2, s2, b13=b13, swiglu_limit=limit)
+    I = w13.shape[1] // 2
+    a = np.full(I, limit / (1.0 + np.exp(-limit)) * limit)
+    W2 = formats.dequant_mxfp4(w2, s2)
+    for t in range(3):
+        e = ids[t, 0]
+        assert np.allclose(out[t], float(np.float32(w[t, 0])) * (W2[e] @ a), rtol=1e-12)
