@@ -168,6 +168,10 @@ int moe_a16w4_int4g32(const moe_dims_t* d, const void* x, const int32_t* topk_id
  * (MXFP4 per 32-value block of each row; FP8 with w13_input_scale for x and
  * w2_input_scale for a).  The GEMMs run on exact codes (FP8: the e4m3 values,
  * the scale applied to the float32 result).
+ * swiglu_limit: ``get_fused_moe_quant_config`` passes the layer's
+ * ``swiglu_limit`` as ``gemm1_clamp_limit``, without a formula; reading used:
+ * the gate_up GEMM's output, bias included, clamped element by element to
+ * [-limit, limit] before the SiLU gating (h = clamp(W13[e] x + b13[e])).
  * A zero-initialised struct (all NULL / 0) is the plain layer.
  */
 typedef struct moe_options {
@@ -179,13 +183,15 @@ typedef struct moe_options {
   int32_t act_quant;               /* MOE_AQ_*                              */
   float w13_input_scale;           /* MOE_AQ_FP8: finite, > 0               */
   float w2_input_scale;            /* MOE_AQ_FP8: finite, > 0               */
+  float swiglu_limit;              /* 0: off; else finite, > 0              */
 } moe_options_t;
 
 /* moe_a16w4_mxfp4 / moe_a16w4_int4g32 with optional inputs (``opt`` may be
  * NULL: the plain call).  Returns MOE_ERR_BAD_DIMS for global_num_experts
  * outside [1, 2^20] with a map, router_weight_on_input not 0 or 1, act_quant
- * outside MOE_AQ_*, an FP8 input scale that is not finite and positive, or
- * act_quant set with int4 weights or with router_weight_on_input. */
+ * outside MOE_AQ_*, an FP8 input scale that is not finite and positive, a
+ * swiglu_limit that is negative, infinite or NaN, or act_quant set with int4
+ * weights or with router_weight_on_input. */
 int moe_a16w4_mxfp4_ex(const moe_dims_t* d, const void* x, const int32_t* topk_ids, const float* topk_w,
                        const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
                        const uint8_t* w2_scale, const moe_options_t* opt, void* out, void* workspace,

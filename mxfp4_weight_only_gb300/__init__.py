@@ -68,10 +68,11 @@ def _workspace(d: MoeDims, workspace, device):
 
 
 def _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant=None,
-             w13_input_scale=1.0, w2_input_scale=1.0):
+             w13_input_scale=1.0, w2_input_scale=1.0, swiglu_limit=None):
     """The optional inputs as a MoeOptions struct, or None when none is set."""
     aq = _AQ[act_quant]
-    if w13_bias is None and w2_bias is None and expert_map is None and not router_weight_on_input and not aq:
+    if (w13_bias is None and w2_bias is None and expert_map is None and not router_weight_on_input and not aq
+            and swiglu_limit is None):
         return None
     if w13_bias is not None:
         _need(w13_bias, "w13_bias", torch.bfloat16, (E, 2 * I))
@@ -82,12 +83,13 @@ def _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input, act
         G = expert_map.shape[0]
         _need(expert_map, "expert_map", torch.int32, (G,))
     return MoeOptions(_ptr(w13_bias).value, _ptr(w2_bias).value, _ptr(expert_map).value, G,
-                      1 if router_weight_on_input else 0, aq, float(w13_input_scale), float(w2_input_scale))
+                      1 if router_weight_on_input else 0, aq, float(w13_input_scale), float(w2_input_scale),
+                      0.0 if swiglu_limit is None else float(swiglu_limit))
 
 
 def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, stream, scale_dtype,
          w13_bias=None, w2_bias=None, expert_map=None, router_weight_on_input=False, act_quant=None,
-         w13_input_scale=1.0, w2_input_scale=1.0):
+         w13_input_scale=1.0, w2_input_scale=1.0, swiglu_limit=None):
     T, H = x.shape
     E, two_i, _ = w13.shape
     I = two_i // 2
@@ -105,7 +107,7 @@ def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, s
     d = dims(E, H, I, topk, T, path)
     workspace = _workspace(d, workspace, x.device)
     opt = _options(E, H, I, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant, w13_input_scale,
-                   w2_input_scale)
+                   w2_input_scale, swiglu_limit)
     if opt is None:
         rc = getattr(_lib(), fn_name)(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(w13), _ptr(s13),
                                       _ptr(w2), _ptr(s2), _ptr(out), _ptr(workspace), workspace.numel(),
@@ -122,30 +124,32 @@ def _moe(fn_name, x, topk_ids, topk_w, w13, s13, w2, s2, out, workspace, path, s
 def moe_a16w4_mxfp4(x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out=None, workspace=None,
                     path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
                     router_weight_on_input: bool = False, act_quant=None, w13_input_scale: float = 1.0,
-                    w2_input_scale: float = 1.0):
+                    w2_input_scale: float = 1.0, swiglu_limit=None):
     """Fused MoE on MXFP4 weights (uint8 packed E2M1 + uint8 E8M0 scales).
 
     Optional: ``w13_bias`` bf16 [E, 2I], ``w2_bias`` bf16 [E, H], ``expert_map``
     int32 [global experts] (topk_ids then hold global ids),
     ``router_weight_on_input``, and ``act_quant`` ("mxfp4": W4A4, "fp8": W4A8
-    with the static ``w13_input_scale`` / ``w2_input_scale``); any of them
-    selects ``moe_a16w4_mxfp4_ex``."""
+    with the static ``w13_input_scale`` / ``w2_input_scale``), and
+    ``swiglu_limit`` (gate_up outputs clamped to [-limit, limit] before the
+    gating); any of them selects ``moe_a16w4_mxfp4_ex``."""
     return _moe("moe_a16w4_mxfp4", x, topk_ids, topk_w, w13, w13_scale, w2, w2_scale, out, workspace, path,
                 stream, torch.uint8, w13_bias, w2_bias, expert_map, router_weight_on_input, act_quant,
-                w13_input_scale, w2_input_scale)
+                w13_input_scale, w2_input_scale, swiglu_limit)
 
 
 def moe_a16w4_int4g32(x, topk_ids, topk_w, w13_q, w13_s, w2_q, w2_s, out=None, workspace=None,
                       path: int = MOE_PATH_AUTO, stream=None, w13_bias=None, w2_bias=None, expert_map=None,
                       router_weight_on_input: bool = False, act_quant=None, w13_input_scale: float = 1.0,
-                      w2_input_scale: float = 1.0):
+                      w2_input_scale: float = 1.0, swiglu_limit=None):
     """Fused MoE on int4_per_group_32 weights (uint8 packed int4 + float32 or bfloat16 group
     scales: bfloat16 selects ``moe_a16w4_int4g32_bf16s``); options as ``moe_a16w4_mxfp4``
     (the library rejects ``act_quant`` with int4 weights)."""
     bf16 = w13_s.dtype == torch.bfloat16
     return _moe("moe_a16w4_int4g32_bf16s" if bf16 else "moe_a16w4_int4g32", x, topk_ids, topk_w, w13_q, w13_s,
                 w2_q, w2_s, out, workspace, path, stream, torch.bfloat16 if bf16 else torch.float32, w13_bias,
-                w2_bias, expert_map, router_weight_on_input, act_quant, w13_input_scale, w2_input_scale)
+                w2_bias, expert_map, router_weight_on_input, act_quant, w13_input_scale, w2_input_scale,
+                swiglu_limit)
 
 
 def requant_mxfp4_to_int4g32(w, scale, out_q=None, out_s=None, experts_per_chunk: int = 8, stream=None,

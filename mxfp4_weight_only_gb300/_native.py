@@ -37,7 +37,7 @@ _DimsP = ctypes.POINTER(MoeDims)
 class MoeOptions(ctypes.Structure):
     _fields_ = [("w13_bias", _vp), ("w2_bias", _vp), ("expert_map", _vp), ("global_num_experts", _i32),
                 ("router_weight_on_input", _i32), ("act_quant", _i32), ("w13_input_scale", ctypes.c_float),
-                ("w2_input_scale", ctypes.c_float)]
+                ("w2_input_scale", ctypes.c_float), ("swiglu_limit", ctypes.c_float)]
 
 
 _OptP = ctypes.POINTER(MoeOptions)

@@ -84,6 +84,8 @@ int read_options(const moe_options_t* o, LayerOptions* lo) {
     lo->s13 = o->w13_input_scale;
     lo->s2 = o->w2_input_scale;
   }
+  if (!(o->swiglu_limit >= 0.f && o->swiglu_limit <= 3.0e38f)) return MOE_ERR_BAD_DIMS;  // NaN fails too
+  lo->clamp = o->swiglu_limit;
   // the schemes quantise the activations of MXFP4-weight layers; the router
   // weight on the input is not modelled together with them
   if (lo->aq != MOE_AQ_NONE && lo->rwi) return MOE_ERR_BAD_DIMS;
@@ -425,6 +427,6 @@ const char* moe_error_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 103; }
+int moe_abi_version(void) { return 104; }
 
 }  // extern "C"

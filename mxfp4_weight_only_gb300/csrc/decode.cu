@@ -93,6 +93,7 @@ struct GemmParams {
   int rwi;                 // router weight on the input (gate_up scales h), unweighted combine
   int aq;                  // activation quantisation of this GEMM's input (ActQuant)
   float ascale;            // kActFp8: the input's static scale, applied to the float32 sums
+  float clamp;             // gate_up: outputs clamped to [-clamp, clamp] before the gating (0: off)
 };
 
 // (c0, c1) += (s0, s1) * (x0, x1) as one packed f32x2 FMA (same rounding as two fmaf).
@@ -656,6 +657,10 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
             hg += bf16_lo(bias[kOut * j + row]);
             hu += bf16_lo(bias[p.I + kOut * j + row]);
           }
+          if (p.clamp > 0.f) {
+            hg = fminf(fmaxf(hg, -p.clamp), p.clamp);
+            hu = fminf(fmaxf(hu, -p.clamp), p.clamp);
+          }
           p.dst[(size_t)chk(base + grp * kGroup + col, p.P, p.status) * p.I + chk(kOut * j + row, p.I, p.status)] =
               silu(hg) * hu;
         }
@@ -1064,6 +1069,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g1.rwi = a.opt.rwi;
   g1.aq = a.opt.aq;
   g1.ascale = a.opt.s13;
+  g1.clamp = a.opt.clamp;
 
   GemmParams g2 = g1;
   g2.ascale = a.opt.s2;

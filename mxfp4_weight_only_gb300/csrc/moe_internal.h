@@ -53,6 +53,7 @@ struct LayerOptions {
   int rwi = 0;                     // router weight on the input, unweighted combine
   int aq = 0;                      // activation quantisation of both GEMM inputs (ActQuant)
   float s13 = 1.f, s2 = 1.f;       // static FP8 input scales of the gate_up / down GEMMs
+  float clamp = 0.f;               // swiglu_limit: gate_up outputs clamped to [-clamp, clamp]; 0 = off
 };
 
 // Byte offsets of the workspace regions for one problem.

@@ -115,6 +115,7 @@ struct TcParams {
   const uint16_t* bias;  // bf16 [E][N] added to the outputs (gate_up: b13, down: b2), or null
   int rwi;            // router weight on the input: gate_up scales h by it, down adds unweighted
   int E, P;           // experts, pairs (T * topk): the bounds the checked build tests indices against
+  float clamp;        // gate_up: outputs clamped to [-clamp, clamp] before the gating (0: off)
   float ascale;       // FP8 activations: the static scale of this GEMM's input (applied to the
                       // float32 sums; the operands hold the e4m3 values); 1 otherwise
 };
@@ -727,7 +728,13 @@ __global__ void __launch_bounds__(kPThreads, 2) tc_gemm_kernel(const __grid_cons
               hg *= wt;
               hu *= wt;
             }
-            av[i] = silu(hg + bias0) * (hu + bias1);
+            hg += bias0;
+            hu += bias1;
+            if (p.clamp > 0.f) {
+              hg = fminf(fmaxf(hg, -p.clamp), p.clamp);
+              hu = fminf(fmaxf(hu, -p.clamp), p.clamp);
+            }
+            av[i] = silu(hg) * hu;
           }
           if (nvalid >= 16) {
 #pragma unroll
@@ -974,6 +981,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   p.ascale = a.opt.aq == kActFp8 ? a.opt.s13 : 1.f;
   p.E = a.E;
   p.P = (int)P;
+  p.clamp = a.opt.clamp;
   timing_mark(2, false, s);
   e = a.kind == WeightKind::kMxfp4  ? launch_tc<WeightKind::kMxfp4, true>(map_x, p, 2 * a.num_sms, s)
       : a.kind == WeightKind::kInt4 ? launch_tc<WeightKind::kInt4, true>(map_x, p, 2 * a.num_sms, s)

@@ -53,7 +53,7 @@ def test_checked_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_error_strings(lib):
-    assert lib.moe_abi_version() == 103
+    assert lib.moe_abi_version() == 104
     assert lib.moe_error_string(0) == b"ok"
     assert b"SwiGLU" in lib.moe_error_string(-4)
 
@@ -131,6 +131,9 @@ def test_option_errors_are_host_side(lib):
         assert call(MoeOptions(None, None, None, 0, 0, 2, s13, s2)) == -2
     assert call(MoeOptions(None, None, None, 0, 1, 1, 1.0, 1.0)) == -2
     assert call(MoeOptions(None, None, None, 0, 1, 2, 0.5, 0.5)) == -2
+    # swiglu_limit: finite and >= 0 (0 = off)
+    for lim in (-1.0, float("nan"), float("inf")):
+        assert call(MoeOptions(None, None, None, 0, 0, 0, 1.0, 1.0, lim)) == -2
     # not with int4 weights
     opt = MoeOptions(None, None, None, 0, 0, 1, 1.0, 1.0)
     assert lib.moe_a16w4_int4g32_ex(ctypes.byref(d), p, p, p, p, p, p, p, ctypes.byref(opt), p,

@@ -63,13 +63,13 @@ def problem(seed, E, H, I, T, topk, G=None):
     return x, ids, w, w13, s13, w2, s2, b13, b2, emap
 
 
-def run(mw, prob, path, bias, rwi, use_map, kind="mxfp4"):
+def run(mw, prob, path, bias, rwi, use_map, kind="mxfp4", limit=None):
     x, ids, w, w13, s13, w2, s2, b13, b2, emap = prob
     if kind == "int4":
         w13, s13 = requant.requant_mxfp4_to_int4g32(w13, s13)
         w2, s2 = requant.requant_mxfp4_to_int4g32(w2, s2)
-    kw = dict(router_weight_on_input=rwi)
-    okw = dict(router_weight_on_input=rwi, kind="mxfp4" if kind == "mxfp4" else "int4g32")
+    kw = dict(router_weight_on_input=rwi, swiglu_limit=limit)
+    okw = dict(router_weight_on_input=rwi, kind="mxfp4" if kind == "mxfp4" else "int4g32", swiglu_limit=limit)
     if bias:
         kw.update(w13_bias=bf16_dev(b13), w2_bias=bf16_dev(b2))
         okw.update(b13=b13, b2=b2)
@@ -123,3 +123,17 @@ def test_all_options_together_int4(mw, path):
 def test_all_options_together_mxfp4_fused(mw):
     prob = problem(78, 8, 512, 256, 6, 4, G=20)
     assert_moe_close(*run(mw, prob, DECODE, True, True, True))
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("kind", ["mxfp4", "int4"])
+def test_swiglu_limit(mw, case, kind):
+    # the gate_up outputs (bias included) clamped to [-0.4, 0.4]: about half of
+    # them are clamped here
+    path, E, H, I, T, topk = case
+    prob = problem(E * 17 + T, E, H, I, T, topk)
+    got, ref = run(mw, prob, path, True, False, False, kind=kind, limit=0.4)
+    assert_moe_close(got, ref)
+    plain = run(mw, prob, path, True, False, False, kind=kind)[1]
+    assert not np.allclose(ref, plain, rtol=1e-2)  # the clamp changes the layer
+
