@@ -124,7 +124,7 @@ def test_quantize_act_fp8_ties_and_saturation(mw):
     assert np.array_equal(q.cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("scale", [0.0123, 37.0, 3.3e-5, 1.7e30])
+@pytest.mark.parametrize("scale", [0.0123, 37.0, 3.3e-5, 1e-24, 1e23, 1.7e30])
 def test_quantize_act_fp8_near_midpoints(mw, scale):
     # v = fl32(m * scale) and its float32 neighbours, m every e4m3 midpoint:
     # quotients v / scale within a few ulps of a rounding decision (the
