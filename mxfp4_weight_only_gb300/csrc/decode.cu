@@ -171,9 +171,50 @@ __device__ __forceinline__ void load8(const void* row, int k0, float (&v)[8]) {
   }
 }
 
+// Converts this lane's activation values over the warp's blocks into f16
+// MMA fragments at scale ``sc`` (SCALED) or 1; FIND_MAX also returns their
+// largest magnitude (before any quantisation).
+template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ, bool SCALED, bool FIND_MAX>
+__device__ __forceinline__ void convert_frags(const GemmParams& p, const void* row, bool valid, int wb0, int cnt,
+                                              int t, float sc, uint32_t (&xf)[NBW][4], float& mx) {
+#pragma unroll
+  for (int bb = 0; bb < NBW; ++bb) {
+    float v[8];
+    if (valid && bb < cnt) {
+      load8<GATE_UP>(row, (wb0 + bb) * 32 + 8 * t, v);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = 0.f;
+    }
+    if (FIND_MAX) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(v[q]));
+    }
+    if (AQ) act_quant8(p.aq, p.ascale, v);  // warp-uniform: every lane calls it
+    if (SCALED) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] *= sc;
+    }
+    if (KIND == WeightKind::kMxfp4) {
+      xf[bb][0] = f32x2_to_f16x2(v[0], v[1]);
+      xf[bb][1] = f32x2_to_f16x2(v[2], v[3]);
+      xf[bb][2] = f32x2_to_f16x2(v[4], v[5]);
+      xf[bb][3] = f32x2_to_f16x2(v[6], v[7]);
+    } else {
+      xf[bb][0] = f32x2_to_f16x2(v[0], v[4]);
+      xf[bb][1] = f32x2_to_f16x2(v[1], v[5]);
+      xf[bb][2] = f32x2_to_f16x2(v[2], v[6]);
+      xf[bb][3] = f32x2_to_f16x2(v[3], v[7]);
+    }
+  }
+}
+
 // Activation fragments of one 8-pair column block (pairs slot0 + g, g = lane/4)
 // over the calling warp's blocks [wb0, wb0 + cnt), as f16 scaled by a power of
 // two per pair; inv receives the undo factors for accumulator columns 2t, 2t+1.
+// One pass converts at scale 1 and finds each range's largest magnitude; only
+// when some range of the warp needs a power of two other than 1 does a second
+// pass convert again (one global-memory round trip in the common case).
 // AQ: the kernel variant for quantised activations (p.aq); the plain variant
 // carries none of that code.
 template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
@@ -191,15 +232,7 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
     }
   }
   float mx = 0.f;
-#pragma unroll
-  for (int bb = 0; bb < NBW; ++bb) {
-    if (valid && bb < cnt) {
-      float v[8];
-      load8<GATE_UP>(row, (wb0 + bb) * 32 + 8 * t, v);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(v[q]));
-    }
-  }
+  convert_frags<KIND, GATE_UP, NBW, AQ, false, true>(p, row, valid, wb0, cnt, t, 1.f, xf, mx);
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   // power of two taking the range's largest magnitude into [2^14, 2^15) --
@@ -218,30 +251,9 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
     const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
     ex = (lg >= -4 && lg <= 14) ? 0 : min(max(14 - lg, -126), 126);
   }
-  const float sc = exp2_int(ex);
-#pragma unroll
-  for (int bb = 0; bb < NBW; ++bb) {
-    float v[8];
-    if (valid && bb < cnt) {
-      load8<GATE_UP>(row, (wb0 + bb) * 32 + 8 * t, v);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = 0.f;
-    }
-    if (AQ) act_quant8(p.aq, p.ascale, v);  // warp-uniform: every lane calls it
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] *= sc;
-    if (KIND == WeightKind::kMxfp4) {
-      xf[bb][0] = f32x2_to_f16x2(v[0], v[1]);
-      xf[bb][1] = f32x2_to_f16x2(v[2], v[3]);
-      xf[bb][2] = f32x2_to_f16x2(v[4], v[5]);
-      xf[bb][3] = f32x2_to_f16x2(v[6], v[7]);
-    } else {
-      xf[bb][0] = f32x2_to_f16x2(v[0], v[4]);
-      xf[bb][1] = f32x2_to_f16x2(v[1], v[5]);
-      xf[bb][2] = f32x2_to_f16x2(v[2], v[6]);
-      xf[bb][3] = f32x2_to_f16x2(v[3], v[7]);
-    }
+  if (__any_sync(0xffffffffu, ex != 0)) {
+    float unused = 0.f;
+    convert_frags<KIND, GATE_UP, NBW, AQ, true, false>(p, row, valid, wb0, cnt, t, exp2_int(ex), xf, unused);
   }
   const int ex0 = __shfl_sync(0xffffffffu, ex, (2 * t) * 4);
   const int ex1 = __shfl_sync(0xffffffffu, ex, (2 * t + 1) * 4);
