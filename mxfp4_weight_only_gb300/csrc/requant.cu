@@ -15,12 +15,13 @@
 // therefore depends only on the two codes: tables built at kernel start with
 // the same IEEE round-to-nearest divisions give, per cmax, the output byte of
 // every packed input byte (two signed codes), so a group costs sixteen
-// shared-memory byte loads instead of 32 divisions (an earlier version
-// applied an 8-entry table four nibbles at a time with byte permutes and a
-// separate sign select: 223 instructions per group, ALU-bound); likewise
-// fl32(amax / 7) = fl32(cmax / 7) * 2^(s-127).  Groups whose scale byte puts values near the subnormal range or
-// near overflow take the per-element division path, so results are bit-exact
-// for every scale byte in [0, 252].
+// shared-memory byte loads, each addressed by one byte permute, instead of
+// 32 divisions; likewise fl32(amax / 7) = fl32(cmax / 7) * 2^(s-127).  The
+// largest code itself comes from byte permutes (one-hot bytes, then the
+// highest set bit of their OR), which keeps the integer work per group below
+// the HBM time.  Groups whose scale byte puts values near the subnormal range
+// or near overflow take the per-element division path, so results are
+// bit-exact for every scale byte in [0, 252].
 //
 // bf16 scales (the "groupwise bf16 scales" of the PR #51274 commit message):
 // the scale is rounded to bf16 (nearest even) before the elements are divided
@@ -47,10 +48,12 @@ __device__ __forceinline__ float e2m1_mag(uint32_t c) {
 }
 
 // One packed word (four bytes, eight E2M1 codes) -> its four output bytes
-// (eight int4 codes) through the byte table of the group's largest code.
-__device__ __forceinline__ uint32_t lookup_word(uint32_t w, const uint8_t* tab) {
-  const uint32_t b0 = tab[w & 0xFFu], b1 = tab[(w >> 8) & 0xFFu];
-  const uint32_t b2 = tab[(w >> 16) & 0xFFu], b3 = tab[w >> 24];
+// (eight int4 codes) through the byte table of the group's largest code:
+// row_sel = cmax << 8, so one byte permute forms each entry's index
+// cmax * 256 + byte into the [8][256] table.
+__device__ __forceinline__ uint32_t lookup_word(uint32_t w, uint32_t row_sel, const uint8_t* tab) {
+  const uint32_t b0 = tab[prmt(w, row_sel, 0x7650u)], b1 = tab[prmt(w, row_sel, 0x7651u)];
+  const uint32_t b2 = tab[prmt(w, row_sel, 0x7652u)], b3 = tab[prmt(w, row_sel, 0x7653u)];
   return prmt(prmt(b0, b1, 0x0040u), prmt(b2, b3, 0x0040u), 0x5410u);
 }
 
@@ -62,16 +65,18 @@ template <bool BF16>
 __device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const uint8_t (*ltab)[256],
                                               const float* lut_s, uint4& q_out, float& s_out) {
   const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-  // largest magnitude code in the group
-  uint32_t m = 0;
+  // largest magnitude code in the group: a byte permute turns four
+  // magnitudes (selector nibbles, sign bits cleared) into one-hot bytes
+  // 1 << m, the OR of all of them has bit cmax as its highest
+  uint32_t oh = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t mg = wd[i] & 0x77777777u;
-    m = __vmaxu4(m, __vmaxu4(mg & 0x0F0F0F0Fu, (mg >> 4) & 0x0F0F0F0Fu));
+    oh |= prmt(0x08040201u, 0x80402010u, mg) | prmt(0x08040201u, 0x80402010u, mg >> 16);
   }
-  m = __vmaxu4(m, m >> 16);
-  m = __vmaxu4(m, m >> 8);
-  const uint32_t cmax = m & 0xFu;
+  oh |= oh >> 16;
+  oh |= oh >> 8;
+  const uint32_t cmax = 31u - __clz((oh & 0xFFu) | 1u);
   const float sc_unit = e8m0_to_float(s);
   uint32_t oq[4];
   float oscale;
@@ -83,9 +88,8 @@ __device__ __forceinline__ void requant_group(const uint4& v, uint32_t s, const 
     // normal float for these scale bytes, so the power of two commutes with
     // the rounding
     oscale = lut_s[cmax] * sc_unit;
-    const uint8_t* tab = ltab[cmax];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) oq[i] = lookup_word(wd[i], tab);
+    for (int i = 0; i < 4; ++i) oq[i] = lookup_word(wd[i], cmax << 8, &ltab[0][0]);
   } else {
     // exact per-element path (values near the subnormal range or near overflow)
     const float amax = e2m1_mag(cmax) * sc_unit;
@@ -116,8 +120,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t* __restrict__ w,
                                                                   const uint8_t* __restrict__ scale,
                                                                   uint8_t* __restrict__ out_q,
-                                                                  void* __restrict__ out_s,
-                                                                  long long n_groups) {
+                                                                  void* __restrict__ out_s, int n_groups) {
   // per cmax (largest magnitude code of a group, 1..7): fl32(cmax / 7), the
   // int4 code of each signed E2M1 code, and from those the output byte of
   // every packed byte (two codes)
@@ -149,14 +152,14 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
 
   // kGroupsPerIter groups per thread and iteration, all loads issued before
   // any arithmetic, so that many 16-byte loads per thread are in flight
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n_groups;
-       g += kGroupsPerIter * stride) {
+  // 32-bit group indices (the host launches at most 2^30 groups at a time)
+  const int stride = gridDim.x * blockDim.x;
+  for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < n_groups; g += kGroupsPerIter * stride) {
     uint4 v[kGroupsPerIter];
     uint32_t sb[kGroupsPerIter];
 #pragma unroll
     for (int i = 0; i < kGroupsPerIter; ++i) {
-      const long long gi = g + i * stride;
+      const int gi = g + i * stride;
       v[i] = make_uint4(0, 0, 0, 0);
       sb[i] = 0;
       if (gi < n_groups) {
@@ -166,13 +169,14 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
     }
 #pragma unroll
     for (int i = 0; i < kGroupsPerIter; ++i) {
-      const long long gi = g + i * stride;
+      const int gi = g + i * stride;
       if (gi < n_groups) {
         uint4 q;
         float o;
         requant_group<BF16>(v[i], sb[i], ltab, lut_s, q, o);
         __stcs(reinterpret_cast<uint4*>(out_q) + gi, q);
-        if (BF16) reinterpret_cast<uint16_t*>(out_s)[gi] = (uint16_t)(__float_as_uint(o) >> 16);  // exact
+        // (o is a bf16 value here: its high half is exact)
+        if (BF16) __stcs(reinterpret_cast<unsigned short*>(out_s) + gi, (unsigned short)(__float_as_uint(o) >> 16));
         else __stcs(reinterpret_cast<float*>(out_s) + gi, o);
       }
     }
@@ -195,12 +199,23 @@ cudaError_t launch_requant(const uint8_t* w, const uint8_t* scale, uint8_t* out_
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_kernel<false>, kRequantThreads, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
-  const long long want = (n_groups + kRequantThreads - 1) / kRequantThreads;
-  const long long resident = (long long)sms * per_sm;
-  const int grid = (int)(want < resident ? want : resident);
-  if (bf16) requant_kernel<true><<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
-  else requant_kernel<false><<<grid, kRequantThreads, 0, s>>>(w, scale, out_q, out_s, n_groups);
-  return cudaGetLastError();
+  // pieces of at most 2^30 groups, so that the kernel indexes in 32 bits
+  constexpr long long kPiece = 1ll << 30;
+  for (long long g0 = 0; g0 < n_groups; g0 += kPiece) {
+    const int n = (int)(n_groups - g0 < kPiece ? n_groups - g0 : kPiece);
+    const long long want = (n + kRequantThreads - 1) / kRequantThreads;
+    const long long resident = (long long)sms * per_sm;
+    const int grid = (int)(want < resident ? want : resident);
+    if (bf16)
+      requant_kernel<true><<<grid, kRequantThreads, 0, s>>>(w + g0 * 16, scale + g0, out_q + g0 * 16,
+                                                          reinterpret_cast<uint16_t*>(out_s) + g0, n);
+    else
+      requant_kernel<false><<<grid, kRequantThreads, 0, s>>>(w + g0 * 16, scale + g0, out_q + g0 * 16,
+                                                           reinterpret_cast<float*>(out_s) + g0, n);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace moe
