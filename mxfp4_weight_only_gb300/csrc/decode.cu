@@ -128,18 +128,27 @@ __device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c
 // With n = q + 8 (offset binary), n placed in the low mantissa bits of f16
 // 1024 gives 1024 + n (minus 1032: q); n placed 4 bits higher gives 1024 + 16n
 // (times 1/16 minus 72: q); one byte permute brings nibbles 2, 3, 6, 7 down.
+// Flipping a nibble's top bit (q -> q + 8) and setting the exponent bits of
+// 1024 touch disjoint bits of the masked word, so (w & mask) ^ (flip | 1024)
+// does both in one logic operation.
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(a), "r"(b), "r"(c));  // (a & b) ^ c
+  return r;
+}
+
 __device__ __forceinline__ void int4x8_to_f16x8(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2,
                                                 uint32_t& o3) {
-  const uint32_t u = w ^ 0x88888888u;   // offset binary: q + 8
-  const uint32_t v = prmt(u, 0u, 0x4341u);  // bytes 1 and 3 of u into bytes 0 and 2
-  const uint32_t magic = 0x64006400u;   // f16 1024 in both halves
-  const uint32_t bias = 0x64086408u;    // f16 1032
-  const uint32_t sixteenth = 0x2C002C00u;  // f16 1/16
-  const uint32_t m72 = 0xD480D480u;     // f16 -72
-  o0 = f16x2_sub((u & 0x000F000Fu) | magic, bias);
-  o1 = f16x2_fma((u & 0x00F000F0u) | magic, sixteenth, m72);
-  o2 = f16x2_sub((v & 0x000F000Fu) | magic, bias);
-  o3 = f16x2_fma((v & 0x00F000F0u) | magic, sixteenth, m72);
+  const uint32_t v = prmt(w, 0u, 0x4341u);  // bytes 1 and 3 of w into bytes 0 and 2
+  const uint32_t lo = 0x64086408u;          // f16 1024 | the flip of the low nibble's top bit (bit 3)
+  const uint32_t hi = 0x64806480u;          // f16 1024 | the flip of the high nibble's top bit (bit 7)
+  const uint32_t bias = 0x64086408u;        // f16 1032
+  const uint32_t sixteenth = 0x2C002C00u;   // f16 1/16
+  const uint32_t m72 = 0xD480D480u;         // f16 -72
+  o0 = f16x2_sub(and_xor(w, 0x000F000Fu, lo), bias);
+  o1 = f16x2_fma(and_xor(w, 0x00F000F0u, hi), sixteenth, m72);
+  o2 = f16x2_sub(and_xor(v, 0x000F000Fu, lo), bias);
+  o3 = f16x2_fma(and_xor(v, 0x00F000F0u, hi), sixteenth, m72);
 }
 
 // Two E8M0 bytes (low byte = first) -> their values 2^(s-127) as floats, exact
