@@ -261,17 +261,24 @@ __device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c
 // (K order, lower element in the low half): bf16(fl32(q * s)).  Byte j goes
 // to bytes 0 and 2 of a word; masking keeps its low nibble in the low half
 // and its high nibble 4 bits up in the high half, placed in the mantissa of
-// f16 1024; one f16x2 FMA (x1, x1/16 and -1032, -72) leaves the two exact q.
+// f16 1024 with each nibble's top bit flipped (q + 8, offset binary; one
+// logic operation with the masking, the bits being disjoint); one f16x2 FMA
+// (x1, x1/16 and -1032, -72) leaves the two exact q.
+__device__ __forceinline__ uint32_t int4_pair_f16(uint32_t w, int j) {
+  const uint32_t v = prmt(w, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
+  uint32_t m;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(m) : "r"(v), "r"(0x00F0000Fu), "r"(0x64806408u));  // (v & mask) ^ c
+  return f16x2_fma(m, 0x2C003C00u, 0xD480E408u);
+}
+
 __device__ __forceinline__ void dequant_block_int4(const uint4& q, float s, uint4 (&out)[4]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t u = w[i] ^ 0x88888888u;  // offset binary: q + 8
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t v = prmt(u, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
-      const uint32_t h = f16x2_fma((v & 0x00F0000Fu) | 0x64006400u, 0x2C003C00u, 0xD480E408u);
+      const uint32_t h = int4_pair_f16(w[i], j);
       float lo, hi;
       asm("{\n .reg .f16 l, u;\n mov.b32 {l, u}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, u;\n}"
           : "=f"(lo), "=f"(hi)
@@ -321,13 +328,9 @@ __device__ __forceinline__ void dequant_block_int4_f16(const uint4& q, float s, 
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t u = w[i] ^ 0x88888888u;  // offset binary: q + 8
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t v = prmt(u, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
-      o[j] = f16x2_mul(f16x2_fma((v & 0x00F0000Fu) | 0x64006400u, 0x2C003C00u, 0xD480E408u), sc);
-    }
+    for (int j = 0; j < 4; ++j) o[j] = f16x2_mul(int4_pair_f16(w[i], j), sc);
     out[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
