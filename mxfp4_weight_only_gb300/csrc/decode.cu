@@ -92,7 +92,7 @@ struct GemmParams {
   int G;                   // entries of emap
   int rwi;                 // router weight on the input (gate_up scales h), unweighted combine
   int aq;                  // activation quantisation of this GEMM's input (ActQuant)
-  float ascale;            // kActFp8: the input's static scale, applied to the float32 sums
+  float ascale;            // kActFp8: the input's static scale, applied to the reduced float32 sums
   float clamp;             // gate_up: outputs clamped to [-clamp, clamp] before the gating (0: off)
 };
 
@@ -254,7 +254,7 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   // Quantised activations (p.aq): MXFP4 values code * 2^(s-127) are at most
   // 6/5 of their block's largest magnitude, so the same power of two keeps
   // them below 2^15 * 1.2 (finite in f16); FP8 leaves the e4m3 values (exact
-  // in f16, at most 448) unscaled and folds the static scale into inv.
+  // in f16, at most 448) unscaled.
   int ex = 0;
   if (mx > 0.f && !(AQ && p.aq == kActFp8)) {
     const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
@@ -268,10 +268,8 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   const int ex1 = __shfl_sync(0xffffffffu, ex, (2 * t + 1) * 4);
   inv[0] = exp2_int(-ex0);
   inv[1] = exp2_int(-ex1);
-  if (AQ && p.aq == kActFp8) {
-    inv[0] = p.ascale;  // ex is 0 for FP8
-    inv[1] = p.ascale;
-  }
+  // (FP8: ex is 0 and inv 1; the static scale multiplies the reduced sums in
+  // the epilogue, once per output, so the main loop needs no folded scales)
 }
 
 // Scales of rows r and r+8 of one 16-row tile for blocks b, b+1 (b even).
@@ -668,6 +666,10 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
           hu += rb[w * kRows * kGroup + (row + kOut) * kGroup + col];
         }
         if (my_pair >= 0) {
+          if (p.aq == kActFp8) {  // FP8 inputs: the static scale, once per output
+            hg *= p.ascale;
+            hu *= p.ascale;
+          }
           // h = (router weight) * W13 x + b13: the weight on the input scales
           // the GEMM's output exactly as it would scale x
           if (p.rwi) {
@@ -694,6 +696,7 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) y += rb[w * kRows * kGroup + row * kGroup + col];
         if (my_pair >= 0) {
+          if (p.aq == kActFp8) y *= p.ascale;  // FP8 inputs: the static scale, once per output
           if (bias) y += bf16_lo(bias[kRows * j + row]);
           p.dst[(size_t)my_pair * p.N + chk(kRows * j + row, p.N, p.status)] = y;
         }
