@@ -183,7 +183,7 @@ __device__ __forceinline__ void load8(const void* row, int k0, float (&v)[8]) {
 // Converts this lane's activation values over the warp's blocks into f16
 // MMA fragments at scale ``sc`` (SCALED) or 1; FIND_MAX also returns their
 // largest magnitude (before any quantisation).
-template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ, bool SCALED, bool FIND_MAX>
+template <WeightKind KIND, bool GATE_UP, int NBW, int AQ, bool SCALED, bool FIND_MAX>
 __device__ __forceinline__ void convert_frags(const GemmParams& p, const void* row, bool valid, int wb0, int cnt,
                                               int t, float sc, uint32_t (&xf)[NBW][4], float& mx) {
 #pragma unroll
@@ -199,7 +199,7 @@ __device__ __forceinline__ void convert_frags(const GemmParams& p, const void* r
 #pragma unroll
       for (int q = 0; q < 8; ++q) mx = fmaxf(mx, fabsf(v[q]));
     }
-    if (AQ) act_quant8(p.aq, p.ascale, v);  // warp-uniform: every lane calls it
+    if (AQ != kActNone) act_quant8(AQ, p.ascale, v);  // warp-uniform: every lane calls it
     if (SCALED) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) v[q] *= sc;
@@ -224,9 +224,10 @@ __device__ __forceinline__ void convert_frags(const GemmParams& p, const void* r
 // One pass converts at scale 1 and finds each range's largest magnitude; only
 // when some range of the warp needs a power of two other than 1 does a second
 // pass convert again (one global-memory round trip in the common case).
-// AQ: the kernel variant for quantised activations (p.aq); the plain variant
-// carries none of that code.
-template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
+// AQ: the activation quantisation the kernel variant applies (ActQuant, a
+// compile-time mode, so each variant carries only its own quantiser and the
+// plain variant none).
+template <WeightKind KIND, bool GATE_UP, int NBW, int AQ>
 __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* spair, int slot0, int base, int npairs,
                                            int wb0, int cnt, int g, int t, uint32_t (&xf)[NBW][4], float (&inv)[2]) {
   const int slot = slot0 + g;
@@ -256,7 +257,7 @@ __device__ __forceinline__ void load_frags(const GemmParams& p, const int32_t* s
   // them below 2^15 * 1.2 (finite in f16); FP8 leaves the e4m3 values (exact
   // in f16, at most 448) unscaled.
   int ex = 0;
-  if (mx > 0.f && !(AQ && p.aq == kActFp8)) {
+  if (mx > 0.f && AQ != kActFp8) {
     const int lg = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2), normal mx
     ex = (lg >= -4 && lg <= 14) ? 0 : min(max(14 - lg, -126), 126);
   }
@@ -758,7 +759,7 @@ __device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t
 // Consumer warps: split K, MMA each unit's weight rows against up to 8
 // activation columns held in registers, hand the partial sums to the
 // epilogue warp.
-template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
+template <WeightKind KIND, bool GATE_UP, int NBW, int AQ>
 __device__ void consume_units(const GemmParams& p, const Grouping& gr, const UnitRange& r, const CtaSmem& c,
                               RingPos& wr, RingPos& rr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -828,7 +829,7 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
 // ------------------------------------------------------------------ kernels
 
 // One GEMM stage (gate_up with the activation, or down) as its own launch.
-template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
+template <WeightKind KIND, bool GATE_UP, int NBW, int AQ>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const CtaSmem c = carve_smem(smem);
@@ -872,7 +873,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemm_kernel(const GemmP
 // units, measured slower: every CTA then reloads its activation fragments in
 // twice as many places, and each reload is a global-memory round trip of
 // about 2 us under the full weight stream.)
-template <WeightKind KIND, int NBW, bool AQ>
+template <WeightKind KIND, int NBW, int AQ>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const GemmParams p1, const GemmParams p2) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const CtaSmem c = carve_smem(smem);
@@ -980,7 +981,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
   *reinterpret_cast<uint2*>(out + (size_t)t * H + 4 * c4) = o;
 }
 
-template <WeightKind KIND, bool GATE_UP, int NBW, bool AQ>
+template <WeightKind KIND, bool GATE_UP, int NBW, int AQ>
 cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
   const size_t smem = kSmemFixed + (size_t)gp.n_stages * gp.stage_bytes;
   auto kern = decode_gemm_kernel<KIND, GATE_UP, NBW, AQ>;
@@ -992,7 +993,7 @@ cudaError_t launch_gemm(const GemmParams& gp, int grid, cudaStream_t s) {
 // activation blocks of 32 per consumer warp (even), which sizes the register fragments
 int blocks_per_warp(int K) { return 2 * (((K >> 5) + 2 * kConsumerWarps - 1) / (2 * kConsumerWarps)); }
 
-template <WeightKind KIND, bool GATE_UP, bool AQ>
+template <WeightKind KIND, bool GATE_UP, int AQ>
 cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
   const int nbw = blocks_per_warp(gp.K);
   if (nbw <= 8) return launch_gemm<KIND, GATE_UP, 8, AQ>(gp, grid, s);
@@ -1004,10 +1005,11 @@ cudaError_t dispatch_nbw(const GemmParams& gp, int grid, cudaStream_t s) {
 // activations (the library rejects the combination).
 template <bool GATE_UP>
 cudaError_t dispatch_gemm(const GemmParams& gp, WeightKind kind, int grid, cudaStream_t s) {
-  if (kind == WeightKind::kInt4) return dispatch_nbw<WeightKind::kInt4, GATE_UP, false>(gp, grid, s);
-  if (kind == WeightKind::kInt4Bf16) return dispatch_nbw<WeightKind::kInt4Bf16, GATE_UP, false>(gp, grid, s);
-  return gp.aq != kActNone ? dispatch_nbw<WeightKind::kMxfp4, GATE_UP, true>(gp, grid, s)
-                           : dispatch_nbw<WeightKind::kMxfp4, GATE_UP, false>(gp, grid, s);
+  if (kind == WeightKind::kInt4) return dispatch_nbw<WeightKind::kInt4, GATE_UP, kActNone>(gp, grid, s);
+  if (kind == WeightKind::kInt4Bf16) return dispatch_nbw<WeightKind::kInt4Bf16, GATE_UP, kActNone>(gp, grid, s);
+  if (gp.aq == kActMxfp4) return dispatch_nbw<WeightKind::kMxfp4, GATE_UP, kActMxfp4>(gp, grid, s);
+  if (gp.aq == kActFp8) return dispatch_nbw<WeightKind::kMxfp4, GATE_UP, kActFp8>(gp, grid, s);
+  return dispatch_nbw<WeightKind::kMxfp4, GATE_UP, kActNone>(gp, grid, s);
 }
 
 // The fused kernel holds fragments for up to 8 blocks per warp (K <= 3584 in
@@ -1019,7 +1021,7 @@ constexpr int kFusedNbw = 8;
 // wait on one another, so it is launched as a cooperative grid of this size:
 // the launch then either places every CTA at once or fails, instead of
 // leaving CTAs waiting for others that cannot be scheduled.
-template <WeightKind KIND, bool AQ>
+template <WeightKind KIND, int AQ>
 int fused_resident_ctas(size_t smem, int sms) {
   auto kern = decode_fused_kernel<KIND, kFusedNbw, AQ>;
   int dev = 0, coop = 0, per_sm = 0;
@@ -1030,7 +1032,7 @@ int fused_resident_ctas(size_t smem, int sms) {
   return per_sm * sms;
 }
 
-template <WeightKind KIND, bool AQ>
+template <WeightKind KIND, int AQ>
 cudaError_t launch_fused(const GemmParams& g1, const GemmParams& g2, int grid, cudaStream_t s) {
   const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
   auto kern = decode_fused_kernel<KIND, kFusedNbw, AQ>;
@@ -1106,7 +1108,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   g2.dst = a.ybuf;
   g2.bias = a.opt.b2;
 
-  const bool aq = a.opt.aq != kActNone;  // MXFP4 weights only (checked by the library)
+  const int aq = a.opt.aq;  // quantised activations: MXFP4 weights only (checked by the library)
   // one launch for both GEMMs when both fit the fused kernel's fragments and a
   // resident grid fits the flag array
   bool fused = a.sync != nullptr && blocks_per_warp(a.H) <= kFusedNbw && blocks_per_warp(a.I) <= kFusedNbw;
@@ -1115,10 +1117,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     fill_stage_geometry(g1, a.kind, &g2);
     fill_stage_geometry(g2, a.kind, &g1);
     const size_t smem = kSmemFixed + (size_t)g1.n_stages * g1.stage_bytes;
-    fused_grid = a.kind == WeightKind::kInt4       ? fused_resident_ctas<WeightKind::kInt4, false>(smem, a.num_sms)
-                 : a.kind == WeightKind::kInt4Bf16 ? fused_resident_ctas<WeightKind::kInt4Bf16, false>(smem, a.num_sms)
-                 : aq ? fused_resident_ctas<WeightKind::kMxfp4, true>(smem, a.num_sms)
-                      : fused_resident_ctas<WeightKind::kMxfp4, false>(smem, a.num_sms);
+    fused_grid = a.kind == WeightKind::kInt4 ? fused_resident_ctas<WeightKind::kInt4, kActNone>(smem, a.num_sms)
+                 : a.kind == WeightKind::kInt4Bf16
+                     ? fused_resident_ctas<WeightKind::kInt4Bf16, kActNone>(smem, a.num_sms)
+                 : aq == kActMxfp4 ? fused_resident_ctas<WeightKind::kMxfp4, kActMxfp4>(smem, a.num_sms)
+                 : aq == kActFp8   ? fused_resident_ctas<WeightKind::kMxfp4, kActFp8>(smem, a.num_sms)
+                                   : fused_resident_ctas<WeightKind::kMxfp4, kActNone>(smem, a.num_sms);
     g1.wait_extra = a.wait.extra_waiters;
     fused = fused_grid >= 1 && g1.n_stages >= 2 && fused_grid + a.wait.extra_waiters <= kMaxSyncCtas;
   }
@@ -1132,10 +1136,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e;
   if (fused) {
     timing_mark(1, false, s);
-    e = a.kind == WeightKind::kInt4       ? launch_fused<WeightKind::kInt4, false>(g1, g2, fused_grid, s)
-        : a.kind == WeightKind::kInt4Bf16 ? launch_fused<WeightKind::kInt4Bf16, false>(g1, g2, fused_grid, s)
-        : aq ? launch_fused<WeightKind::kMxfp4, true>(g1, g2, fused_grid, s)
-             : launch_fused<WeightKind::kMxfp4, false>(g1, g2, fused_grid, s);
+    e = a.kind == WeightKind::kInt4       ? launch_fused<WeightKind::kInt4, kActNone>(g1, g2, fused_grid, s)
+        : a.kind == WeightKind::kInt4Bf16 ? launch_fused<WeightKind::kInt4Bf16, kActNone>(g1, g2, fused_grid, s)
+        : aq == kActMxfp4                 ? launch_fused<WeightKind::kMxfp4, kActMxfp4>(g1, g2, fused_grid, s)
+        : aq == kActFp8                   ? launch_fused<WeightKind::kMxfp4, kActFp8>(g1, g2, fused_grid, s)
+                                          : launch_fused<WeightKind::kMxfp4, kActNone>(g1, g2, fused_grid, s);
     timing_mark(1, true, s);
     if (e != cudaSuccess) {
       // a cooperative grid that cannot be placed (for example under an SM
