@@ -46,7 +46,11 @@ constexpr int kTiles = 2;             // 16-row MMA tiles per item
 constexpr int kRows = 16 * kTiles;    // weight rows per item
 constexpr int kGroup = 8;             // pair columns per group (one 8-column MMA block)
 constexpr int kRedFloats = kConsumerWarps * kRows * kGroup;  // one reduction buffer
-constexpr int kRedBufs = 3;                                  // reduction ring depth
+// reduction ring depth: two buffers keep the consumers ahead of the epilogue
+// warp (whose per-unit work is short) and leave room for a third weight stage
+// of int4 with bf16 scales (65 KB stages; with three buffers only two fit:
+// int4 bf16-scale decode 6-7 % slower, the other kinds unchanged)
+constexpr int kRedBufs = 2;
 static_assert(kGroup == kMoeGroup, "routing and the decode kernels must agree on the group size");
 
 
