@@ -408,38 +408,18 @@ def run_ours(args, rank: int, world: int):
     hin = [torch.from_numpy(np.concatenate([b[0].view(np.uint8).ravel(), b[1].view(np.uint8).ravel(),
                                             b[2].view(np.uint8).ravel()])).pin_memory() for b in hb]
     hout = [torch.empty((T, SHAPE.H), dtype=torch.int16).pin_memory() for _ in range(ROTATE)]
-    # two device buffers each way, so that a step's upload (on its own stream)
-    # overlaps the previous step's kernels and its download (on a third
-    # stream) the next step's kernels, as a serving loop would run them;
-    # events order each buffer's reuse
-    din = [torch.empty(nbx + 2 * nbi, dtype=torch.uint8, device=dev) for _ in range(2)]
-    dxs = [d[:nbx].view(torch.bfloat16).view(T, SHAPE.H) for d in din]
-    dids = [d[nbx:nbx + nbi].view(torch.int32).view(T, SHAPE.topk) for d in din]
-    dws = [d[nbx + nbi:].view(torch.float32).view(T, SHAPE.topk) for d in din]
-    dout = [torch.empty((T, SHAPE.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # upload b done
-    ev_used = [torch.cuda.Event() for _ in range(2)]    # kernels that read din[b] / wrote dout[b] done
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # download of dout[b] done
-    for b in range(2):
-        for e in (ev_used[b], ev_out[b]):
-            e.record(stream)
+    din = torch.empty(nbx + 2 * nbi, dtype=torch.uint8, device=dev)
+    dx = din[:nbx].view(torch.bfloat16).view(T, SHAPE.H)
+    dids = din[nbx:nbx + nbi].view(torch.int32).view(T, SHAPE.topk)
+    dw = din[nbx + nbi:].view(torch.float32).view(T, SHAPE.topk)
+    dout = torch.empty((T, SHAPE.H), dtype=torch.bfloat16, device=dev)
 
     def e2e_steps(n):
         for i in range(n):
-            r, b = i % ROTATE, i % 2
-            up.wait_event(ev_used[b])
-            with torch.cuda.stream(up):
-                din[b].copy_(hin[r], non_blocking=True)
-            ev_in[b].record(up)
-            stream.wait_event(ev_in[b])
-            stream.wait_event(ev_out[b])
-            m.moe_a16w4_mxfp4(dxs[b], dids[b], dws[b], *copies[i % len(copies)], out=dout[b], workspace=ws1)
-            ev_used[b].record(stream)
-            down.wait_event(ev_used[b])
-            with torch.cuda.stream(down):
-                hout[r].copy_(dout[b].view(torch.int16), non_blocking=True)
-            ev_out[b].record(down)
+            r = i % ROTATE
+            din.copy_(hin[r], non_blocking=True)
+            m.moe_a16w4_mxfp4(dx, dids, dw, *copies[i % len(copies)], out=dout, workspace=ws1)
+            hout[r].copy_(dout.view(torch.int16), non_blocking=True)
 
     with torch.cuda.stream(stream):
         e2e_steps(max(W, 3))
@@ -447,9 +427,7 @@ def run_ours(args, rank: int, world: int):
         barrier()
         s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s_ev.record()
-        up.wait_event(s_ev)  # the first upload starts inside the timed region
         e2e_steps(K)
-        stream.wait_event(ev_out[(K - 1) % 2])  # the last download is inside the timed region
         e_ev.record()
         stream.synchronize()
     e2e_ms = max_over_ranks(s_ev.elapsed_time(e_ev), world, dev)
@@ -488,10 +466,7 @@ def run_ours(args, rank: int, world: int):
                                            "distinct active experts x 11,698,176 B (w13 + E8M0 scales) per launch")},
         "kernels_us": {k: round(v, 2) for k, v in kavg.items()},
         "gpu_launches": launches_per_step * K,
-        "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "per step: pinned-host upload of x, ids and weights (one copy), the library call, "
-                       "download of the output; uploads and downloads on their own streams overlap the "
-                       "neighbouring steps' kernels (two device buffers each way, event-ordered)"},
+        "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks, "status": status, "wall_s": round(wall, 4),
         "cpu_baseline": cpu, "rows": rows,
     }
