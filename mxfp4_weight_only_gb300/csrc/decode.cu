@@ -719,6 +719,16 @@ __device__ void reduce_units(const GemmParams& p, const Grouping& gr, const Unit
 // With FOLD the scale is multiplied by each pair column's power-of-two undo
 // first, so the partial sums stay at the magnitude of the result (no float32
 // overflow for large block scales with tiny, up-scaled activations).
+// Four 8x8 matrices of 16-bit elements from shared memory: lane L supplies the
+// row address of row L % 8 of matrix L / 8 and receives, from each matrix, the
+// 4 bytes of row L / 4 at byte offset 4 (L % 4) -- for packed weight rows the
+// same words the MMA fragments take.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 template <WeightKind KIND, int NBW, bool FOLD>
 __device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t* sw, const uint8_t* ss, int wb0,
                                               int cnt, int g, int t, const uint32_t (&xf)[NBW][4],
@@ -726,6 +736,10 @@ __device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t
 #pragma unroll
   for (int tl = 0; tl < kTiles; ++tl) acc[tl][0] = acc[tl][1] = acc[tl][2] = acc[tl][3] = 0.f;
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  // this lane's row address for the weight loads: matrices 0 / 1 = rows 0-7 /
+  // 8-15 of the tile in block b, matrices 2 / 3 the same in block b + 1
+  const int lane = threadIdx.x & 31, mat = lane >> 3;
+  const uint32_t wrow = smem_u32(sw) + ((lane & 7) + 8 * (mat & 1)) * p.row_stride + (mat >> 1) * 16 + wb0 * 16;
 #pragma unroll
   for (int bb = 0; bb < NBW; bb += 2) {
     if (bb < cnt) {
@@ -743,12 +757,13 @@ __device__ __forceinline__ void unit_mainloop(const GemmParams& p, const uint8_t
             if (FOLD) mul_f32x2_bcast(m[r2][h][0], m[r2][h][1], sc[r2][h], inv[0], inv[1]);
             else m[r2][h][0] = m[r2][h][1] = sc[r2][h];
           }
+        uint32_t wq[2][2];  // [block b / b+1][row g / g+8]: 8 packed weights each
+        ldsm_x4(wrow + 16 * tl * p.row_stride + bb * 16, wq[0][0], wq[0][1], wq[1][0], wq[1][1]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint8_t* rg = sw + row * p.row_stride + (b + h) * 16 + 4 * t;
           uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-          weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg), a0, a1, a2, a3);
-          weights_to_f16<KIND>(*reinterpret_cast<const uint32_t*>(rg + 8 * p.row_stride), c0, c1, c2, c3);
+          weights_to_f16<KIND>(wq[h][0], a0, a1, a2, a3);
+          weights_to_f16<KIND>(wq[h][1], c0, c1, c2, c3);
           float dd[4];
           mma_f16_16816(dd, a0, c0, a1, c1, xf[bb + h][0], xf[bb + h][1], zero);
           mma_f16_16816(dd, a2, c2, a3, c3, xf[bb + h][2], xf[bb + h][3], dd);
