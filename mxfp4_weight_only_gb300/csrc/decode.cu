@@ -794,6 +794,7 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
   float inv[2];  // power-of-two undo for accumulator columns 2t, 2t+1
   bool fold = false;  // some column of this warp scaled: undo folded into the block scales
   int cur_e = -1, cur_grp = -1;
+  int cur_tok = -2;  // gate_up: the token whose x row this lane's fragments hold (-1: none)
   UnitCursor cur;
   if (r.u0 < r.u1) cur.init(gr.gpre, p.tiles, r.d0, r.u0);
   for (int u = r.u0; u < r.u1; ++u) {
@@ -804,8 +805,21 @@ __device__ void consume_units(const GemmParams& p, const Grouping& gr, const Uni
     const int base = chk(gr.base(d, e), p.P + 1, p.status);
     const int npairs = chk(gr.end(d, e), p.P + 1, p.status) - base;
     if (e != cur_e || grp != cur_grp) {
-      load_frags<KIND, GATE_UP, NBW, AQ>(p, gr.spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
-      fold = __any_sync(0xffffffffu, inv[0] != 1.f || inv[1] != 1.f);
+      // gate_up fragments are rows of x: a group with the same tokens as the
+      // last one (one token: every expert's group) needs no reload.  Checked
+      // only where the grouping is in shared memory (a cheap read).
+      bool same = false;
+      int tok = -1;
+      if (GATE_UP && gr.local) {
+        const int slot = grp * kGroup + g;
+        if (slot < npairs) tok = chk(gr.spair[chk(base + slot, p.P, p.status)], p.P, p.status) / p.topk;
+        same = __all_sync(0xffffffffu, tok == cur_tok);
+      }
+      if (!same) {
+        load_frags<KIND, GATE_UP, NBW, AQ>(p, gr.spair, grp * kGroup, base, npairs, wb0, cnt, g, t, xf, inv);
+        fold = __any_sync(0xffffffffu, inv[0] != 1.f || inv[1] != 1.f);
+        cur_tok = tok;
+      }
       cur_e = e;
       cur_grp = grp;
     }
