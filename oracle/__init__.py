@@ -6,7 +6,7 @@ library computes.  It exists only to check that library: it is imported by
 ``bench.py`` — never by the library itself, which has no CPU fallback.  It
 shares no code with the CUDA path (no kernels, headers, tables or helpers).
 
-Sources, all on the pages this build follows:
+Sources, all on the pages the library follows:
 
 * vLLM ``Mxfp4MoEMethod`` API page (quantization/mxfp4):
   ``create_weights`` fixes the byte layouts (uint8 ``w13[E, 2I, H/2]``,
