@@ -383,6 +383,19 @@ __device__ __forceinline__ void mx_quant8(float (&v)[8], uint32_t& codes, uint32
 // rounded division decides.  The bound needs 1/s and y to be normal floats:
 // scales outside [2^-126, 2^126] always divide; quotients too small for the
 // bound round to zero at both ends and in fact.
+// The e4m3 codes of fl32(v / s) by correctly rounded division: the rare
+// fallback of fp8_quant8, kept out of line so that its code does not weigh on
+// the kernels that inline the quantiser (values by value, codes returned in
+// registers).
+struct CodePair {
+  uint32_t c0, c1;
+};
+static __device__ __noinline__ CodePair fp8_codes_by_division(float v0, float v1, float v2, float v3, float v4, float v5,
+                                                             float v6, float v7, float s) {
+  return CodePair{f32x4_to_e4m3x4(__fdiv_rn(v0, s), __fdiv_rn(v1, s), __fdiv_rn(v2, s), __fdiv_rn(v3, s)),
+                  f32x4_to_e4m3x4(__fdiv_rn(v4, s), __fdiv_rn(v5, s), __fdiv_rn(v6, s), __fdiv_rn(v7, s))};
+}
+
 __device__ __forceinline__ void fp8_quant8(float (&v)[8], float s, uint32_t& c0, uint32_t& c1) {
   bool exact = !(s >= 0x1p-126f && s <= 0x1p126f);
   if (!exact) {
@@ -401,11 +414,9 @@ __device__ __forceinline__ void fp8_quant8(float (&v)[8], float s, uint32_t& c0,
     exact = c0 != f32x4_to_e4m3x4(hi[0], hi[1], hi[2], hi[3]) || c1 != f32x4_to_e4m3x4(hi[4], hi[5], hi[6], hi[7]);
   }
   if (exact) {
-    float r[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) r[q] = __fdiv_rn(v[q], s);
-    c0 = f32x4_to_e4m3x4(r[0], r[1], r[2], r[3]);
-    c1 = f32x4_to_e4m3x4(r[4], r[5], r[6], r[7]);
+    const CodePair c = fp8_codes_by_division(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], s);
+    c0 = c.c0;
+    c1 = c.c1;
   }
   uint32_t h[4];
   e4m3x4_to_f16x4(c0, h[0], h[1]);
